@@ -1,0 +1,468 @@
+"""Seeded synthetic inputs for QSA gather-GQA sparse attention.
+
+This module only *makes inputs*: ragged query rows, a paged KV cache scattered
+through a shuffled page table, and a per-row selection of cache positions.  It
+holds none of the attention arithmetic, so both the CPU oracle (through the
+tests) and the CUDA path can be fed from it without sharing any code.
+
+Layouts follow the QSASparseAttentionRaggedPaged page ("Tensor shapes"):
+
+* ``q``               ``[total_q, num_q_heads, head_dim]``
+* ``input_row_offsets`` ``[batch + 1]`` uint32
+* ``kv_blocks``       ``[num_pages, 2, num_layers, page_size, num_kv_heads, head_dim]``
+  with ``page_stride`` elements between pages (``-1`` = packed)
+* ``cache_lengths``   ``[batch]`` uint32
+* ``kv_lookup_table`` ``[batch, max_pages]`` uint32
+* ``token_indices``   ``[total_q, selection_width]`` int32, valid entries first
+* ``counts``          ``[total_q]`` int32
+
+Element storage is raw: float32 values, bfloat16 *bits* (uint16) or FP8 e4m3fn
+*bits* (uint8).  The float -> bf16 / e4m3 encodings are PyTorch's CPU casts
+(round to nearest even).
+
+Conventions this generator fixes (the pages leave them open):
+
+* Row ``t`` of sequence ``b`` sits at position ``pos = cache_lengths[b] + t``;
+  the cache already holds this step's keys, so positions ``[0, cache_lengths[b]
+  + rows_b)`` are valid and a row selects from ``[0, pos]``.
+* Axis 1 of ``kv_blocks``: index 0 holds K, index 1 holds V.
+* Cache slots that no sequence owns, the layers other than ``layer_idx``, the
+  padding between pages and one extra "poison page" are filled with NaN, and
+  table entries past a sequence's last page point at the poison page, so any
+  stray read shows up as NaN instead of a fault.
+
+Random draw order: the sequence structure (rows, cache lengths) comes from
+``default_rng(seed + 1000)`` inside the workload function; then one
+``default_rng(seed)`` draws the page permutation -> q -> per sequence K then V
+in logical order -> per row (count, indices, tail) in row order.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+from typing import Callable, List, Optional, Sequence
+
+import numpy as np
+
+DTYPES = ("f32", "bf16", "e4m3")
+
+# NaN bit patterns used to poison every cache byte no selection may read.
+_POISON = {"f32": np.uint32(0x7FC00000), "bf16": np.uint16(0x7FC0), "e4m3": np.uint8(0x7F)}
+_STORAGE = {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}
+ELEM_BYTES = {"f32": 4, "bf16": 2, "e4m3": 1}
+
+
+def encode(x: np.ndarray, dtype: str) -> np.ndarray:
+    """float32 array -> raw storage of ``dtype`` (RNE casts done by PyTorch on CPU)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if dtype == "f32":
+        return x
+    import torch
+
+    t = torch.from_numpy(x)
+    if dtype == "bf16":
+        return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    if dtype == "e4m3":
+        return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    raise ValueError(dtype)
+
+
+@dataclasses.dataclass
+class QSAInputs:
+    """One call's worth of inputs, all host numpy arrays in raw storage."""
+
+    name: str
+    dtype: str
+    out_dtype: str
+    q: np.ndarray
+    kv_flat: np.ndarray  # raw storage, num_pages * page pitch (+ nothing else)
+    kv_shape: tuple  # (num_pages, 2, num_layers, page_size, num_kv_heads, head_dim)
+    page_stride: int  # -1 when packed, else elements between pages
+    input_row_offsets: np.ndarray
+    cache_lengths: np.ndarray
+    kv_lookup_table: np.ndarray
+    max_prompt_length: int
+    max_cache_length: int
+    layer_idx: int
+    token_indices: np.ndarray
+    counts: np.ndarray
+    scale: float
+    group: int
+    poison_page: int
+    # logical (unpaged) K and V per sequence, raw storage [kv_len, nkv, D]; kept
+    # only on request so independent checks can skip the paging entirely.
+    logical_k: Optional[List[np.ndarray]] = None
+    logical_v: Optional[List[np.ndarray]] = None
+
+    @property
+    def total_q(self) -> int:
+        return int(self.q.shape[0])
+
+    @property
+    def num_q_heads(self) -> int:
+        return int(self.q.shape[1])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.q.shape[2])
+
+    @property
+    def num_kv_heads(self) -> int:
+        return int(self.kv_shape[4])
+
+    @property
+    def batch(self) -> int:
+        return int(self.cache_lengths.shape[0])
+
+    @property
+    def selection_width(self) -> int:
+        return int(self.token_indices.shape[1])
+
+    @property
+    def page_pitch(self) -> int:
+        """Elements from one page to the next."""
+        n, two, L, P, nkv, D = self.kv_shape
+        return two * L * P * nkv * D if self.page_stride == -1 else self.page_stride
+
+    def kv_view(self) -> np.ndarray:
+        """The 6-D ``kv_blocks`` view over ``kv_flat`` (strided when padded)."""
+        n, two, L, P, nkv, D = self.kv_shape
+        es = self.kv_flat.itemsize
+        strides = (self.page_pitch * es, L * P * nkv * D * es, P * nkv * D * es, nkv * D * es, D * es, es)
+        return np.lib.stride_tricks.as_strided(self.kv_flat, shape=self.kv_shape, strides=strides)
+
+    def row_sequence(self) -> np.ndarray:
+        """Sequence id of every query row (from ``input_row_offsets``)."""
+        off = self.input_row_offsets.astype(np.int64)
+        return np.repeat(np.arange(self.batch), np.diff(off))
+
+    def valid_counts(self) -> np.ndarray:
+        """``counts`` clamped to ``[0, selection_width]``."""
+        return np.clip(self.counts.astype(np.int64), 0, self.selection_width)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes the method must move: each selected K and V row once per
+        (row, kv head), plus q, the output and the valid indices and counts."""
+        ekv = ELEM_BYTES[self.dtype]
+        eo = ELEM_BYTES[self.out_dtype]
+        n = int(self.valid_counts().sum())
+        D = self.head_dim
+        return (
+            n * self.num_kv_heads * 2 * D * ekv
+            + self.total_q * self.num_q_heads * D * (ekv + eo)
+            + n * 4
+            + self.total_q * 4
+        )
+
+
+# ----------------------------------------------------------------------------
+# selection recipes (per row); each returns the valid prefix as int64
+# ----------------------------------------------------------------------------
+
+def _sel_uniform_distinct(count_rule: str) -> Callable:
+    """Distinct positions drawn uniformly from [0, pos], in random order."""
+
+    def pick(rng, pos, W, P):
+        hi = min(W, pos + 1)
+        cnt = hi if count_rule == "full" else int(rng.integers(1, hi + 1))
+        return rng.choice(pos + 1, size=cnt, replace=False).astype(np.int64)
+
+    return pick
+
+
+def _sel_local_plus_uniform(local: int = 64) -> Callable:
+    """The ``local`` positions nearest pos plus distinct uniform picks from the
+    rest of [0, pos]; count = min(W, pos + 1); sorted ascending."""
+
+    def pick(rng, pos, W, P):
+        cnt = min(W, pos + 1)
+        lo = max(0, pos - local + 1)
+        near = np.arange(lo, pos + 1, dtype=np.int64)
+        rest = cnt - near.size
+        far = rng.choice(lo, size=rest, replace=False).astype(np.int64) if rest > 0 else np.zeros(0, np.int64)
+        return np.sort(np.concatenate([far, near]))
+
+    return pick
+
+
+def _sel_block_runs(runs: int = 64, run_len: int = 64) -> Callable:
+    """``runs`` distinct runs of ``run_len`` positions with run-aligned starts,
+    always including the run that holds pos, clipped to pos; ascending."""
+
+    def pick(rng, pos, W, P):
+        last = pos // run_len
+        n_runs = min(runs, last + 1)
+        others = rng.choice(last, size=n_runs - 1, replace=False) if n_runs > 1 else np.zeros(0, np.int64)
+        starts = np.sort(np.concatenate([others.astype(np.int64), [last]])) * run_len
+        idx = (starts[:, None] + np.arange(run_len)[None, :]).reshape(-1)
+        return idx[idx <= pos].astype(np.int64)
+
+    return pick
+
+
+def _tail_const(v: int) -> Callable:
+    def fill(rng, n, kv_len):
+        return np.full(n, v, dtype=np.int64)
+
+    return fill
+
+
+def _tail_out_of_range(rng, n, kv_len):
+    """Random ints outside [0, kv_len): half >= kv_len, half negative."""
+    hi = rng.integers(kv_len, 2**31 - 1, size=n, dtype=np.int64)
+    lo = rng.integers(-(2**31), 0, size=n, dtype=np.int64)
+    return np.where(rng.random(n) < 0.5, hi, lo)
+
+
+# ----------------------------------------------------------------------------
+# the generic builder
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class WorkloadSpec:
+    name: str
+    seed: int
+    rows: Sequence[int]  # new query rows per sequence
+    cache_lengths: Sequence[int]
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_layers: int
+    layer_idx: int
+    dtype: str
+    out_dtype: str
+    selection_width: int
+    select: Callable
+    tail: Callable
+    page_pad: Optional[int] = None  # extra elements between pages (None = packed)
+    scale: Optional[float] = None
+
+    def build(self, keep_logical: bool = False, rng=None) -> QSAInputs:
+        return _build(self, keep_logical, rng)
+
+
+def assemble(name: str, dtype: str, out_dtype: str, q: np.ndarray, logical_k: Sequence[np.ndarray],
+             logical_v: Sequence[np.ndarray], rows: Sequence[int], cache_lengths: Sequence[int],
+             page_size: int, num_layers: int, layer_idx: int, token_indices: np.ndarray,
+             counts: np.ndarray, scale: float, page_perm: Optional[np.ndarray] = None,
+             page_pad: Optional[int] = None, keep_logical: bool = False) -> QSAInputs:
+    """Pages logical per-sequence K/V (raw storage ``[kv_len_b, nkv, D]``) into
+    ``kv_blocks`` through the page assignment ``page_perm`` (identity when None)
+    and wraps everything as a :class:`QSAInputs`."""
+    B = len(rows)
+    rows = np.asarray(rows, dtype=np.int64)
+    cache = np.asarray(cache_lengths, dtype=np.int64)
+    total_q, nq, D = q.shape
+    nkv = int(logical_k[0].shape[1]) if B else 1
+    P, L = int(page_size), int(num_layers)
+    assert nq % nkv == 0 and 0 <= layer_idx < L
+    kv_len = cache + rows
+    for b in range(B):
+        assert logical_k[b].shape == (kv_len[b], nkv, D) and logical_v[b].shape == (kv_len[b], nkv, D)
+    npages = -(-kv_len // P)
+    total_pages = int(npages.sum())
+    poison_page = total_pages
+    num_pages = total_pages + 1
+    max_pages = max(1, int(npages.max()) if B else 1)
+    perm = np.arange(total_pages) if page_perm is None else np.asarray(page_perm)
+    assert perm.shape == (total_pages,)
+    table = np.full((B, max_pages), poison_page, dtype=np.uint32)
+    start = 0
+    for b in range(B):
+        table[b, : npages[b]] = perm[start : start + npages[b]]
+        start += npages[b]
+
+    packed = 2 * L * P * nkv * D
+    page_stride = -1 if page_pad is None else packed + int(page_pad)
+    pitch = packed if page_stride == -1 else page_stride
+    kv_flat = np.empty(num_pages * pitch, dtype=_STORAGE[dtype])
+    kv_flat.view(_POISON[dtype].dtype)[:] = _POISON[dtype]
+    es = kv_flat.itemsize
+    kv6 = np.lib.stride_tricks.as_strided(
+        kv_flat,
+        shape=(num_pages, 2, L, P, nkv, D),
+        strides=(pitch * es, L * P * nkv * D * es, P * nkv * D * es, nkv * D * es, D * es, es),
+    )
+    for b in range(B):
+        n = int(kv_len[b])
+        kb, vb = logical_k[b], logical_v[b]
+        full = n // P
+        pages = table[b, : npages[b]].astype(np.int64)
+        if full:
+            kv6[pages[:full], 0, layer_idx] = kb[: full * P].reshape(full, P, nkv, D)
+            kv6[pages[:full], 1, layer_idx] = vb[: full * P].reshape(full, P, nkv, D)
+        rem = n - full * P
+        if rem:
+            kv6[pages[full], 0, layer_idx, :rem] = kb[full * P :]
+            kv6[pages[full], 1, layer_idx, :rem] = vb[full * P :]
+
+    offsets = np.zeros(B + 1, dtype=np.uint32)
+    offsets[1:] = np.cumsum(rows)
+    return QSAInputs(
+        name=name,
+        dtype=dtype,
+        out_dtype=out_dtype,
+        q=np.ascontiguousarray(q),
+        kv_flat=kv_flat,
+        kv_shape=(num_pages, 2, L, P, nkv, D),
+        page_stride=page_stride,
+        input_row_offsets=offsets,
+        cache_lengths=cache.astype(np.uint32),
+        kv_lookup_table=table,
+        max_prompt_length=int(rows.max()) if B else 0,
+        max_cache_length=int(cache.max()) if B else 0,
+        layer_idx=int(layer_idx),
+        token_indices=np.ascontiguousarray(token_indices, dtype=np.int32),
+        counts=np.ascontiguousarray(counts, dtype=np.int32),
+        scale=float(scale),
+        group=nq // nkv,
+        poison_page=poison_page,
+        logical_k=list(logical_k) if keep_logical else None,
+        logical_v=list(logical_v) if keep_logical else None,
+    )
+
+
+def _build(spec: WorkloadSpec, keep_logical: bool, rng) -> QSAInputs:
+    if rng is None:
+        rng = np.random.default_rng(spec.seed)
+    B = len(spec.rows)
+    rows = np.asarray(spec.rows, dtype=np.int64)
+    cache = np.asarray(spec.cache_lengths, dtype=np.int64)
+    nq, nkv, D, P = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.page_size
+    W = spec.selection_width
+    kv_len = cache + rows
+    total_pages = int((-(-kv_len // P)).sum())
+    perm = rng.permutation(total_pages)
+
+    total_q = int(rows.sum())
+    q = encode(rng.standard_normal((total_q, nq, D), dtype=np.float32), spec.dtype)
+    logical_k, logical_v = [], []
+    for b in range(B):
+        n = int(kv_len[b])
+        logical_k.append(encode(rng.standard_normal((n, nkv, D), dtype=np.float32), spec.dtype))
+        logical_v.append(encode(rng.standard_normal((n, nkv, D), dtype=np.float32), spec.dtype))
+
+    token_indices = np.empty((total_q, W), dtype=np.int32)
+    counts = np.empty(total_q, dtype=np.int32)
+    r = 0
+    for b in range(B):
+        for t in range(int(rows[b])):
+            pos = int(cache[b]) + t
+            sel = spec.select(rng, pos, W, P)
+            assert sel.size <= W
+            counts[r] = sel.size
+            token_indices[r, : sel.size] = sel
+            if sel.size < W:
+                token_indices[r, sel.size :] = spec.tail(rng, W - sel.size, int(kv_len[b]))
+            r += 1
+
+    scale = spec.scale if spec.scale is not None else 1.0 / math.sqrt(D)
+    return assemble(spec.name, spec.dtype, spec.out_dtype, q, logical_k, logical_v, rows, cache, P,
+                    spec.num_layers, spec.layer_idx, token_indices, counts, scale, page_perm=perm,
+                    page_pad=spec.page_pad, keep_logical=keep_logical)
+
+
+# ----------------------------------------------------------------------------
+# the five workloads (full size by default; keyword overrides shrink them for
+# parity tests while keeping each one's structure)
+# ----------------------------------------------------------------------------
+
+def tiny_ragged(seed: int = 0) -> WorkloadSpec:
+    """fp32, batch 2, rows [3,5] on cache [17,40], 4 q heads on 1 kv head,
+    head_dim 64, page 16, 2 layers (layer 1), packed permuted pages, width 8,
+    counts U[1, min(8, pos+1)], distinct U[0,pos], tail 999999."""
+    return WorkloadSpec(
+        name="tiny_ragged_fp32", seed=seed, rows=[3, 5], cache_lengths=[17, 40],
+        num_q_heads=4, num_kv_heads=1, head_dim=64, page_size=16, num_layers=2, layer_idx=1,
+        dtype="f32", out_dtype="f32", selection_width=8,
+        select=_sel_uniform_distinct("uniform"), tail=_tail_const(999999),
+    )
+
+
+def bf16_decode(seed: int = 2, batch: int = 64, cache_range=(1024, 8192), width: int = 2048,
+                num_layers: int = 4, layer_idx: int = 2) -> WorkloadSpec:
+    """bf16 decode: one new token per sequence, cache U[1024, 8192], 32 q heads
+    on 8 kv heads, head_dim 128, page 128, 4 layers (layer 2), width 2048,
+    counts = min(2048, pos+1), distinct U[0,pos] in random order, tail -1."""
+    rng = np.random.default_rng(seed + 1000)
+    cache = rng.integers(cache_range[0], cache_range[1] + 1, size=batch)
+    return WorkloadSpec(
+        name="bf16_decode", seed=seed, rows=[1] * batch, cache_lengths=cache.tolist(),
+        num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=128, num_layers=num_layers,
+        layer_idx=layer_idx, dtype="bf16", out_dtype="bf16", selection_width=width,
+        select=_sel_uniform_distinct("full"), tail=_tail_const(-1),
+    )
+
+
+def bf16_chunked_prefill(seed: int = 3, rows=(512, 1024, 256, 2048), cache=(0, 4096, 16384, 8192),
+                         width: int = 2048) -> WorkloadSpec:
+    """bf16 chunked prefill: rows [512,1024,256,2048] on cache [0,4096,16384,8192],
+    64 q heads on 8 kv heads, head_dim 128, page 64, 1 layer, width 2048,
+    counts = min(2048, pos+1); the 64 positions nearest pos plus distinct
+    uniform picks from the rest, sorted ascending; tail -1."""
+    return WorkloadSpec(
+        name="bf16_chunked_prefill", seed=seed, rows=list(rows), cache_lengths=list(cache),
+        num_q_heads=64, num_kv_heads=8, head_dim=128, page_size=64, num_layers=1, layer_idx=0,
+        dtype="bf16", out_dtype="bf16", selection_width=width,
+        select=_sel_local_plus_uniform(64), tail=_tail_const(-1),
+    )
+
+
+def bf16_long_decode(seed: int = 4, batch: int = 32, cache_range=(65536, 131072), runs: int = 64) -> WorkloadSpec:
+    """bf16 long-context decode: batch 32, cache U[65536, 131072], 16 q heads on
+    1 kv head, head_dim 128, page 64, 1 layer; selection = 64 distinct
+    page-aligned runs of 64 (the run holding pos always in, clipped to pos),
+    ascending; width 4096; tail -1."""
+    rng = np.random.default_rng(seed + 1000)
+    cache_l = rng.integers(cache_range[0], cache_range[1] + 1, size=batch)
+    return WorkloadSpec(
+        name="bf16_long_decode", seed=seed, rows=[1] * batch, cache_lengths=cache_l.tolist(),
+        num_q_heads=16, num_kv_heads=1, head_dim=128, page_size=64, num_layers=1, layer_idx=0,
+        dtype="bf16", out_dtype="bf16", selection_width=runs * 64,
+        select=_sel_block_runs(runs, 64), tail=_tail_const(-1),
+    )
+
+
+def fp8_mixed(seed: int = 5, n_decode: int = 120, n_prefill: int = 8, prefill_rows: int = 512,
+              cache_range=(256, 32768), width: int = 1024) -> WorkloadSpec:
+    """FP8 e4m3 mixed batch: 120 decode sequences + 8 prefill sequences of 512
+    rows placed by a seeded permutation, cache log-uniform in [256, 32768],
+    32 q heads on 4 kv heads, head_dim 128, page 128, 2 layers (layer 0),
+    page_stride = packed page + 4096 elements, bf16 output, width 1024,
+    counts U[1, min(1024, pos+1)], distinct U[0,pos], tail random
+    out-of-range ints."""
+    rng = np.random.default_rng(seed + 1000)
+    kinds = np.array([1] * n_decode + [prefill_rows] * n_prefill)
+    rows = kinds[rng.permutation(kinds.size)]
+    lo, hi = math.log(cache_range[0]), math.log(cache_range[1])
+    cache = np.floor(np.exp(rng.uniform(lo, hi, size=kinds.size))).astype(np.int64)
+    return WorkloadSpec(
+        name="fp8_mixed", seed=seed, rows=rows.tolist(), cache_lengths=cache.tolist(),
+        num_q_heads=32, num_kv_heads=4, head_dim=128, page_size=128, num_layers=2, layer_idx=0,
+        dtype="e4m3", out_dtype="bf16", selection_width=width,
+        select=_sel_uniform_distinct("uniform"), tail=_tail_out_of_range, page_pad=4096,
+    )
+
+
+WORKLOADS = {
+    "tiny_ragged_fp32": tiny_ragged,
+    "bf16_decode": bf16_decode,
+    "bf16_chunked_prefill": bf16_chunked_prefill,
+    "bf16_long_decode": bf16_long_decode,
+    "fp8_mixed": fp8_mixed,
+}
+
+
+def small_variants() -> dict:
+    """Reduced copies of the four large workloads: each keeps its dtype, head
+    layout, page size, selection recipe and tail rule, at sizes the oracle
+    finishes in seconds while still spanning several 64-key tiles and a
+    ragged last tile."""
+    return {
+        "bf16_decode_small": bf16_decode(seed=12, batch=6, cache_range=(150, 900), width=512),
+        "bf16_prefill_small": bf16_chunked_prefill(seed=13, rows=(40, 9, 23), cache=(0, 300, 77), width=256),
+        "bf16_long_decode_small": bf16_long_decode(seed=14, batch=3, cache_range=(3000, 9000), runs=12),
+        "fp8_mixed_small": fp8_mixed(seed=15, n_decode=5, n_prefill=2, prefill_rows=17,
+                                     cache_range=(40, 1500), width=200),
+    }

@@ -1,0 +1,214 @@
+/*
+ * CPU oracle for QSA gather-GQA sparse attention over a ragged, paged KV cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the slow, obviously correct
+ * definition the CUDA path is checked against.  Only the tests, the smoke
+ * check and the bench's CPU-baseline leg may load it; the product library
+ * never links or calls it, and it shares no code, header or table with it.
+ *
+ * What it computes (QSASparseAttentionRaggedPaged, "Gather-GQA over the token
+ * indices a QSA selection names", with the tensor shapes listed on that page):
+ *
+ *   for each query row r of sequence b (input_row_offsets[b] <= r < [b+1]),
+ *   each kv head h and each of the `group` query heads i that share it:
+ *     n   = min(max(counts[r], 0), selection_width)   valid entries come first
+ *     p_j = token_indices[r, j]                        j < n, never read past n
+ *     K_j = kv_blocks[page(b, p_j), 0, layer_idx, p_j % page_size, h, :]
+ *     V_j = kv_blocks[page(b, p_j), 1, layer_idx, p_j % page_size, h, :]
+ *     page(b, p) = kv_lookup_table[b, p / page_size], pages page_stride
+ *                  elements apart (or packed when page_stride == -1)
+ *     s_j = scale * sum_d q[r, h*group + i, d] * K_j[d]
+ *     out[r, h*group + i, :] = sum_j softmax(s)_j * V_j
+ *
+ * Everything is float64; inputs are decoded exactly from their storage type
+ * (IEEE binary32, bfloat16, or scale-free FP8 e4m3fn).  Readings taken where
+ * the page is silent: axis 1 of kv_blocks is K at 0 and V at 1; query head
+ * h*group+i uses kv head h; no causal mask is applied (the selection alone
+ * decides what is attended); an empty selection gives a zero row; an index
+ * outside [0, cache_lengths[b] + rows_b) inside the valid prefix is a
+ * precondition violation and makes the oracle fail.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_E4M3 = 2 };
+
+enum {
+  ORACLE_OK = 0,
+  ORACLE_BAD_ARGUMENT = 1,
+  ORACLE_INDEX_OUT_OF_RANGE = 2,
+  ORACLE_BAD_PAGE = 3,
+  ORACLE_BAD_ROW = 4,
+  ORACLE_NO_MEMORY = 5
+};
+
+/* IEEE binary32 element -> double (exact). */
+static double decode_f32(const void* base, int64_t i) {
+  float f;
+  memcpy(&f, (const unsigned char*)base + 4 * i, 4);
+  return (double)f;
+}
+
+/* bfloat16 element -> double (exact): the upper 16 bits of a binary32. */
+static double decode_bf16(const void* base, int64_t i) {
+  uint16_t h;
+  uint32_t w;
+  float f;
+  memcpy(&h, (const unsigned char*)base + 2 * i, 2);
+  w = (uint32_t)h << 16;
+  memcpy(&f, &w, 4);
+  return (double)f;
+}
+
+/* FP8 e4m3fn element -> double (exact), from the format's definition:
+ * 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,
+ * S.1111.111 is NaN, exponent 0 is subnormal (m/8 * 2^-6). */
+static double decode_e4m3(const void* base, int64_t i) {
+  unsigned b = ((const unsigned char*)base)[i];
+  int sign = (b >> 7) & 1;
+  int e = (b >> 3) & 15;
+  int m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m / 8.0, -6);
+  else
+    v = ldexp(1.0 + (double)m / 8.0, e - 7);
+  return sign ? -v : v;
+}
+
+static double decode(int dtype, const void* base, int64_t i) {
+  if (dtype == ORACLE_F32) return decode_f32(base, i);
+  if (dtype == ORACLE_BF16) return decode_bf16(base, i);
+  return decode_e4m3(base, i);
+}
+
+/*
+ * Computes the attention output for the query rows listed in `rows`
+ * (n_rows of them) into out[n_rows, num_q_heads, head_dim] (float64).
+ * All arrays are host memory, contiguous, row-major, shaped as the
+ * QSASparseAttentionRaggedPaged page lists; kv_blocks pages are `page_stride`
+ * elements apart (-1 = packed).  On an index error *bad_row receives the row.
+ */
+int qsa_oracle_sparse_attention(
+    double* out, const int64_t* rows, int64_t n_rows,
+    const void* q, int q_dtype, int64_t total_q, int64_t num_q_heads, int64_t head_dim,
+    const uint32_t* input_row_offsets, int64_t batch,
+    const void* kv_blocks, int kv_dtype, int64_t num_pages, int64_t page_stride,
+    int64_t num_layers, int64_t page_size, int64_t num_kv_heads,
+    const uint32_t* cache_lengths, const uint32_t* kv_lookup_table, int64_t max_pages,
+    int64_t layer_idx, const int32_t* token_indices, int64_t selection_width,
+    const int32_t* counts, double scale, int64_t group, int64_t* bad_row) {
+  int64_t packed_page, pitch, ri;
+  double* s;
+  double* w;
+
+  *bad_row = -1;
+  if (group <= 0 || num_kv_heads <= 0 || num_q_heads != group * num_kv_heads) return ORACLE_BAD_ARGUMENT;
+  if (layer_idx < 0 || layer_idx >= num_layers) return ORACLE_BAD_ARGUMENT;
+  if (q_dtype != kv_dtype || q_dtype < 0 || q_dtype > 2) return ORACLE_BAD_ARGUMENT;
+  packed_page = 2 * num_layers * page_size * num_kv_heads * head_dim;
+  if (page_stride != -1 && page_stride < packed_page) return ORACLE_BAD_ARGUMENT;
+  pitch = (page_stride == -1) ? packed_page : page_stride;
+
+  s = (double*)malloc(sizeof(double) * (size_t)(selection_width > 0 ? selection_width : 1));
+  w = (double*)malloc(sizeof(double) * (size_t)(selection_width > 0 ? selection_width : 1));
+  if (!s || !w) {
+    free(s);
+    free(w);
+    return ORACLE_NO_MEMORY;
+  }
+
+  for (ri = 0; ri < n_rows; ++ri) {
+    int64_t r = rows[ri];
+    int64_t b = -1, k, kv_len, n, h, i, j, d;
+
+    if (r < 0 || r >= total_q) goto bad_row_exit;
+    /* the sequence that owns row r: input_row_offsets[b] <= r < input_row_offsets[b+1] */
+    for (k = 0; k < batch; ++k)
+      if ((int64_t)input_row_offsets[k] <= r && r < (int64_t)input_row_offsets[k + 1]) {
+        b = k;
+        break;
+      }
+    if (b < 0) goto bad_row_exit;
+    /* the cache already holds this step's rows of sequence b */
+    kv_len = (int64_t)cache_lengths[b] + ((int64_t)input_row_offsets[b + 1] - (int64_t)input_row_offsets[b]);
+
+    n = counts[r];
+    if (n < 0) n = 0;
+    if (n > selection_width) n = selection_width;
+
+    for (h = 0; h < num_kv_heads; ++h) {
+      for (i = 0; i < group; ++i) {
+        int64_t head = h * group + i;
+        int64_t q_off = (r * num_q_heads + head) * head_dim;
+        double* o = out + (ri * num_q_heads + head) * head_dim;
+        double m = -INFINITY, z = 0.0;
+
+        for (d = 0; d < head_dim; ++d) o[d] = 0.0;
+        if (n == 0) continue; /* empty selection: zero row */
+
+        /* scores s_j = scale * q . K_j over the valid prefix only */
+        for (j = 0; j < n; ++j) {
+          int64_t p = token_indices[r * selection_width + j];
+          int64_t logical_page, page, slot, k_off;
+          double dot = 0.0;
+          if (p < 0 || p >= kv_len) {
+            *bad_row = r;
+            free(s);
+            free(w);
+            return ORACLE_INDEX_OUT_OF_RANGE;
+          }
+          logical_page = p / page_size;
+          slot = p % page_size;
+          if (logical_page >= max_pages) goto bad_page_exit;
+          page = (int64_t)kv_lookup_table[b * max_pages + logical_page];
+          if (page >= num_pages) goto bad_page_exit;
+          k_off = page * pitch + ((0 * num_layers + layer_idx) * page_size + slot) * num_kv_heads * head_dim +
+                  h * head_dim;
+          for (d = 0; d < head_dim; ++d) dot += decode(q_dtype, q, q_off + d) * decode(kv_dtype, kv_blocks, k_off + d);
+          s[j] = scale * dot;
+        }
+        /* softmax over the n scores (max-subtracted, natural exponent) */
+        for (j = 0; j < n; ++j)
+          if (s[j] > m || isnan(s[j])) m = s[j];
+        for (j = 0; j < n; ++j) {
+          w[j] = exp(s[j] - m);
+          z += w[j];
+        }
+        /* out = sum_j softmax_j * V_j */
+        for (j = 0; j < n; ++j) {
+          int64_t p = token_indices[r * selection_width + j];
+          int64_t page = (int64_t)kv_lookup_table[b * max_pages + p / page_size];
+          int64_t v_off = page * pitch +
+                          ((1 * num_layers + layer_idx) * page_size + p % page_size) * num_kv_heads * head_dim +
+                          h * head_dim;
+          double a = w[j] / z;
+          for (d = 0; d < head_dim; ++d) o[d] += a * decode(kv_dtype, kv_blocks, v_off + d);
+        }
+      }
+    }
+    continue;
+  bad_page_exit:
+    *bad_row = r;
+    free(s);
+    free(w);
+    return ORACLE_BAD_PAGE;
+  bad_row_exit:
+    *bad_row = r;
+    free(s);
+    free(w);
+    return ORACLE_BAD_ROW;
+  }
+  free(s);
+  free(w);
+  return ORACLE_OK;
+}
+
+/* Decodes `n` elements of storage type `dtype` to float64 (exact). */
+void qsa_oracle_decode(double* out, const void* src, int dtype, int64_t n) {
+  int64_t i;
+  for (i = 0; i < n; ++i) out[i] = decode(dtype, src, i);
+}
