@@ -1,0 +1,357 @@
+#!/usr/bin/env python3
+"""Throughput of QSA gather-GQA sparse attention over a ragged, paged KV cache.
+
+A step is one call of the whole hot path (row -> sequence lookup, selection
+read, page translation, K/V gather, online softmax, split-K combine, output)
+over one batch of the bf16 decode workload: 64 sequences with one new token
+each, cache lengths U[1024, 8192], 32 query heads on 8 kv heads, head_dim 128,
+page 128, 4 layers (layer 2), selection width 2048.  Inputs are synthetic and
+seeded.  The cache is 4.8 GB and each step gathers ~0.52 GB of random rows;
+L2 is flushed (a 2x-L2 buffer is written) before every timed step.
+
+One JSON line on stdout (rank 0).  ``--impl reference`` times the float64 CPU
+oracle on a bounded sample of the same workload instead.  Under torchrun each
+rank runs its own replica (the op shards with no exchange), timings are
+max-reduced and ``value`` is the aggregate over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse attn query-tokens/s per layer; effective HBM GB/s (% of GB300 peak)"
+UNIT = "query-tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="bf16_decode")
+    ap.add_argument("--kernel", type=int, default=0, help="force 1 CUDA-core / 2 tensor-core kernel")
+    ap.add_argument("--splits", type=int, default=0, help="force CTAs per (row, kv head)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the CPU baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "index_gathered_sparse_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, n), "rb") as f:
+            h.update(n.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+        e = rec.get(workload)
+        if e and e.get("kernel_hash") == kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        cmd = ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "200"]
+        if gpu_id:
+            cmd += ["-i", gpu_id]
+        try:
+            self.p = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.p = None
+
+    def stop(self) -> dict:
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.p.terminate()
+        out, _ = self.p.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def sample_rows(total_q: int):
+    """A fixed spread of rows used by the CPU measurements."""
+    import numpy as np
+
+    order = np.random.default_rng(123).permutation(total_q)
+    return order.astype(np.int64)
+
+
+def cpu_oracle_rate(x, seconds: float, rows_per_call: int = 1):
+    """Rows per second of the float64 oracle on this host, one thread."""
+    import oracle
+
+    rows = sample_rows(x.total_q)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        sel = rows[done % rows.size: done % rows.size + rows_per_call]
+        oracle.sparse_attention(x, sel)
+        done += sel.size
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return done / el, done, el
+
+
+def run_reference(args, x, rank, world):
+    """The reference arm: the float64 CPU oracle timed on the host cores."""
+    import numpy as np
+
+    import oracle
+
+    if rank != 0:
+        return
+    oracle.build()
+    rows = sample_rows(x.total_q)
+    t0 = time.perf_counter()
+    oracle.sparse_attention(x, rows[:1])
+    per_row = time.perf_counter() - t0
+    rows_per_step = max(1, int(round(0.5 / max(per_row, 1e-6))))
+    k = 0
+
+    def step():
+        nonlocal k
+        sel = np.take(rows, np.arange(k, k + rows_per_step), mode="wrap")
+        oracle.sparse_attention(x, sel)
+        k += rows_per_step
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    el = time.perf_counter() - t0
+    value = rows_per_step * args.steps / el
+    sample = f"{rows_per_step} query row(s) of the {x.name} workload per step (all heads, full selections)"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy)", "config": workload_config(x),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(x) -> dict:
+    return {
+        "workload": x.name, "batch": x.batch, "total_q": x.total_q, "num_q_heads": x.num_q_heads,
+        "num_kv_heads": x.num_kv_heads, "group": x.group, "head_dim": x.head_dim, "page_size": x.kv_shape[3],
+        "num_layers": x.kv_shape[2], "layer_idx": x.layer_idx, "selection_width": x.selection_width,
+        "cache_dtype": x.dtype, "out_dtype": x.out_dtype,
+        "l2": "flushed (2x L2 buffer written) before every timed step",
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    import numpy as np  # noqa: F401
+
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    spec = wl.WORKLOADS[args.workload]()
+    if world > 1:
+        spec.seed += 100 * rank  # independent replicas
+    t_gen = time.perf_counter()
+    x = spec.build()
+    print(f"[bench] rank {rank}: built {x.name} in {time.perf_counter() - t_gen:.1f}s", file=sys.stderr)
+
+    if args.impl == "reference":
+        run_reference(args, x, rank, world)
+        return
+
+    import torch
+
+    from index_gathered_sparse_gb300 import binding as B
+    from index_gathered_sparse_gb300 import build as libbuild
+
+    libbuild.build()
+    if world > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = wl.to_torch(x, dev)
+    code = {"f32": B.QSA_F32, "bf16": B.QSA_BF16, "e4m3": B.QSA_F8E4M3}[x.dtype]
+    plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, x.selection_width, x.group,
+                      kernel=args.kernel, splits=args.splits)
+    B.qsa_reserve_workspace(plan["workspace_bytes"])
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def call():
+        B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_id = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+    except Exception:
+        gpu_id = None
+    sampler = ClockSampler(gpu_id)
+    # warm-up: at least W steps and at least ~1 s so the clock samples see load
+    t0 = time.perf_counter()
+    n_warm = 0
+    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < 1.0:
+        flush_buf.fill_(n_warm & 0xFF)
+        call()
+        n_warm += 1
+        if n_warm % 64 == 0:
+            torch.cuda.synchronize()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_buf.fill_(i & 0xFF)
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    barrier()
+    per_step = [a.elapsed_time(b) for a, b in ev]  # ms
+    clocks = sampler.stop()
+    t_rank = sum(per_step)
+    if world > 1:
+        t = torch.tensor([t_rank], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        t_rank = float(t.item())
+    ms_per_step = t_rank / args.steps
+    value = world * x.total_q / (ms_per_step / 1e3)
+
+    flags = B.qsa_read_device_status(clear=True)
+    if flags:
+        print(f"[bench] warning: device status word {flags:#x}", file=sys.stderr)
+
+    # ---- end to end: per-step inputs from pinned host memory, output back ----
+    e2e = None
+    if not args.no_e2e:
+        host = {k: d[k].cpu().pin_memory() for k in
+                ("q", "input_row_offsets", "cache_lengths", "kv_lookup_table", "token_indices", "counts")}
+        out_host = torch.empty(d["output"].shape, dtype=d["output"].dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_host.numel() * out_host.element_size()
+
+        def e2e_step():
+            for k, t in host.items():
+                d[k].copy_(t, non_blocking=True)
+            call()
+            out_host.copy_(d["output"], non_blocking=True)
+
+        for i in range(3):
+            flush_buf.fill_(i)
+            e2e_step()
+        barrier()
+        n_e2e = max(3, min(args.steps, 100))
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_e2e)]
+        for i in range(n_e2e):
+            flush_buf.fill_(i & 0xFF)
+            evs[i][0].record(stream)
+            e2e_step()
+            evs[i][1].record(stream)
+        barrier()
+        te = sum(a.elapsed_time(b) for a, b in evs)
+        if world > 1:
+            t = torch.tensor([te], device=dev, dtype=torch.float64)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            te = float(t.item())
+        e2e = {"value": world * x.total_q / (te / n_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    alg_bytes = x.algorithmic_bytes()
+    peak, peak_src = measured_peaks()
+    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": recorded_traffic(x.name), "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs copy)",
+                "kernel": "qsa mma_kernel" if plan["kernel"] == 2 else "qsa simt_kernel",
+                "algorithmic_bytes_per_launch": alg_bytes}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        rate, rows, el = cpu_oracle_rate(x, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{rows} query rows of {x.name} (all heads, full selections) in {el:.1f}s, one thread"}
+
+    if rank == 0:
+        cfg = workload_config(x)
+        cfg.update({"kernel": plan["kernel"], "splits": plan["splits"], "ctas": plan["ctas"],
+                    "parallelism": f"replicas x{world}"})
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": x.dtype, "data": "synthetic (seeded numpy)", "config": cfg,
+            "effective_gbs": achieved, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "clocks": clocks, "device_status": flags,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * qsa.h - C ABI of libqsa: QSA gather-GQA sparse attention over a ragged,
+ * paged KV cache, as hand-written CUDA kernels for GB300 (sm_103a).
+ *
+ * The operation is the one the MAX kernel page "QSASparseAttentionRaggedPaged"
+ * documents ("Gather-GQA over the token indices a QSA selection names"; its
+ * "Tensor shapes" list, the `execute` method's parameters and arguments, and
+ * its "Raises" clause):
+ *
+ *   for each query row r of sequence b (input_row_offsets[b] <= r < [b+1]),
+ *   each kv head h in [0, num_kv_heads) and each i in [0, group):
+ *     n   = min(max(counts[r], 0), selection_width)
+ *     p_j = token_indices[r, j]  for j < n       (entries at or past counts
+ *                                                 are never read)
+ *     K_j = kv_blocks[page, 0, layer_idx, p_j % page_size, h, :]
+ *     V_j = kv_blocks[page, 1, layer_idx, p_j % page_size, h, :]
+ *           with page = kv_lookup_table[b, p_j / page_size]
+ *     output[r, h*group + i, :] = softmax_j(scale * q[r, h*group+i, :] . K_j) . V_j
+ *
+ * Conventions the page leaves open and this library fixes:
+ *   - axis 1 of kv_blocks is K at index 0 and V at index 1;
+ *   - query head h*group+i reads kv head h (consecutive query heads share);
+ *   - no causal mask: exactly the listed positions are attended;
+ *   - n == 0 (counts <= 0) writes a zero row; counts > selection_width is
+ *     clamped to selection_width; a repeated index is its own softmax term;
+ *   - a position outside [0, cache_lengths[b] + rows_b) inside the valid
+ *     prefix (or a page-table entry >= num_pages) is skipped and recorded in
+ *     the library's device status word (see qsa_read_device_status); it is
+ *     never dereferenced;
+ *   - FP8 is e4m3fn and scale-free: stored bytes are the values themselves.
+ *
+ * Memory, ownership, errors:
+ *   - every qsa_tensor `data` is a DEVICE pointer on the current CUDA device,
+ *     contiguous row-major (kv_blocks: its page axis is `page_stride`
+ *     elements apart); the caller owns every buffer and the stream, and must
+ *     keep them alive until the work enqueued on `stream` has finished.
+ *   - calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream).  No call reads device memory on the host, synchronises
+ *     or copies device->host, so they can be captured in a CUDA graph once the
+ *     split-K workspace is sized (qsa_reserve_workspace).
+ *   - argument problems are reported before anything is launched, as a
+ *     non-zero qsa_status ("Raises: Error if the operand shapes disagree with
+ *     the parameters"); nothing falls back to another implementation.
+ */
+#ifndef QSA_H_
+#define QSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QSA_API __attribute__((visibility("default")))
+#else
+#define QSA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element types.  QSA_F8E4M3 is FP8 e4m3fn (bias 7, no infinities, max 448). */
+typedef enum qsa_dtype {
+  QSA_F32 = 0,
+  QSA_BF16 = 1,
+  QSA_F8E4M3 = 2,
+  QSA_U32 = 3,
+  QSA_I32 = 4
+} qsa_dtype;
+
+/* A tensor descriptor: device pointer, element type (qsa_dtype), rank and
+ * shape.  Unused trailing shape entries are ignored. */
+typedef struct qsa_tensor {
+  void* data;
+  int32_t dtype;
+  int32_t ndim;
+  int64_t shape[6];
+} qsa_tensor;
+
+typedef enum qsa_status {
+  QSA_OK = 0,
+  QSA_ERR_NULL = 1,        /* a needed pointer is NULL */
+  QSA_ERR_SHAPE = 2,       /* ranks or extents disagree with each other or with group */
+  QSA_ERR_DTYPE = 3,       /* an operand has the wrong element type */
+  QSA_ERR_UNSUPPORTED = 4, /* a legal combination this build has no kernel for */
+  QSA_ERR_ARG = 5,         /* a scalar argument is out of range (layer_idx, page_stride, ...) */
+  QSA_ERR_CUDA = 6         /* a CUDA runtime call failed (launch, allocation) */
+} qsa_status;
+
+/* Bits of the device status word. */
+#define QSA_STATUS_BAD_INDEX 1u /* a position inside counts outside [0, kv_len) */
+#define QSA_STATUS_BAD_PAGE 2u  /* p / page_size >= max_pages or a table entry >= num_pages */
+#define QSA_STATUS_BAD_ROW 4u   /* a query row owned by no sequence (bad input_row_offsets) */
+
+/*
+ * qsa_sparse_attention_ragged_paged - one layer of QSA sparse attention.
+ *
+ *   output            [total_q, num_q_heads, head_dim]  F32 or BF16, written
+ *   q                 [total_q, num_q_heads, head_dim]  same type as kv_blocks
+ *   input_row_offsets [batch + 1]                       U32, ragged query offsets
+ *                     (nondecreasing, [0] == 0, [batch] == total_q)
+ *   kv_blocks         [num_pages, 2, num_layers, page_size, num_kv_heads, head_dim]
+ *                     F32, BF16 or F8E4M3; read only
+ *   page_stride       elements from one page to the next; -1 = packed
+ *                     (2*num_layers*page_size*num_kv_heads*head_dim);
+ *                     otherwise >= that packed size
+ *   cache_lengths     [batch]              U32, keys cached per sequence before
+ *                     this step; the cache already holds this step's rows, so
+ *                     sequence b has cache_lengths[b] + rows_b valid positions
+ *   kv_lookup_table   [batch, max_pages]   U32, logical page -> physical page
+ *   max_prompt_length host scalar: max new rows of any sequence (a hint only)
+ *   max_cache_length  host scalar: max cache_lengths entry (a hint only)
+ *   layer_idx         layer of kv_blocks to read, < num_layers
+ *   token_indices     [total_q, selection_width] I32, positions within the
+ *                     row's own sequence, valid entries first
+ *   counts            [total_q]            I32, valid entries per row
+ *   scale             multiplies q.K before the softmax
+ *   group             query heads per kv head (num_q_heads == group*num_kv_heads)
+ *   stream            cudaStream_t to enqueue on
+ *
+ * Kernel coverage: output F32 or BF16; head_dim 64 or 128.  BF16 and F8E4M3
+ * with head_dim 128 run on the tensor-core kernel (group 1..16); the rest on
+ * the CUDA-core kernel (group 1..8 or 16).  Device pointers must be 16-byte aligned, and
+ * page_stride * element size a multiple of 16 bytes.  kv_blocks may span up
+ * to 64 GiB.
+ *
+ * Differences from the page's signature: page_stride, max_prompt_length and
+ * max_cache_length are host scalars (the page passes them as device tensors),
+ * so a call never needs a device->host read.
+ *
+ * When more than one CTA shares a (row, kv head), the call uses a split-K
+ * workspace owned by the library, one per (device, stream), grown on demand
+ * with cudaMalloc; call qsa_reserve_workspace first to keep allocation off
+ * the hot path and out of graph capture.  Calls on the same stream are
+ * ordered; calls on different streams use different workspaces.
+ */
+QSA_API qsa_status qsa_sparse_attention_ragged_paged(
+    qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks,
+    int64_t page_stride, qsa_tensor cache_lengths, qsa_tensor kv_lookup_table,
+    uint32_t max_prompt_length, uint32_t max_cache_length, uint32_t layer_idx,
+    qsa_tensor token_indices, qsa_tensor counts, float scale, int32_t group, void* stream);
+
+/* Launch controls for tests and measurement.  Zero fields mean "choose". */
+typedef struct qsa_options {
+  int32_t kernel;    /* 0 auto, 1 CUDA-core kernel, 2 tensor-core kernel */
+  int32_t splits;    /* 0 auto, else CTAs per (row, kv head) along the selection */
+  int32_t reserved[6];
+} qsa_options;
+
+/* Same as qsa_sparse_attention_ragged_paged, with explicit launch controls
+ * (NULL = defaults).  A forced kernel that cannot run the case returns
+ * QSA_ERR_UNSUPPORTED. */
+QSA_API qsa_status qsa_sparse_attention_ragged_paged_ex(
+    qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks,
+    int64_t page_stride, qsa_tensor cache_lengths, qsa_tensor kv_lookup_table,
+    uint32_t max_prompt_length, uint32_t max_cache_length, uint32_t layer_idx,
+    qsa_tensor token_indices, qsa_tensor counts, float scale, int32_t group, void* stream,
+    const qsa_options* options);
+
+/* Describes the launch a call with these extents would make, without
+ * launching: kernel (1 CUDA-core, 2 tensor-core), CTAs per (row, kv head)
+ * along the selection, total CTAs and split-K workspace bytes.  dtype is the
+ * q / kv_blocks element type.  Host only; reads no device memory (it queries
+ * the current device's SM count and the kernel's occupancy). */
+QSA_API qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
+                    int64_t selection_width, int32_t group, const qsa_options* options, int32_t* kernel,
+                    int32_t* splits, int64_t* ctas, size_t* workspace_bytes);
+
+/* Makes sure the split-K workspace of (current device, stream) holds at least
+ * `bytes` bytes (allocating and zeroing it if not).  Blocking; not for the
+ * hot path or inside stream capture. */
+QSA_API qsa_status qsa_reserve_workspace(void* stream, size_t bytes);
+
+/* Frees every workspace and status word this library allocated on the
+ * current device (after synchronising the device). */
+QSA_API qsa_status qsa_release_device_state(void);
+
+/* Reads (and with clear != 0 also zeroes) the current device's status word,
+ * a bitwise OR of QSA_STATUS_* flags raised by kernels since the last clear.
+ * Synchronises `stream`; for tests and debugging, not the hot path. */
+QSA_API qsa_status qsa_read_device_status(void* stream, int32_t clear, uint32_t* flags);
+
+/* Human-readable name of a status code (static storage). */
+QSA_API const char* qsa_status_string(qsa_status status);
+
+/* Message describing the last non-OK status returned to this thread
+ * (thread-local storage, valid until this thread's next call). */
+QSA_API const char* qsa_last_error_message(void);
+
+/* Library version, (major << 16) | minor. */
+QSA_API int32_t qsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QSA_H_ */

@@ -1,0 +1,500 @@
+// Host side of libqsa: argument checks, launch planning, per-device state and
+// the extern "C" entry points declared in qsa.h.
+//
+// The checks follow the QSASparseAttentionRaggedPaged page's contract ("Raises:
+// Error: If the operand shapes disagree with the parameters"): every mismatch
+// is reported before anything is launched, and nothing here reads device
+// memory, synchronises or copies device -> host on the call path.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "qsa.h"
+#include "qsa_internal.cuh"
+
+namespace {
+
+using qsa::Params;
+
+thread_local std::string g_last_error;
+
+qsa_status fail(qsa_status s, const std::string& msg) {
+  g_last_error = msg;
+  return s;
+}
+
+int elem_bytes(int dtype) {
+  switch (dtype) {
+    case QSA_F32: return 4;
+    case QSA_BF16: return 2;
+    case QSA_F8E4M3: return 1;
+    case QSA_U32: return 4;
+    case QSA_I32: return 4;
+    default: return 0;
+  }
+}
+
+int64_t numel(const qsa_tensor& t) {
+  int64_t n = 1;
+  for (int i = 0; i < t.ndim && i < 6; ++i) n *= t.shape[i];
+  return n;
+}
+
+const char* dtype_name(int d) {
+  switch (d) {
+    case QSA_F32: return "F32";
+    case QSA_BF16: return "BF16";
+    case QSA_F8E4M3: return "F8E4M3";
+    case QSA_U32: return "U32";
+    case QSA_I32: return "I32";
+    default: return "?";
+  }
+}
+
+// Everything the checks resolve, and the launch plan.
+struct Resolved {
+  int elem = 0;  // qsa::Elem
+  int64_t total_q = 0, nq = 0, D = 0, num_pages = 0, L = 0, P = 0, nkv = 0, batch = 0, max_pages = 0, W = 0;
+  int64_t pitch = 0;  // elements between pages
+  int out_bf16 = 0;
+  int kernel = 0;  // 1 CUDA-core, 2 tensor-core
+  int splits = 1;
+  int band = 0;
+  int64_t ctas = 0;
+  size_t ws_partial_bytes = 0, ws_bytes = 0;
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Picks the kernel for a resolved call: the tensor-core kernel for BF16 and
+// FP8 with head_dim 128, the CUDA-core kernel otherwise (or as forced).
+qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
+  const bool mma_ok = (R.elem == qsa::kBF16 || R.elem == qsa::kE4M3) && R.D == 128;
+  const bool simt_ok = group <= 8 || group == 16;
+  const int want = opt ? opt->kernel : 0;
+  if (want == 2) {
+    if (!mma_ok) return fail(QSA_ERR_UNSUPPORTED, "tensor-core kernel needs BF16 or F8E4M3 with head_dim 128");
+    R.kernel = 2;
+  } else if (want == 1) {
+    if (!simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
+    R.kernel = 1;
+  } else if (want == 0) {
+    R.kernel = mma_ok ? 2 : 1;
+    if (R.kernel == 1 && !simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
+  } else {
+    return fail(QSA_ERR_ARG, "options.kernel must be 0, 1 or 2");
+  }
+  if (opt && opt->splits < 0) return fail(QSA_ERR_ARG, "options.splits must be >= 0");
+  if (R.kernel == 1 && opt && opt->splits > 1) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel has no split-K");
+  return QSA_OK;
+}
+
+qsa_status check_args(const qsa_tensor& output, const qsa_tensor& q, const qsa_tensor& offs, const qsa_tensor& kv,
+                      int64_t page_stride, const qsa_tensor& cache_lengths, const qsa_tensor& table,
+                      uint32_t layer_idx, const qsa_tensor& indices, const qsa_tensor& counts, int32_t group,
+                      const qsa_options* opt, Resolved& R) {
+  // ranks
+  struct {
+    const qsa_tensor* t;
+    int ndim;
+    const char* name;
+  } ranks[] = {{&output, 3, "output"},        {&q, 3, "q"},
+               {&offs, 1, "input_row_offsets"}, {&kv, 6, "kv_blocks"},
+               {&cache_lengths, 1, "cache_lengths"}, {&table, 2, "kv_lookup_table"},
+               {&indices, 2, "token_indices"}, {&counts, 1, "counts"}};
+  for (auto& x : ranks) {
+    if (x.t->ndim != x.ndim)
+      return fail(QSA_ERR_SHAPE, std::string(x.name) + ": rank " + std::to_string(x.t->ndim) + ", expected " +
+                                     std::to_string(x.ndim));
+    for (int i = 0; i < x.ndim; ++i)
+      if (x.t->shape[i] < 0) return fail(QSA_ERR_SHAPE, std::string(x.name) + ": negative extent");
+  }
+  // element types
+  if (q.dtype != QSA_F32 && q.dtype != QSA_BF16 && q.dtype != QSA_F8E4M3)
+    return fail(QSA_ERR_DTYPE, std::string("q: element type ") + dtype_name(q.dtype) + " is not F32, BF16 or F8E4M3");
+  if (kv.dtype != q.dtype)
+    return fail(QSA_ERR_DTYPE, std::string("kv_blocks: element type ") + dtype_name(kv.dtype) + " differs from q (" +
+                                   dtype_name(q.dtype) + ")");
+  if (output.dtype != QSA_F32 && output.dtype != QSA_BF16)
+    return fail(QSA_ERR_DTYPE, "output: element type must be F32 or BF16");
+  if (offs.dtype != QSA_U32) return fail(QSA_ERR_DTYPE, "input_row_offsets: element type must be U32");
+  if (cache_lengths.dtype != QSA_U32) return fail(QSA_ERR_DTYPE, "cache_lengths: element type must be U32");
+  if (table.dtype != QSA_U32) return fail(QSA_ERR_DTYPE, "kv_lookup_table: element type must be U32");
+  if (indices.dtype != QSA_I32) return fail(QSA_ERR_DTYPE, "token_indices: element type must be I32");
+  if (counts.dtype != QSA_I32) return fail(QSA_ERR_DTYPE, "counts: element type must be I32");
+
+  // extents
+  R.total_q = q.shape[0];
+  R.nq = q.shape[1];
+  R.D = q.shape[2];
+  R.num_pages = kv.shape[0];
+  R.L = kv.shape[2];
+  R.P = kv.shape[3];
+  R.nkv = kv.shape[4];
+  R.batch = cache_lengths.shape[0];
+  R.max_pages = table.shape[1];
+  R.W = indices.shape[1];
+  for (int i = 0; i < 3; ++i)
+    if (output.shape[i] != q.shape[i]) return fail(QSA_ERR_SHAPE, "output: shape differs from q");
+  if (kv.shape[1] != 2) return fail(QSA_ERR_SHAPE, "kv_blocks: axis 1 must have extent 2 (K, V)");
+  if (kv.shape[5] != R.D) return fail(QSA_ERR_SHAPE, "kv_blocks: head_dim differs from q");
+  if (group < 1) return fail(QSA_ERR_SHAPE, "group must be >= 1");
+  if (R.nkv < 1 || R.nq != (int64_t)group * R.nkv)
+    return fail(QSA_ERR_SHAPE, "num_q_heads (" + std::to_string(R.nq) + ") != group (" + std::to_string(group) +
+                                   ") * num_kv_heads (" + std::to_string(R.nkv) + ")");
+  if (offs.shape[0] != R.batch + 1) return fail(QSA_ERR_SHAPE, "input_row_offsets: extent must be batch + 1");
+  if (table.shape[0] != R.batch) return fail(QSA_ERR_SHAPE, "kv_lookup_table: first extent must be batch");
+  if (indices.shape[0] != R.total_q) return fail(QSA_ERR_SHAPE, "token_indices: first extent must be total_q");
+  if (counts.shape[0] != R.total_q) return fail(QSA_ERR_SHAPE, "counts: extent must be total_q");
+  if (R.batch == 0 && R.total_q > 0) return fail(QSA_ERR_SHAPE, "query rows without any sequence (batch == 0)");
+  if (R.P < 1 || R.L < 1) return fail(QSA_ERR_SHAPE, "kv_blocks: page_size and num_layers must be >= 1");
+
+  // pointers
+  if (!output.data && numel(output)) return fail(QSA_ERR_NULL, "output is NULL");
+  if (!q.data && numel(q)) return fail(QSA_ERR_NULL, "q is NULL");
+  if (!offs.data) return fail(QSA_ERR_NULL, "input_row_offsets is NULL");
+  if (!kv.data && numel(kv)) return fail(QSA_ERR_NULL, "kv_blocks is NULL");
+  if (!cache_lengths.data && numel(cache_lengths)) return fail(QSA_ERR_NULL, "cache_lengths is NULL");
+  if (!table.data && numel(table)) return fail(QSA_ERR_NULL, "kv_lookup_table is NULL");
+  if (!indices.data && numel(indices)) return fail(QSA_ERR_NULL, "token_indices is NULL");
+  if (!counts.data && numel(counts)) return fail(QSA_ERR_NULL, "counts is NULL");
+
+  // scalars
+  if ((int64_t)layer_idx >= R.L)
+    return fail(QSA_ERR_ARG, "layer_idx " + std::to_string(layer_idx) + " >= num_layers " + std::to_string(R.L));
+  const int64_t packed = 2 * R.L * R.P * R.nkv * R.D;
+  if (page_stride != -1 && page_stride < packed)
+    return fail(QSA_ERR_ARG, "page_stride must be -1 (packed) or >= the packed page size " + std::to_string(packed));
+  R.pitch = page_stride == -1 ? packed : page_stride;
+  R.elem = q.dtype == QSA_F32 ? qsa::kF32 : q.dtype == QSA_BF16 ? qsa::kBF16 : qsa::kE4M3;
+  R.out_bf16 = output.dtype == QSA_BF16;
+  const int eb = elem_bytes(q.dtype);
+
+  // what this build can run
+  if (R.D != 64 && R.D != 128) return fail(QSA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (group > 16) return fail(QSA_ERR_UNSUPPORTED, "group must be <= 16");
+  if ((R.pitch * eb) % 16) return fail(QSA_ERR_UNSUPPORTED, "page_stride * element size must be a multiple of 16 bytes");
+  if (!aligned16(kv.data) || !aligned16(q.data) || !aligned16(output.data))
+    return fail(QSA_ERR_UNSUPPORTED, "q, output and kv_blocks must be 16-byte aligned");
+  if (R.num_pages > 0xFFFFFFFFLL) return fail(QSA_ERR_UNSUPPORTED, "more than 2^32 - 1 pages");
+  const double kv_bytes = ((double)(R.num_pages > 0 ? R.num_pages - 1 : 0) * R.pitch + packed) * eb;
+  if (kv_bytes >= 68719476736.0 - 16.0) return fail(QSA_ERR_UNSUPPORTED, "kv_blocks larger than 64 GiB");
+  if (R.total_q > 0x7FFFFFFF || R.W > 0x7FFFFFFF || R.batch > 0x7FFFFFFF || R.max_pages > 0x7FFFFFFF)
+    return fail(QSA_ERR_UNSUPPORTED, "an extent exceeds 2^31 - 1");
+  if (R.nq * R.D * R.total_q > ((int64_t)1 << 40)) return fail(QSA_ERR_UNSUPPORTED, "q larger than 2^40 elements");
+
+  return choose_kernel(R, group, opt);
+}
+
+struct DeviceState {
+  uint32_t* status = nullptr;
+  std::map<void*, std::pair<void*, size_t>> workspaces;  // stream -> (buffer, bytes)
+  int sms = 0;
+  int occ[2][2] = {{0, 0}, {0, 0}};  // [bf16, e4m3][nt - 1]
+};
+
+std::mutex g_mu;
+std::map<int, DeviceState> g_dev;
+
+qsa_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(QSA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+// Launch plan of the tensor-core kernel: CTAs per (row, kv head).
+qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int dev) {
+  R.splits = 1;
+  R.band = qsa::kMmaTile;
+  if (R.kernel == 1) {
+    R.ctas = R.total_q * R.nkv;
+    R.ws_bytes = R.ws_partial_bytes = 0;
+    return QSA_OK;
+  }
+  const int64_t T = qsa::kMmaTile;
+  const int64_t min_splits = R.W > 0 ? (R.W + qsa::kMmaMaxBand - 1) / qsa::kMmaMaxBand : 1;
+  int64_t splits;
+  if (opt && opt->splits > 0) {
+    splits = opt->splits;
+    if (splits < min_splits)
+      return fail(QSA_ERR_ARG, "options.splits below " + std::to_string(min_splits) + " for this selection width");
+    if (splits > 4096) return fail(QSA_ERR_ARG, "options.splits above 4096");
+  } else {
+    int sms = 0, occ = 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      DeviceState& st = g_dev[dev];
+      if (!st.sms) {
+        const cudaError_t e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+      }
+      const int k = R.elem == qsa::kBF16 ? 0 : 1, nt = group <= 8 ? 0 : 1;
+      if (!st.occ[k][nt]) st.occ[k][nt] = k == 0 ? qsa::mma_ctas_per_sm_bf16(group) : qsa::mma_ctas_per_sm_e4m3(group);
+      sms = st.sms;
+      occ = st.occ[k][nt];
+    }
+    const int64_t units = R.total_q * R.nkv;
+    const int64_t slots = (int64_t)sms * occ;
+    splits = min_splits;
+    if (units > 0 && units < 2 * slots) {
+      // too few (row, kv head) units to fill the GPU: cut each selection into
+      // bands of >= 128 keys until there are about four waves of CTAs
+      const int64_t want = (4 * slots + units - 1) / units;
+      const int64_t most = std::max<int64_t>(min_splits, (R.W + 127) / 128);
+      splits = std::max<int64_t>(min_splits, std::min<int64_t>(want, most));
+    }
+  }
+  if (R.W > 0) {
+    int64_t band = (R.W + splits - 1) / splits;
+    band = (band + T - 1) / T * T;
+    if (!(opt && opt->splits > 0)) splits = (R.W + band - 1) / band;  // drop bands that start past W
+    R.band = (int)band;
+  }
+  R.splits = (int)splits;
+  R.ctas = R.total_q * R.nkv * R.splits;
+  if (R.splits > 1) {
+    const int64_t units = R.total_q * R.nkv;
+    R.ws_partial_bytes = ((size_t)(units * R.splits * group * (R.D + 2) * 4) + 255) / 256 * 256;
+    R.ws_bytes = R.ws_partial_bytes + (size_t)units * 4;
+  } else {
+    R.ws_bytes = R.ws_partial_bytes = 0;
+  }
+  return QSA_OK;
+}
+
+// Grows (never shrinks) the split-K workspace of (dev, stream); zeroes it so
+// every arrival ticket starts at 0.  Under the lock.
+qsa_status ensure_workspace(DeviceState& st, void* stream, size_t bytes, void** out) {
+  auto& ws = st.workspaces[stream];
+  if (ws.second < bytes) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaStreamIsCapturing((cudaStream_t)stream, &cs);
+    if (cs != cudaStreamCaptureStatusNone)
+      return fail(QSA_ERR_CUDA, "split-K workspace must be reserved (qsa_reserve_workspace) before stream capture");
+    if (ws.first) {
+      cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+      cudaFree(ws.first);
+      ws.first = nullptr;
+      ws.second = 0;
+    }
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, bytes);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+    e = cudaMemset(p, 0, bytes);
+    if (e != cudaSuccess) {
+      cudaFree(p);
+      return cuda_fail(e, "cudaMemset(workspace)");
+    }
+    ws.first = p;
+    ws.second = bytes;
+  }
+  *out = ws.first;
+  return QSA_OK;
+}
+
+qsa_status ensure_status(DeviceState& st) {
+  if (st.status) return QSA_OK;
+  void* p = nullptr;
+  cudaError_t e = cudaMalloc(&p, 256);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(status)");
+  e = cudaMemset(p, 0, 256);
+  if (e != cudaSuccess) {
+    cudaFree(p);
+    return cuda_fail(e, "cudaMemset(status)");
+  }
+  st.status = static_cast<uint32_t*>(p);
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
+                                                qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths,
+                                                qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
+                                                uint32_t max_cache_length, uint32_t layer_idx,
+                                                qsa_tensor token_indices, qsa_tensor counts, float scale,
+                                                int32_t group, void* stream, const qsa_options* options) {
+  (void)max_prompt_length;  // launch-sizing hints only: the plan uses host-known extents
+  (void)max_cache_length;
+  Resolved R;
+  qsa_status s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table,
+                            layer_idx, token_indices, counts, group, options, R);
+  if (s != QSA_OK) return s;
+  if (R.total_q == 0) return QSA_OK;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  s = plan_launch(R, group, options, dev);
+  if (s != QSA_OK) return s;
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceState& st = g_dev[dev];
+    s = ensure_status(st);
+    if (s != QSA_OK) return s;
+    p.status = st.status;
+    if (R.splits > 1) {
+      void* ws = nullptr;
+      s = ensure_workspace(st, stream, R.ws_bytes, &ws);
+      if (s != QSA_OK) return s;
+      p.ws_partial = static_cast<float*>(ws);
+      p.ws_ticket = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + R.ws_partial_bytes);
+    }
+  }
+  const int64_t eb = elem_bytes(q.dtype);
+  p.out = output.data;
+  p.q = static_cast<const unsigned char*>(q.data);
+  p.row_offsets = static_cast<const uint32_t*>(input_row_offsets.data);
+  p.kv = static_cast<const unsigned char*>(kv_blocks.data);
+  p.cache_lengths = static_cast<const uint32_t*>(cache_lengths.data);
+  p.table = static_cast<const uint32_t*>(kv_lookup_table.data);
+  p.indices = static_cast<const int32_t*>(token_indices.data);
+  p.counts = static_cast<const int32_t*>(counts.data);
+  p.page_pitch_bytes = R.pitch * eb;
+  p.k_layer_bytes = (int64_t)layer_idx * R.P * R.nkv * R.D * eb;
+  p.v_minus_k_bytes = R.L * R.P * R.nkv * R.D * eb;
+  p.slot_bytes = R.nkv * R.D * eb;
+  p.head_bytes = R.D * eb;
+  p.total_q = (int32_t)R.total_q;
+  p.batch = (int32_t)R.batch;
+  p.nq = (int32_t)R.nq;
+  p.nkv = (int32_t)R.nkv;
+  p.group = group;
+  p.D = (int32_t)R.D;
+  p.P = (int32_t)R.P;
+  p.W = (int32_t)R.W;
+  p.max_pages = (int32_t)R.max_pages;
+  p.num_pages = (uint32_t)R.num_pages;
+  p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax in base 2
+  p.out_bf16 = R.out_bf16;
+  p.splits = R.splits;
+  p.band = R.band;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (R.kernel == 1)
+    e = qsa::launch_simt(p, R.elem, st);
+  else
+    e = R.elem == qsa::kBF16 ? qsa::launch_mma_bf16(p, st) : qsa::launch_mma_e4m3(p, st);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return QSA_OK;
+}
+
+qsa_status qsa_sparse_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
+                                             qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths,
+                                             qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
+                                             uint32_t max_cache_length, uint32_t layer_idx, qsa_tensor token_indices,
+                                             qsa_tensor counts, float scale, int32_t group, void* stream) {
+  return qsa_sparse_attention_ragged_paged_ex(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
+                                              kv_lookup_table, max_prompt_length, max_cache_length, layer_idx,
+                                              token_indices, counts, scale, group, stream, nullptr);
+}
+
+qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
+                    int64_t selection_width, int32_t group, const qsa_options* options, int32_t* kernel,
+                    int32_t* splits, int64_t* ctas, size_t* workspace_bytes) {
+  Resolved R;
+  if (dtype != QSA_F32 && dtype != QSA_BF16 && dtype != QSA_F8E4M3)
+    return fail(QSA_ERR_DTYPE, "dtype must be F32, BF16 or F8E4M3");
+  if (total_q < 0 || num_kv_heads < 1 || selection_width < 0 || group < 1)
+    return fail(QSA_ERR_SHAPE, "negative or empty extent");
+  if (head_dim != 64 && head_dim != 128) return fail(QSA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (group > 16) return fail(QSA_ERR_UNSUPPORTED, "group must be <= 16");
+  if (options && options->splits < 0) return fail(QSA_ERR_ARG, "options.splits must be >= 0");
+  R.elem = dtype == QSA_F32 ? qsa::kF32 : dtype == QSA_BF16 ? qsa::kBF16 : qsa::kE4M3;
+  R.total_q = total_q;
+  R.nkv = num_kv_heads;
+  R.D = head_dim;
+  R.W = selection_width;
+  qsa_status s = choose_kernel(R, group, options);
+  if (s != QSA_OK) return s;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  s = plan_launch(R, group, options, dev);
+  if (s != QSA_OK) return s;
+  if (kernel) *kernel = R.kernel;
+  if (splits) *splits = R.splits;
+  if (ctas) *ctas = R.ctas;
+  if (workspace_bytes) *workspace_bytes = R.ws_bytes;
+  return QSA_OK;
+}
+
+qsa_status qsa_reserve_workspace(void* stream, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  qsa_status s = ensure_status(st);
+  if (s != QSA_OK) return s;
+  void* ws = nullptr;
+  return bytes ? ensure_workspace(st, stream, bytes, &ws) : QSA_OK;
+}
+
+qsa_status qsa_release_device_state(void) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_dev.find(dev);
+  if (it == g_dev.end()) return QSA_OK;
+  for (auto& kv : it->second.workspaces)
+    if (kv.second.first) cudaFree(kv.second.first);
+  if (it->second.status) cudaFree(it->second.status);
+  g_dev.erase(it);
+  return QSA_OK;
+}
+
+qsa_status qsa_read_device_status(void* stream, int32_t clear, uint32_t* flags) {
+  if (!flags) return fail(QSA_ERR_NULL, "flags is NULL");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  uint32_t* status = nullptr;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    qsa_status s = ensure_status(g_dev[dev]);
+    if (s != QSA_OK) return s;
+    status = g_dev[dev].status;
+  }
+  e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  e = cudaMemcpy(flags, status, sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  if (clear) {
+    e = cudaMemset(status, 0, sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset(status)");
+  }
+  return QSA_OK;
+}
+
+const char* qsa_status_string(qsa_status s) {
+  switch (s) {
+    case QSA_OK: return "QSA_OK";
+    case QSA_ERR_NULL: return "QSA_ERR_NULL";
+    case QSA_ERR_SHAPE: return "QSA_ERR_SHAPE";
+    case QSA_ERR_DTYPE: return "QSA_ERR_DTYPE";
+    case QSA_ERR_UNSUPPORTED: return "QSA_ERR_UNSUPPORTED";
+    case QSA_ERR_ARG: return "QSA_ERR_ARG";
+    case QSA_ERR_CUDA: return "QSA_ERR_CUDA";
+    default: return "QSA_ERR_UNKNOWN";
+  }
+}
+
+const char* qsa_last_error_message(void) { return g_last_error.c_str(); }
+
+int32_t qsa_version(void) { return (0 << 16) | 1; }
+
+}  // extern "C"

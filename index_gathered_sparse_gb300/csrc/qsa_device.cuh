@@ -1,0 +1,177 @@
+// Device helpers shared by libqsa's kernels: row -> sequence lookup, position
+// -> cache row translation through the page table, and the end of a
+// (row, kv head) unit (cross-warp softmax merge, split-K partials and the
+// fused last-CTA combine).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "qsa_internal.cuh"
+
+namespace qsa {
+
+constexpr uint32_t kInvalidOff = 0xFFFFFFFFu;
+
+struct RowInfo {
+  int b;           // owning sequence
+  int64_t kv_len;  // valid positions of that sequence: cache_lengths[b] + rows_b
+  int n;           // valid selection entries: clamp(counts[r], 0, W)
+  bool ok;         // r belongs to a sequence
+};
+
+// Block-wide (every thread must call): finds the sequence b with
+// input_row_offsets[b] <= r < input_row_offsets[b + 1] by counting the
+// offsets [1, batch] that are <= r (the offsets are nondecreasing), one
+// coalesced pass per blockDim.x sequences.
+__device__ __forceinline__ RowInfo row_info(const Params& p, int r) {
+  int c = 0;
+  for (int base = 1; base <= p.batch; base += blockDim.x) {
+    const int k = base + (int)threadIdx.x;
+    const int pred = (k <= p.batch) && (__ldg(p.row_offsets + k) <= (uint32_t)r);
+    c += __syncthreads_count(pred);
+  }
+  RowInfo ri;
+  ri.b = c;
+  ri.ok = false;
+  ri.kv_len = 0;
+  ri.n = 0;
+  if (c < p.batch) {
+    const uint32_t o0 = __ldg(p.row_offsets + c), o1 = __ldg(p.row_offsets + c + 1);
+    if (o0 <= (uint32_t)r && (uint32_t)r < o1) {
+      ri.ok = true;
+      ri.kv_len = (int64_t)__ldg(p.cache_lengths + c) + (int64_t)(o1 - o0);
+      ri.n = min(max(__ldg(p.counts + r), 0), p.W);
+    }
+  }
+  return ri;
+}
+
+// First half of a position's translation: range checks and the logical page.
+// Returns the logical page, or -1 (and sets a status bit) when the position
+// cannot be read.
+__device__ __forceinline__ int64_t logical_page(const Params& p, int64_t kv_len, int32_t pos, uint32_t& bad) {
+  if (pos < 0 || (int64_t)pos >= kv_len) {
+    bad |= QSA_STATUS_BAD_INDEX;
+    return -1;
+  }
+  const uint32_t lp = (uint32_t)pos / (uint32_t)p.P;
+  if (lp >= (uint32_t)p.max_pages) {
+    bad |= QSA_STATUS_BAD_PAGE;
+    return -1;
+  }
+  return (int64_t)lp;
+}
+
+// Second half: the K row of (page, slot, kv head) in 16-byte units from the
+// kv_blocks base, or kInvalidOff when the table entry names no page.
+__device__ __forceinline__ uint32_t k_row_offset16(const Params& p, uint32_t page, int32_t pos, int h, uint32_t& bad) {
+  if (page >= p.num_pages) {
+    bad |= QSA_STATUS_BAD_PAGE;
+    return kInvalidOff;
+  }
+  const int64_t off = (int64_t)page * p.page_pitch_bytes + p.k_layer_bytes +
+                      (int64_t)((uint32_t)pos % (uint32_t)p.P) * p.slot_bytes + (int64_t)h * p.head_bytes;
+  return (uint32_t)(off >> 4);
+}
+
+__device__ __forceinline__ void store_out(const Params& p, int64_t idx, float v) {
+  if (p.out_bf16)
+    reinterpret_cast<__nv_bfloat16*>(p.out)[idx] = __float2bfloat16_rn(v);
+  else
+    reinterpret_cast<float*>(p.out)[idx] = v;
+}
+
+// Finishes one (row r, kv head h) unit from NW per-warp softmax states held in
+// shared memory: sm_m[w*GP + i] (running max of the base-2 scores),
+// sm_l[w*GP + i] (sum of exponentials) and sm_o[(w*GP + i)*D + d]
+// (unnormalised output), for query heads i < group.
+//
+// With one CTA per unit it writes output[r, h*group + i, :].  With split-K it
+// stores this CTA's merged partial, and the last CTA of the unit to arrive
+// (an atomic ticket; no CTA ever waits for another) merges all partials and
+// writes the output, then re-arms the ticket for the next call.
+template <int NW>
+__device__ __forceinline__ void finish_unit(const Params& p, int r, int h, int split, bool row_ok, const float* sm_m,
+                                            const float* sm_l, const float* sm_o, int GP) {
+  const int G = p.group, D = p.D;
+  const int64_t out_base = ((int64_t)r * p.nq + (int64_t)h * G) * D;
+  if (p.splits == 1) {
+    for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+      const int i = idx / D, d = idx - i * D;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * GP + i]);
+      float val = 0.f;
+      if (row_ok && M != -CUDART_INF_F) {
+        float L = 0.f, O = 0.f;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+          const float e = exp2f(sm_m[w * GP + i] - M);
+          L += sm_l[w * GP + i] * e;
+          O += sm_o[(w * GP + i) * D + d] * e;
+        }
+        val = O / L;
+      }
+      store_out(p, out_base + idx, val);
+    }
+    return;
+  }
+
+  // split-K: partial layout per (unit, split): o[G][D], m[G], l[G]
+  const int unit = r * p.nkv + h;
+  const int64_t stride = (int64_t)G * (D + 2);
+  float* part = p.ws_partial + ((int64_t)unit * p.splits + split) * stride;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int i = idx / D, d = idx - i * D;
+    float M = -CUDART_INF_F;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) M = fmaxf(M, sm_m[w * GP + i]);
+    float L = 0.f, O = 0.f;
+    if (M != -CUDART_INF_F) {
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float e = exp2f(sm_m[w * GP + i] - M);
+        L += sm_l[w * GP + i] * e;
+        O += sm_o[(w * GP + i) * D + d] * e;
+      }
+    }
+    part[idx] = O;
+    if (d == 0) {
+      part[G * D + i] = M;
+      part[G * D + G + i] = L;
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  __shared__ int s_last;
+  if (threadIdx.x == 0) {
+    const uint32_t t = atomicAdd(p.ws_ticket + unit, 1u);
+    s_last = (t == (uint32_t)(p.splits - 1));
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const float* base = p.ws_partial + (int64_t)unit * p.splits * stride;
+  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
+    const int i = idx / D;
+    float M = -CUDART_INF_F;
+    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(base + s * stride + G * D + i));
+    float val = 0.f;
+    if (row_ok && M != -CUDART_INF_F) {
+      float L = 0.f, O = 0.f;
+      for (int s = 0; s < p.splits; ++s) {
+        const float ms = __ldcg(base + s * stride + G * D + i);
+        const float e = exp2f(ms - M);  // an empty split has ms = -inf -> e = 0
+        L += __ldcg(base + s * stride + G * D + G + i) * e;
+        O += __ldcg(base + s * stride + idx) * e;
+      }
+      val = O / L;
+    }
+    store_out(p, out_base + idx, val);
+  }
+  if (threadIdx.x == 0) p.ws_ticket[unit] = 0u;
+}
+
+}  // namespace qsa

@@ -1,0 +1,55 @@
+// Internal declarations shared by libqsa's translation units (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qsa.h"
+
+namespace qsa {
+
+// Everything a kernel needs, resolved on the host from the descriptors.
+struct Params {
+  void* out;                      // [total_q, nq, D] f32 | bf16
+  const unsigned char* q;         // [total_q, nq, D] element bytes
+  const uint32_t* row_offsets;    // [batch + 1]
+  const unsigned char* kv;        // kv_blocks base
+  const uint32_t* cache_lengths;  // [batch]
+  const uint32_t* table;          // [batch, max_pages]
+  const int32_t* indices;         // [total_q, W]
+  const int32_t* counts;          // [total_q]
+  uint32_t* status;               // device status word (atomicOr)
+  float* ws_partial;              // split-K partials (splits > 1)
+  uint32_t* ws_ticket;            // split-K arrival counters, one per (row, kv head)
+
+  int64_t page_pitch_bytes;  // bytes from one page to the next
+  int64_t k_layer_bytes;     // byte offset of [page, 0, layer_idx, 0, 0, 0] in a page
+  int64_t v_minus_k_bytes;   // byte distance from a K row to its V row
+  int64_t slot_bytes;        // num_kv_heads * D * elem
+  int64_t head_bytes;        // D * elem
+
+  int32_t total_q, batch, nq, nkv, group, D, P, W, max_pages;
+  uint32_t num_pages;
+  float scale_log2;  // scale * log2(e): the softmax runs in base 2
+  int32_t out_bf16;
+  int32_t splits;    // CTAs per (row, kv head)
+  int32_t band;      // keys per split band (multiple of the key tile)
+};
+
+// Element type tags.
+enum Elem { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
+
+// Launchers (return a cudaError_t from the launch).
+cudaError_t launch_simt(const Params& p, int elem, cudaStream_t stream);
+cudaError_t launch_mma_bf16(const Params& p, cudaStream_t stream);
+cudaError_t launch_mma_e4m3(const Params& p, cudaStream_t stream);
+// CTAs of the tensor-core kernel that fit on one SM (for the split planner).
+int mma_ctas_per_sm_bf16(int group);
+int mma_ctas_per_sm_e4m3(int group);
+
+// Tensor-core kernel limits.
+constexpr int kMmaTile = 64;      // keys per pipeline stage (16 per warp)
+constexpr int kMmaMaxBand = 2048; // keys one CTA translates up front
+constexpr int kMmaThreads = 128;
+
+}  // namespace qsa

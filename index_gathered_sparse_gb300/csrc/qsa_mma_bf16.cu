@@ -1,0 +1,13 @@
+// BF16 instantiations of the tensor-core kernel (group <= 8: one 8-wide head
+// tile; group <= 16: two).
+#include "qsa_mma.cuh"
+
+namespace qsa {
+
+cudaError_t launch_mma_bf16(const Params& p, cudaStream_t s) {
+  return p.group <= 8 ? launch_mma_nt<kBF16, 1>(p, s) : launch_mma_nt<kBF16, 2>(p, s);
+}
+
+int mma_ctas_per_sm_bf16(int group) { return mma_occupancy<kBF16>(group); }
+
+}  // namespace qsa

@@ -289,9 +289,10 @@ def assemble(name: str, dtype: str, out_dtype: str, q: np.ndarray, logical_k: Se
         kb, vb = logical_k[b], logical_v[b]
         full = n // P
         pages = table[b, : npages[b]].astype(np.int64)
-        if full:
-            kv6[pages[:full], 0, layer_idx] = kb[: full * P].reshape(full, P, nkv, D)
-            kv6[pages[:full], 1, layer_idx] = vb[: full * P].reshape(full, P, nkv, D)
+        # page by page: fancy indexing through a strided view is far slower
+        for i in range(full):
+            kv6[pages[i], 0, layer_idx] = kb[i * P : (i + 1) * P]
+            kv6[pages[i], 1, layer_idx] = vb[i * P : (i + 1) * P]
         rem = n - full * P
         if rem:
             kv6[pages[full], 0, layer_idx, :rem] = kb[full * P :]
@@ -466,3 +467,44 @@ def small_variants() -> dict:
         "fp8_mixed_small": fp8_mixed(seed=15, n_decode=5, n_prefill=2, prefill_rows=17,
                                      cache_range=(40, 1500), width=200),
     }
+
+
+def to_torch(x: QSAInputs, device, out_dtype: Optional[str] = None) -> dict:
+    """Uploads ``x`` and returns the keyword arguments of
+    ``binding.qsa_sparse_attention_ragged_paged`` (output freshly allocated).
+    U32 operands travel as int32 tensors holding the same bits."""
+    import torch
+
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}
+
+    def raw(a: np.ndarray, dtype: str):
+        a = np.ascontiguousarray(a)
+        if dtype == "f32":
+            return torch.from_numpy(a)
+        if dtype == "bf16":
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+        return torch.from_numpy(a).view(torch.float8_e4m3fn)
+
+    def i32(a: np.ndarray):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int32)).to(device)
+
+    n, two, L, P, nkv, D = x.kv_shape
+    flat = raw(x.kv_flat, x.dtype).to(device)
+    kv = flat.as_strided(x.kv_shape, (x.page_pitch, L * P * nkv * D, P * nkv * D, nkv * D, D, 1))
+    od = out_dtype or x.out_dtype
+    return dict(
+        output=torch.empty((x.total_q, x.num_q_heads, D), dtype=tdt[od], device=device),
+        q=raw(x.q, x.dtype).to(device),
+        input_row_offsets=i32(x.input_row_offsets),
+        kv_blocks=kv,
+        page_stride=x.page_stride,
+        cache_lengths=i32(x.cache_lengths),
+        kv_lookup_table=i32(x.kv_lookup_table),
+        max_prompt_length=x.max_prompt_length,
+        max_cache_length=x.max_cache_length,
+        layer_idx=x.layer_idx,
+        token_indices=i32(x.token_indices),
+        counts=i32(x.counts),
+        scale=x.scale,
+        group=x.group,
+    )
