@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--min-warmup-s", type=float, default=1.0,
+                    help="keep warming up at least this long (0 for profiler runs)")
     return ap.parse_args()
 
 
@@ -123,6 +125,33 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def replica_spec(name: str, rank: int, world: int):
+    """The workload one rank runs: every rank gets its own seeded batch."""
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    spec = wl.WORKLOADS[name]()
+    if world > 1:
+        spec.seed += 100 * rank
+    return spec
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of each rank's ``x`` (identity on one rank)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_rate(rows_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job query-tokens/s: every rank's rows over the slowest rank's step."""
+    return world * rows_per_rank / (ms_per_step / 1e3)
 
 
 def sample_rows(total_q: int):
@@ -206,9 +235,7 @@ def main():
 
     from index_gathered_sparse_gb300 import workloads as wl
 
-    spec = wl.WORKLOADS[args.workload]()
-    if world > 1:
-        spec.seed += 100 * rank  # independent replicas
+    spec = replica_spec(args.workload, rank, world)
     t_gen = time.perf_counter()
     x = spec.build()
     print(f"[bench] rank {rank}: built {x.name} in {time.perf_counter() - t_gen:.1f}s", file=sys.stderr)
@@ -256,7 +283,7 @@ def main():
     # warm-up: at least W steps and at least ~1 s so the clock samples see load
     t0 = time.perf_counter()
     n_warm = 0
-    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < 1.0:
+    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < args.min_warmup_s:
         flush_buf.fill_(n_warm & 0xFF)
         call()
         n_warm += 1
@@ -272,13 +299,8 @@ def main():
     barrier()
     per_step = [a.elapsed_time(b) for a, b in ev]  # ms
     clocks = sampler.stop()
-    t_rank = sum(per_step)
-    if world > 1:
-        t = torch.tensor([t_rank], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        t_rank = float(t.item())
-    ms_per_step = t_rank / args.steps
-    value = world * x.total_q / (ms_per_step / 1e3)
+    ms_per_step = max_over_ranks(sum(per_step), world, dev) / args.steps
+    value = aggregate_rate(x.total_q, world, ms_per_step)
 
     flags = B.qsa_read_device_status(clear=True)
     if flags:
@@ -311,12 +333,8 @@ def main():
             e2e_step()
             evs[i][1].record(stream)
         barrier()
-        te = sum(a.elapsed_time(b) for a, b in evs)
-        if world > 1:
-            t = torch.tensor([te], device=dev, dtype=torch.float64)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            te = float(t.item())
-        e2e = {"value": world * x.total_q / (te / n_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        te = max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world, dev)
+        e2e = {"value": aggregate_rate(x.total_q, world, te / n_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
     alg_bytes = x.algorithmic_bytes()

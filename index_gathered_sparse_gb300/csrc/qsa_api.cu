@@ -192,9 +192,20 @@ qsa_status check_args(const qsa_tensor& output, const qsa_tensor& q, const qsa_t
   return choose_kernel(R, group, opt);
 }
 
+// Split-K scratch of one (device, stream): f32 partials (contents never need
+// to survive a call) and the per-(row, kv head) arrival tickets, which must
+// read 0 at the start of every call: each is zeroed when allocated and re-armed
+// by the last CTA that used it, so they live in their own buffer.
+struct Workspace {
+  void* partial = nullptr;
+  size_t partial_bytes = 0;
+  uint32_t* tickets = nullptr;
+  size_t ticket_count = 0;
+};
+
 struct DeviceState {
   uint32_t* status = nullptr;
-  std::map<void*, std::pair<void*, size_t>> workspaces;  // stream -> (buffer, bytes)
+  std::map<void*, Workspace> workspaces;  // keyed by stream
   int sms = 0;
   int occ[2][2] = {{0, 0}, {0, 0}};  // [bf16, e4m3][nt - 1]
 };
@@ -266,34 +277,47 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   return QSA_OK;
 }
 
-// Grows (never shrinks) the split-K workspace of (dev, stream); zeroes it so
-// every arrival ticket starts at 0.  Under the lock.
-qsa_status ensure_workspace(DeviceState& st, void* stream, size_t bytes, void** out) {
-  auto& ws = st.workspaces[stream];
-  if (ws.second < bytes) {
+// Grows (never shrinks) the split-K workspace of (dev, stream) to hold
+// `partial_bytes` of partials and `tickets` arrival tickets.  Under the lock.
+qsa_status ensure_workspace(DeviceState& st, void* stream, size_t partial_bytes, size_t tickets, Workspace** out) {
+  Workspace& ws = st.workspaces[stream];
+  const bool grow_p = ws.partial_bytes < partial_bytes, grow_t = ws.ticket_count < tickets;
+  if (grow_p || grow_t) {
     cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
     cudaStreamIsCapturing((cudaStream_t)stream, &cs);
     if (cs != cudaStreamCaptureStatusNone)
       return fail(QSA_ERR_CUDA, "split-K workspace must be reserved (qsa_reserve_workspace) before stream capture");
-    if (ws.first) {
-      cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
-      cudaFree(ws.first);
-      ws.first = nullptr;
-      ws.second = 0;
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);  // the old buffers may still be in use
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  }
+  if (grow_p) {
+    if (ws.partial) cudaFree(ws.partial);
+    ws.partial = nullptr;
+    ws.partial_bytes = 0;
+    cudaError_t e = cudaMalloc(&ws.partial, partial_bytes);
+    if (e != cudaSuccess) {
+      ws.partial = nullptr;
+      return cuda_fail(e, "cudaMalloc(split-K partials)");
     }
+    ws.partial_bytes = partial_bytes;
+  }
+  if (grow_t) {
+    if (ws.tickets) cudaFree(ws.tickets);
+    ws.tickets = nullptr;
+    ws.ticket_count = 0;
     void* p = nullptr;
-    cudaError_t e = cudaMalloc(&p, bytes);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-    e = cudaMemset(p, 0, bytes);
+    cudaError_t e = cudaMalloc(&p, tickets * sizeof(uint32_t));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMalloc(split-K tickets)");
+    e = cudaMemset(p, 0, tickets * sizeof(uint32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) {
       cudaFree(p);
-      return cuda_fail(e, "cudaMemset(workspace)");
+      return cuda_fail(e, "cudaMemset(split-K tickets)");
     }
-    ws.first = p;
-    ws.second = bytes;
+    ws.tickets = static_cast<uint32_t*>(p);
+    ws.ticket_count = tickets;
   }
-  *out = ws.first;
+  *out = &ws;
   return QSA_OK;
 }
 
@@ -344,11 +368,11 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
     if (s != QSA_OK) return s;
     p.status = st.status;
     if (R.splits > 1) {
-      void* ws = nullptr;
-      s = ensure_workspace(st, stream, R.ws_bytes, &ws);
+      Workspace* ws = nullptr;
+      s = ensure_workspace(st, stream, R.ws_partial_bytes, (size_t)(R.total_q * R.nkv), &ws);
       if (s != QSA_OK) return s;
-      p.ws_partial = static_cast<float*>(ws);
-      p.ws_ticket = reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + R.ws_partial_bytes);
+      p.ws_partial = static_cast<float*>(ws->partial);
+      p.ws_ticket = ws->tickets;
     }
   }
   const int64_t eb = elem_bytes(q.dtype);
@@ -437,8 +461,10 @@ qsa_status qsa_reserve_workspace(void* stream, size_t bytes) {
   DeviceState& st = g_dev[dev];
   qsa_status s = ensure_status(st);
   if (s != QSA_OK) return s;
-  void* ws = nullptr;
-  return bytes ? ensure_workspace(st, stream, bytes, &ws) : QSA_OK;
+  // the reservation covers tickets for as many (row, kv head) units as
+  // `bytes` of partials could serve at the smallest partial (2 splits x 1 head x 64 + 2 floats)
+  Workspace* ws = nullptr;
+  return bytes ? ensure_workspace(st, stream, bytes, bytes / (2 * 66 * sizeof(float)) + 1, &ws) : QSA_OK;
 }
 
 qsa_status qsa_release_device_state(void) {
@@ -450,8 +476,10 @@ qsa_status qsa_release_device_state(void) {
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_dev.find(dev);
   if (it == g_dev.end()) return QSA_OK;
-  for (auto& kv : it->second.workspaces)
-    if (kv.second.first) cudaFree(kv.second.first);
+  for (auto& kv : it->second.workspaces) {
+    if (kv.second.partial) cudaFree(kv.second.partial);
+    if (kv.second.tickets) cudaFree(kv.second.tickets);
+  }
   if (it->second.status) cudaFree(it->second.status);
   g_dev.erase(it);
   return QSA_OK;

@@ -382,14 +382,14 @@ def tiny_ragged(seed: int = 0) -> WorkloadSpec:
 
 
 def bf16_decode(seed: int = 2, batch: int = 64, cache_range=(1024, 8192), width: int = 2048,
-                num_layers: int = 4, layer_idx: int = 2) -> WorkloadSpec:
+                num_layers: int = 4, layer_idx: int = 2, name: str = "bf16_decode") -> WorkloadSpec:
     """bf16 decode: one new token per sequence, cache U[1024, 8192], 32 q heads
     on 8 kv heads, head_dim 128, page 128, 4 layers (layer 2), width 2048,
     counts = min(2048, pos+1), distinct U[0,pos] in random order, tail -1."""
     rng = np.random.default_rng(seed + 1000)
     cache = rng.integers(cache_range[0], cache_range[1] + 1, size=batch)
     return WorkloadSpec(
-        name="bf16_decode", seed=seed, rows=[1] * batch, cache_lengths=cache.tolist(),
+        name=name, seed=seed, rows=[1] * batch, cache_lengths=cache.tolist(),
         num_q_heads=32, num_kv_heads=8, head_dim=128, page_size=128, num_layers=num_layers,
         layer_idx=layer_idx, dtype="bf16", out_dtype="bf16", selection_width=width,
         select=_sel_uniform_distinct("full"), tail=_tail_const(-1),
@@ -449,6 +449,9 @@ def fp8_mixed(seed: int = 5, n_decode: int = 120, n_prefill: int = 8, prefill_ro
 WORKLOADS = {
     "tiny_ragged_fp32": tiny_ragged,
     "bf16_decode": bf16_decode,
+    # the same gathers from a 1-layer cache (1.2 GB instead of 4.8 GB): a
+    # smaller device footprint for profiler captures
+    "bf16_decode_1layer": lambda: bf16_decode(num_layers=1, layer_idx=0, name="bf16_decode_1layer"),
     "bf16_chunked_prefill": bf16_chunked_prefill,
     "bf16_long_decode": bf16_long_decode,
     "fp8_mixed": fp8_mixed,

@@ -208,6 +208,10 @@ def test_empty_and_clamped_counts():
     x = SMALL["fp8_mixed_small"].build()
     x.counts[:3] = 0
     x.counts[3] = -9
+    # counts past the width clamp to the width, so the whole row must then hold
+    # valid positions: repeat the valid prefix over the tail
+    n4 = int(x.counts[4])
+    x.token_indices[4, n4:] = np.resize(x.token_indices[4, :n4], x.selection_width - n4)
     x.counts[4] = x.selection_width + 1000
     ref = oracle.sparse_attention(x)
     for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=5)):
