@@ -233,7 +233,7 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     splits = opt->splits;
     if (splits < min_splits)
       return fail(QSA_ERR_ARG, "options.splits below " + std::to_string(min_splits) + " for this selection width");
-    if (splits > 4096) return fail(QSA_ERR_ARG, "options.splits above 4096");
+    if (splits > qsa::kMaxSplits) return fail(QSA_ERR_ARG, "options.splits above " + std::to_string(qsa::kMaxSplits));
   } else {
     int sms = 0, occ = 0;
     {
@@ -250,13 +250,19 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     }
     const int64_t units = R.total_q * R.nkv;
     const int64_t slots = (int64_t)sms * occ;
+    // Wave model: a CTA costs about (kPrologueKeys + keys it gathers); the
+    // launch costs waves x that.  Pick the split count that minimises it.
+    constexpr int64_t kPrologueKeys = 384;
+    const int64_t most = std::max<int64_t>(min_splits, std::min<int64_t>(qsa::kMaxSplits, (R.W + T - 1) / T));
     splits = min_splits;
-    if (units > 0 && units < 2 * slots) {
-      // too few (row, kv head) units to fill the GPU: cut each selection into
-      // bands of >= 128 keys until there are about four waves of CTAs
-      const int64_t want = (4 * slots + units - 1) / units;
-      const int64_t most = std::max<int64_t>(min_splits, (R.W + 127) / 128);
-      splits = std::max<int64_t>(min_splits, std::min<int64_t>(want, most));
+    double best = -1.0;
+    for (int64_t sp = min_splits; units > 0 && sp <= most; ++sp) {
+      const int64_t waves = (units * sp + slots - 1) / slots;
+      const double cost = (double)waves * (double)(kPrologueKeys + (R.W + sp - 1) / sp);
+      if (best < 0 || cost < best) {
+        best = cost;
+        splits = sp;
+      }
     }
   }
   if (R.W > 0) {
@@ -269,7 +275,7 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   R.ctas = R.total_q * R.nkv * R.splits;
   if (R.splits > 1) {
     const int64_t units = R.total_q * R.nkv;
-    R.ws_partial_bytes = ((size_t)(units * R.splits * group * (R.D + 2) * 4) + 255) / 256 * 256;
+    R.ws_partial_bytes = ((size_t)(units * R.splits * qsa::partial_stride(group, R.D) * 4) + 255) / 256 * 256;
     R.ws_bytes = R.ws_partial_bytes + (size_t)units * 4;
   } else {
     R.ws_bytes = R.ws_partial_bytes = 0;

@@ -91,10 +91,11 @@ __device__ __forceinline__ void store_out(const Params& p, int64_t idx, float v)
 // With one CTA per unit it writes output[r, h*group + i, :].  With split-K it
 // stores this CTA's merged partial, and the last CTA of the unit to arrive
 // (an atomic ticket; no CTA ever waits for another) merges all partials and
-// writes the output, then re-arms the ticket for the next call.
+// writes the output, then re-arms the ticket for the next call.  `scratch`
+// is shared memory for 2 * kMaxSplits * group floats (split-K only).
 template <int NW>
 __device__ __forceinline__ void finish_unit(const Params& p, int r, int h, int split, bool row_ok, const float* sm_m,
-                                            const float* sm_l, const float* sm_o, int GP) {
+                                            const float* sm_l, const float* sm_o, int GP, float* scratch) {
   const int G = p.group, D = p.D;
   const int64_t out_base = ((int64_t)r * p.nq + (int64_t)h * G) * D;
   if (p.splits == 1) {
@@ -121,8 +122,9 @@ __device__ __forceinline__ void finish_unit(const Params& p, int r, int h, int s
 
   // split-K: partial layout per (unit, split): o[G][D], m[G], l[G]
   const int unit = r * p.nkv + h;
-  const int64_t stride = (int64_t)G * (D + 2);
-  float* part = p.ws_partial + ((int64_t)unit * p.splits + split) * stride;
+  const int S = p.splits;
+  const int64_t stride = partial_stride(G, D);
+  float* part = p.ws_partial + ((int64_t)unit * S + split) * stride;
   for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
     const int i = idx / D, d = idx - i * D;
     float M = -CUDART_INF_F;
@@ -148,28 +150,49 @@ __device__ __forceinline__ void finish_unit(const Params& p, int r, int h, int s
   __shared__ int s_last;
   if (threadIdx.x == 0) {
     const uint32_t t = atomicAdd(p.ws_ticket + unit, 1u);
-    s_last = (t == (uint32_t)(p.splits - 1));
+    s_last = (t == (uint32_t)(S - 1));
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const float* base = p.ws_partial + (int64_t)unit * p.splits * stride;
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int i = idx / D;
+  const float* base = p.ws_partial + (int64_t)unit * S * stride;
+  // (1) every split's max and sum into shared memory, all loads in flight at once
+  float* s_m = scratch;               // [S][G]
+  float* s_w = scratch + kMaxSplits * G;  // [S][G]: weight of split s for head i
+  for (int k = threadIdx.x; k < S * G; k += blockDim.x) {
+    const int s = k / G, i = k - s * G;
+    s_m[k] = __ldcg(base + s * stride + G * D + i);
+    s_w[k] = __ldcg(base + s * stride + G * D + G + i);
+  }
+  __syncthreads();
+  // (2) per head: global max, denominator, and each split's normalised weight
+  for (int i = threadIdx.x; i < G; i += blockDim.x) {
     float M = -CUDART_INF_F;
-    for (int s = 0; s < p.splits; ++s) M = fmaxf(M, __ldcg(base + s * stride + G * D + i));
-    float val = 0.f;
-    if (row_ok && M != -CUDART_INF_F) {
-      float L = 0.f, O = 0.f;
-      for (int s = 0; s < p.splits; ++s) {
-        const float ms = __ldcg(base + s * stride + G * D + i);
-        const float e = exp2f(ms - M);  // an empty split has ms = -inf -> e = 0
-        L += __ldcg(base + s * stride + G * D + G + i) * e;
-        O += __ldcg(base + s * stride + idx) * e;
-      }
-      val = O / L;
+    for (int s = 0; s < S; ++s) M = fmaxf(M, s_m[s * G + i]);
+    float L = 0.f;
+    if (M != -CUDART_INF_F)
+      for (int s = 0; s < S; ++s) L += s_w[s * G + i] * exp2f(s_m[s * G + i] - M);
+    const bool live = row_ok && M != -CUDART_INF_F;
+    for (int s = 0; s < S; ++s) s_w[s * G + i] = live ? exp2f(s_m[s * G + i] - M) / L : 0.f;
+  }
+  __syncthreads();
+  // (3) output: four channels per thread, every split's float4 in flight together
+  for (int q4 = threadIdx.x; q4 < G * D / 4; q4 += blockDim.x) {
+    const int idx = q4 * 4, i = idx / D;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) {
+      const float w = s_w[s * G + i];
+      const float4 o = __ldcg(reinterpret_cast<const float4*>(base + s * stride + idx));
+      acc.x = fmaf(w, o.x, acc.x);
+      acc.y = fmaf(w, o.y, acc.y);
+      acc.z = fmaf(w, o.z, acc.z);
+      acc.w = fmaf(w, o.w, acc.w);
     }
-    store_out(p, out_base + idx, val);
+    store_out(p, out_base + idx, acc.x);
+    store_out(p, out_base + idx + 1, acc.y);
+    store_out(p, out_base + idx + 2, acc.z);
+    store_out(p, out_base + idx + 3, acc.w);
   }
   if (threadIdx.x == 0) p.ws_ticket[unit] = 0u;
 }

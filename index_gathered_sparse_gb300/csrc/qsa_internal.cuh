@@ -47,9 +47,18 @@ cudaError_t launch_mma_e4m3(const Params& p, cudaStream_t stream);
 int mma_ctas_per_sm_bf16(int group);
 int mma_ctas_per_sm_e4m3(int group);
 
+// Floats of one split-K partial: o[group][D], m[group], l[group], padded to a
+// multiple of 4 so every partial starts 16-byte aligned.
+__host__ __device__ inline int64_t partial_stride(int64_t group, int64_t D) {
+  return (group * (D + 2) + 3) / 4 * 4;
+}
+
 // Tensor-core kernel limits.
 constexpr int kMmaTile = 64;      // keys per pipeline stage (16 per warp)
 constexpr int kMmaMaxBand = 2048; // keys one CTA translates up front
 constexpr int kMmaThreads = 128;
+// Largest split count the fused split-K combine accepts (its per-split
+// weights live in shared memory).
+constexpr int kMaxSplits = 128;
 
 }  // namespace qsa

@@ -331,6 +331,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   float* sm_o = reinterpret_cast<float*>(smem);  // [NW][GP][D]
   float* sm_m = sm_o + NW * GP * C::D;
   float* sm_l = sm_m + NW * GP;
+  float* scratch = sm_l + NW * GP;  // split-K merge: 2 * kMaxSplits * group floats
+  static_assert((NW * GP * C::D + 2 * NW * GP + 2 * kMaxSplits * GP) * 4 <= C::STAGES * C::STAGE_BYTES,
+                "epilogue buffers must fit in the drained ring");
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -356,7 +359,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
         sm_o[(warp * GP + head) * C::D + d] = o[mt][nt][c];
       }
   __syncthreads();
-  finish_unit<NW>(p, r, h, split, ri.ok, sm_m, sm_l, sm_o, GP);
+  finish_unit<NW>(p, r, h, split, ri.ok, sm_m, sm_l, sm_o, GP, scratch);
 }
 
 template <int KIND, int NT>

@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(128) simt_kernel(const Params p) {
     for (int e = 0; e < EPL; ++e) sm_o[(warp * G + i) * D + lane * EPL + e] = acc[i][e];
   }
   __syncthreads();
-  finish_unit<NW>(p, r, h, 0, ri.ok, sm_m, sm_l, sm_o, G);
+  finish_unit<NW>(p, r, h, 0, ri.ok, sm_m, sm_l, sm_o, G, nullptr);  // never split
 }
 
 template <int ELEM, int D>

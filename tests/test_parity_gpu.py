@@ -153,6 +153,17 @@ def test_head_dim_64_and_odd_groups():
         assert_close(run_gpu(x), oracle.sparse_attention(x), dtype, f"{dtype} g{g}")
 
 
+def test_odd_groups_on_tensor_cores_with_split_k():
+    """Groups 3, 5 and 7 pad the 8-wide head tile; split-K partials of an odd
+    group must still start 16-byte aligned."""
+    for g in (3, 5, 7):
+        spec = wl.bf16_decode(seed=60 + g, batch=4, cache_range=(300, 900), width=384)
+        spec.num_kv_heads, spec.num_q_heads = 2, 2 * g
+        x = spec.build()
+        for kw in (dict(kernel=2, splits=1), dict(kernel=2, splits=3), dict(kernel=2, splits=6)):
+            assert_close(run_gpu(x, **kw), oracle.sparse_attention(x), "bf16", f"g{g} {kw}")
+
+
 def test_group_16_and_12_on_tensor_cores():
     for g in (16, 12):
         spec = wl.bf16_long_decode(seed=40 + g, batch=2, cache_range=(2000, 4000), runs=5)
