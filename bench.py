@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="bf16_decode")
     ap.add_argument("--kernel", type=int, default=0, help="force 1 CUDA-core / 2 tensor-core kernel")
-    ap.add_argument("--splits", type=int, default=0, help="force CTAs per (row, kv head)")
+    ap.add_argument("--splits", type=int, default=0, help="kernel 2: force CTAs per (row, kv head)")
+    ap.add_argument("--ctas", type=int, default=0, help="kernel 3: force the persistent grid size")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -259,14 +260,14 @@ def main():
     d = wl.to_torch(x, dev)
     code = {"f32": B.QSA_F32, "bf16": B.QSA_BF16, "e4m3": B.QSA_F8E4M3}[x.dtype]
     plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, x.selection_width, x.group,
-                      kernel=args.kernel, splits=args.splits)
+                      kernel=args.kernel, splits=args.splits, ctas=args.ctas)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def call():
-        B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits)
+        B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas)
 
     def barrier():
         torch.cuda.synchronize()
@@ -342,7 +343,7 @@ def main():
     achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": recorded_traffic(x.name), "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs copy)",
-                "kernel": "qsa mma_kernel" if plan["kernel"] == 2 else "qsa simt_kernel",
+                "kernel": {1: "qsa simt_kernel", 2: "qsa mma_kernel", 3: "qsa stream_kernel"}[plan["kernel"]],
                 "algorithmic_bytes_per_launch": alg_bytes}
 
     cpu = None

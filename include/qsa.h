@@ -118,8 +118,8 @@ typedef enum qsa_status {
  *   stream            cudaStream_t to enqueue on
  *
  * Kernel coverage: output F32 or BF16; head_dim 64 or 128.  BF16 and F8E4M3
- * with head_dim 128 run on the tensor-core kernel (group 1..16); the rest on
- * the CUDA-core kernel (group 1..8 or 16).  Device pointers must be 16-byte aligned, and
+ * with head_dim 128 run on the persistent tensor-core kernel (group 1..16);
+ * the rest on the CUDA-core kernel (group 1..8 or 16).  Device pointers must be 16-byte aligned, and
  * page_stride * element size a multiple of 16 bytes.  kv_blocks may span up
  * to 64 GiB.
  *
@@ -129,9 +129,10 @@ typedef enum qsa_status {
  *
  * When more than one CTA shares a (row, kv head), the call uses a split-K
  * workspace owned by the library, one per (device, stream), grown on demand
- * with cudaMalloc; call qsa_reserve_workspace first to keep allocation off
- * the hot path and out of graph capture.  Calls on the same stream are
- * ordered; calls on different streams use different workspaces.
+ * with cudaMalloc; call qsa_reserve_workspace with qsa_plan's figure first to
+ * keep allocation off the hot path and out of graph capture.  Calls on the
+ * same stream are ordered; calls on different streams use different
+ * workspaces.
  */
 QSA_API qsa_status qsa_sparse_attention_ragged_paged(
     qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks,
@@ -141,9 +142,12 @@ QSA_API qsa_status qsa_sparse_attention_ragged_paged(
 
 /* Launch controls for tests and measurement.  Zero fields mean "choose". */
 typedef struct qsa_options {
-  int32_t kernel;    /* 0 auto, 1 CUDA-core kernel, 2 tensor-core kernel */
-  int32_t splits;    /* 0 auto, else CTAs per (row, kv head) along the selection */
-  int32_t reserved[6];
+  int32_t kernel;    /* 0 auto, 1 CUDA-core kernel, 2 tensor-core kernel with one
+                        CTA per (row, kv head[, split]), 3 persistent stream-K
+                        tensor-core kernel (the default where it applies) */
+  int32_t splits;    /* kernel 2: 0 auto, else CTAs per (row, kv head) */
+  int32_t ctas;      /* kernel 3: 0 auto (one per SM), else the persistent grid size */
+  int32_t reserved[5];
 } qsa_options;
 
 /* Same as qsa_sparse_attention_ragged_paged, with explicit launch controls

@@ -31,7 +31,8 @@ class qsa_tensor(ctypes.Structure):
 
 
 class qsa_options(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int32), ("splits", ctypes.c_int32), ("reserved", ctypes.c_int32 * 6)]
+    _fields_ = [("kernel", ctypes.c_int32), ("splits", ctypes.c_int32), ("ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 5)]
 
 
 class LibraryMissing(RuntimeError):
@@ -150,10 +151,11 @@ def _kv_desc(kv: torch.Tensor, page_stride: int) -> qsa_tensor:
 def qsa_sparse_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
                                       kv_lookup_table, max_prompt_length, max_cache_length, layer_idx,
                                       token_indices, counts, scale, group, stream=None, *, kernel: int = 0,
-                                      splits: int = 0) -> None:
+                                      splits: int = 0, ctas: int = 0) -> None:
     """One layer of QSA sparse attention on the GPU (asynchronous on
     ``stream``, default: PyTorch's current stream).  Raises QSAError on a
-    non-OK status.  ``kernel`` / ``splits`` force a launch choice (tests)."""
+    non-OK status.  ``kernel`` / ``splits`` / ``ctas`` force a launch choice
+    (tests and sweeps; see qsa_options)."""
     lib = load_library()
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
@@ -165,19 +167,19 @@ def qsa_sparse_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, p
         int(max_cache_length), int(layer_idx), _contig(token_indices, "token_indices"), _contig(counts, "counts"),
         float(scale), int(group), ctypes.c_void_p(stream),
     ]
-    if kernel or splits:
-        opt = qsa_options(kernel=kernel, splits=splits)
+    if kernel or splits or ctas:
+        opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas)
         _check(lib.qsa_sparse_attention_ragged_paged_ex(*args, ctypes.byref(opt)))
     else:
         _check(lib.qsa_sparse_attention_ragged_paged(*args))
 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,
-             kernel: int = 0, splits: int = 0) -> dict:
+             kernel: int = 0, splits: int = 0, ctas: int = 0) -> dict:
     lib = load_library()
     k, s = ctypes.c_int32(), ctypes.c_int32()
     c, w = ctypes.c_int64(), ctypes.c_size_t()
-    opt = qsa_options(kernel=kernel, splits=splits)
+    opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas)
     _check(lib.qsa_plan(dtype, total_q, num_kv_heads, head_dim, selection_width, group, ctypes.byref(opt),
                         ctypes.byref(k), ctypes.byref(s), ctypes.byref(c), ctypes.byref(w)))
     return {"kernel": k.value, "splits": s.value, "ctas": c.value, "workspace_bytes": w.value}

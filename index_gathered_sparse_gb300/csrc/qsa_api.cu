@@ -68,6 +68,8 @@ struct Resolved {
   int band = 0;
   int64_t ctas = 0;
   size_t ws_partial_bytes = 0, ws_bytes = 0;
+  size_t ws_tickets = 0;
+  qsa::StreamPlan sp{};
 };
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -78,20 +80,21 @@ qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
   const bool mma_ok = (R.elem == qsa::kBF16 || R.elem == qsa::kE4M3) && R.D == 128;
   const bool simt_ok = group <= 8 || group == 16;
   const int want = opt ? opt->kernel : 0;
-  if (want == 2) {
-    if (!mma_ok) return fail(QSA_ERR_UNSUPPORTED, "tensor-core kernel needs BF16 or F8E4M3 with head_dim 128");
-    R.kernel = 2;
+  if (want == 2 || want == 3) {
+    if (!mma_ok) return fail(QSA_ERR_UNSUPPORTED, "tensor-core kernels need BF16 or F8E4M3 with head_dim 128");
+    R.kernel = want;
   } else if (want == 1) {
     if (!simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
     R.kernel = 1;
   } else if (want == 0) {
-    R.kernel = mma_ok ? 2 : 1;
+    R.kernel = mma_ok ? 3 : 1;
     if (R.kernel == 1 && !simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
   } else {
-    return fail(QSA_ERR_ARG, "options.kernel must be 0, 1 or 2");
+    return fail(QSA_ERR_ARG, "options.kernel must be 0, 1, 2 or 3");
   }
-  if (opt && opt->splits < 0) return fail(QSA_ERR_ARG, "options.splits must be >= 0");
-  if (R.kernel == 1 && opt && opt->splits > 1) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel has no split-K");
+  if (opt && (opt->splits < 0 || opt->ctas < 0)) return fail(QSA_ERR_ARG, "options.splits and options.ctas must be >= 0");
+  if (R.kernel != 2 && opt && opt->splits > 1) return fail(QSA_ERR_UNSUPPORTED, "only kernel 2 takes options.splits");
+  if (R.kernel != 3 && opt && opt->ctas > 0) return fail(QSA_ERR_UNSUPPORTED, "only kernel 3 takes options.ctas");
   return QSA_OK;
 }
 
@@ -226,6 +229,40 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     R.ws_bytes = R.ws_partial_bytes = 0;
     return QSA_OK;
   }
+  if (R.kernel == 3) {
+    // Persistent stream-K: units of HPU adjacent kv heads, TILE keys per
+    // 32 KB stage, one CTA per SM over equal ranges of virtual tiles.
+    qsa::StreamPlan& sp = R.sp;
+    sp.HPU = R.nkv % 4 == 0 ? 4 : R.nkv % 2 == 0 ? 2 : 1;
+    sp.NG = (int32_t)(R.nkv / sp.HPU);
+    const int64_t tile = (R.elem == qsa::kBF16 ? 16 : 32) * (4 / sp.HPU);
+    sp.VT = (int32_t)std::max<int64_t>(1, (R.W + tile - 1) / tile);
+    sp.U = (int32_t)(R.total_q * sp.NG);
+    sp.T = (int64_t)sp.U * sp.VT;
+    int64_t G = opt && opt->ctas > 0 ? opt->ctas : 0;
+    if (!G) {
+      std::lock_guard<std::mutex> lk(g_mu);
+      DeviceState& st = g_dev[dev];
+      if (!st.sms) {
+        const cudaError_t e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+      }
+      G = st.sms;
+    }
+    G = std::min<int64_t>(G, sp.T);
+    // a unit is shared by at most kmax CTAs; the last one merges their records in
+    // shared memory sized for 32, so spread less when ranges get too short
+    auto kmax = [&](int64_t g) { return (sp.VT + sp.T / g - 1) / (sp.T / g) + 1; };
+    while (G > 1 && kmax(G) > 32) G = std::max<int64_t>(1, G / 2);
+    sp.G = (int32_t)std::max<int64_t>(G, 1);
+    sp.rec_floats = (int32_t)(sp.HPU * qsa::partial_stride(group, R.D));
+    R.splits = 1;
+    R.ctas = sp.G;
+    R.ws_partial_bytes = ((size_t)2 * sp.G * sp.rec_floats * 4 + 255) / 256 * 256;
+    R.ws_tickets = (size_t)sp.U;
+    R.ws_bytes = R.ws_partial_bytes + R.ws_tickets * 4;
+    return QSA_OK;
+  }
   const int64_t T = qsa::kMmaTile;
   const int64_t min_splits = R.W > 0 ? (R.W + qsa::kMmaMaxBand - 1) / qsa::kMmaMaxBand : 1;
   int64_t splits;
@@ -276,6 +313,7 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   if (R.splits > 1) {
     const int64_t units = R.total_q * R.nkv;
     R.ws_partial_bytes = ((size_t)(units * R.splits * qsa::partial_stride(group, R.D) * 4) + 255) / 256 * 256;
+    R.ws_tickets = (size_t)units;
     R.ws_bytes = R.ws_partial_bytes + (size_t)units * 4;
   } else {
     R.ws_bytes = R.ws_partial_bytes = 0;
@@ -373,9 +411,9 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
     s = ensure_status(st);
     if (s != QSA_OK) return s;
     p.status = st.status;
-    if (R.splits > 1) {
+    if (R.ws_bytes > 0) {
       Workspace* ws = nullptr;
-      s = ensure_workspace(st, stream, R.ws_partial_bytes, (size_t)(R.total_q * R.nkv), &ws);
+      s = ensure_workspace(st, stream, R.ws_partial_bytes, R.ws_tickets, &ws);
       if (s != QSA_OK) return s;
       p.ws_partial = static_cast<float*>(ws->partial);
       p.ws_ticket = ws->tickets;
@@ -413,8 +451,10 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (R.kernel == 1)
     e = qsa::launch_simt(p, R.elem, st);
-  else
+  else if (R.kernel == 2)
     e = R.elem == qsa::kBF16 ? qsa::launch_mma_bf16(p, st) : qsa::launch_mma_e4m3(p, st);
+  else
+    e = R.elem == qsa::kBF16 ? qsa::launch_stream_bf16(p, R.sp, st) : qsa::launch_stream_e4m3(p, R.sp, st);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return QSA_OK;
 }
@@ -467,10 +507,10 @@ qsa_status qsa_reserve_workspace(void* stream, size_t bytes) {
   DeviceState& st = g_dev[dev];
   qsa_status s = ensure_status(st);
   if (s != QSA_OK) return s;
-  // the reservation covers tickets for as many (row, kv head) units as
-  // `bytes` of partials could serve at the smallest partial (2 splits x 1 head x 64 + 2 floats)
+  // `bytes` (qsa_plan's figure) covers the partials; size the tickets as if
+  // all of it were tickets, which bounds any split of that figure
   Workspace* ws = nullptr;
-  return bytes ? ensure_workspace(st, stream, bytes, bytes / (2 * 66 * sizeof(float)) + 1, &ws) : QSA_OK;
+  return bytes ? ensure_workspace(st, stream, bytes, bytes / sizeof(uint32_t) + 1, &ws) : QSA_OK;
 }
 
 qsa_status qsa_release_device_state(void) {

@@ -36,6 +36,17 @@ struct Params {
   int32_t band;      // keys per split band (multiple of the key tile)
 };
 
+// Launch plan of the persistent stream-K kernel (computed on the host).
+struct StreamPlan {
+  int64_t T;          // virtual key tiles over all units
+  int32_t U;          // units: query row x group of HPU kv heads
+  int32_t VT;         // virtual tiles per unit (selection_width / TILE, rounded up)
+  int32_t G;          // CTAs (one per SM at most)
+  int32_t NG;         // kv-head groups per row (num_kv_heads / HPU)
+  int32_t HPU;        // kv heads per unit: 4, 2 or 1
+  int32_t rec_floats; // floats of one partial record (HPU heads)
+};
+
 // Element type tags.
 enum Elem { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
 
@@ -43,6 +54,8 @@ enum Elem { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
 cudaError_t launch_simt(const Params& p, int elem, cudaStream_t stream);
 cudaError_t launch_mma_bf16(const Params& p, cudaStream_t stream);
 cudaError_t launch_mma_e4m3(const Params& p, cudaStream_t stream);
+cudaError_t launch_stream_bf16(const Params& p, const StreamPlan& sp, cudaStream_t stream);
+cudaError_t launch_stream_e4m3(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 // CTAs of the tensor-core kernel that fit on one SM (for the split planner).
 int mma_ctas_per_sm_bf16(int group);
 int mma_ctas_per_sm_e4m3(int group);

@@ -1,0 +1,625 @@
+// Persistent stream-K kernel for QSA gather-GQA sparse attention, BF16 and FP8
+// e4m3 caches, head_dim 128 (QSASparseAttentionRaggedPaged: "Gather-GQA over
+// the token indices a QSA selection names"; its `warps` and `unroll`
+// parameters: warps per CTA, gathered keys loaded before any is consumed).
+//
+// Work.  A unit is one query row and a group of HPU adjacent kv heads (4 when
+// num_kv_heads allows): the K rows of those heads are HPU*256 B (BF16) or
+// HPU*128 B (FP8) contiguous in a cache slot, so one translated position
+// feeds HPU heads with one contiguous read.  Every unit owns VT = W / TILE
+// "virtual" key tiles; the launch has one CTA per SM, and CTA c processes the
+// contiguous range [c*T/G, (c+1)*T/G) of all T virtual tiles (stream-K), so
+// the load is balanced to a tile and at most the first and the last unit of a
+// range are shared with other CTAs.  Tiles past a unit's count are skipped.
+//
+// Pipeline.  Everything a tile needs is fetched by cp.async in hops spaced H =
+// STAGES - 1 loop iterations apart, so each hop has landed when the next one
+// reads it and no CTA ever waits on a dependent load in steady state:
+//     unit meta (counts, cache_lengths)   ~ H + 1 units ahead of the index hop
+//     indices  (token_indices)            3H + 1 tiles ahead of compute
+//     page     (kv_lookup_table entries)  2H + 1 tiles ahead
+//     offsets  (computed from both)        H + 1 tiles ahead
+//     K and V rows                         H     tiles ahead (the stage ring)
+// Warps own heads (WPH = 4 / HPU warps per head split a tile's keys) and run
+// the keys-on-M / heads-on-N mma.sync scheme: S^T = K Q^T, online softmax in
+// base 2, P^T by movmatrix, O^T += V^T P^T.  A unit's end merges the warps in
+// shared memory and writes the output, or — for a shared unit — a partial
+// record; after its range, each CTA arrives on the shared units' tickets and
+// the last arrival merges the records (no CTA ever waits for another).
+#pragma once
+
+#include "qsa_mma.cuh"
+
+namespace qsa {
+
+template <int KIND, int NT, int HPU>
+struct StreamCfg {
+  static constexpr int D = 128;
+  static constexpr int ELEM = KIND == kBF16 ? 2 : 1;
+  static constexpr int ROWB = D * ELEM;             // one head's K (or V) row
+  static constexpr int KEYB = HPU * ROWB;           // a unit's K (or V) bytes per key, contiguous
+  static constexpr int SROW = KEYB + 16;            // padded shared-memory row (conflict-free ldmatrix)
+  static constexpr int TILE = (KIND == kBF16 ? 16 : 32) * (4 / HPU);  // keys per stage: 32 KB of K+V
+  static constexpr int WPH = 4 / HPU;               // warps per head
+  static constexpr int KPW = TILE / WPH;            // keys per warp per tile
+  static constexpr int MSL = KPW / 16;              // 16-key MMA slices per warp per tile
+  static constexpr int KV_BYTES = TILE * SROW;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int GP = 8 * NT;                 // padded query heads per kv head
+  static constexpr int KSTEPS = KIND == kBF16 ? 8 : 4;
+  static constexpr int CPK = 2 * KEYB / 16;         // 16-byte chunks per key (K and V)
+  static constexpr int CHUNKS = TILE * CPK;         // per stage
+  static constexpr int RT = 16;                     // tile-record ring (positions, pages, offsets)
+  static constexpr int MR = 32;                     // unit-meta ring
+  static constexpr int MAXOFF = 1024;               // input_row_offsets entries kept in shared memory
+  static constexpr int EPI_FLOATS = 4 * GP * D + 2 * 4 * GP;
+  static constexpr int FIXED = EPI_FLOATS * 4 + 3 * RT * TILE * 4 + MR * 16 + MAXOFF * 4;
+  static constexpr int STAGES = (5 * STAGE_BYTES + FIXED <= 232448) ? 5 : 4;
+  static constexpr int H = STAGES - 1;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
+  static_assert(CHUNKS % kMmaThreads == 0, "stage copy split");
+  static_assert(KPW % 16 == 0, "warp key slices are 16 keys");
+  static_assert(3 * H + 2 <= RT, "tile-record ring too small");
+  static_assert(4 * H + 4 <= MR, "unit-meta ring too small");
+  static_assert(SMEM <= 232448, "shared memory");
+};
+
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+
+template <int KIND, int NT, int HPU>
+__global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, const StreamPlan sp) {
+  using C = StreamCfg<KIND, NT, HPU>;
+  constexpr int H = C::H, S = C::STAGES, TILE = C::TILE, RT = C::RT, MR = C::MR, GP = C::GP;
+  extern __shared__ __align__(128) unsigned char smem[];
+  float* epi = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);  // [4][GP][D] + m[4][GP] + l[4][GP]
+  int32_t* s_pos = reinterpret_cast<int32_t*>(epi + C::EPI_FLOATS);  // [RT][TILE]
+  uint32_t* s_page = reinterpret_cast<uint32_t*>(s_pos + RT * TILE); // [RT][TILE]
+  uint32_t* s_off = s_page + RT * TILE;                               // [RT][TILE]
+  int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
+  uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
+  __shared__ int s_merge[2];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
+  const int hh = warp / C::WPH, kp = warp % C::WPH;
+  const int VT = sp.VT;
+  const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
+  if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
+  const int u_first = (int)(t0 / VT), u_last = (int)((t1 - 1) / VT);
+  uint32_t bad = 0;
+
+  auto unit_row = [&](int u) { return p.total_q - 1 - u / sp.NG; };
+  auto unit_hg = [&](int u) { return u % sp.NG; };
+  // the CTA whose range holds virtual tile x, and a unit's contributing CTAs
+  auto cta_of = [&](int64_t x) { return (int)(((x + 1) * sp.G - 1) / sp.T); };
+  auto first_cta = [&](int u) { return cta_of((int64_t)u * VT); };
+  auto contributors = [&](int u) { return cta_of((int64_t)(u + 1) * VT - 1) - first_cta(u) + 1; };
+  // a shared unit's partial record: two per CTA (its first and its last unit)
+  auto record = [&](int c, int u) {
+    const int uf = (int)((int64_t)c * sp.T / sp.G / VT);
+    return p.ws_partial + ((int64_t)2 * c + (u == uf ? 0 : 1)) * sp.rec_floats;
+  };
+
+  // ---------------- unit meta ----------------
+  auto mslot = [&](int u) { return ((u - u_first) % MR) * 4; };
+  // sequence of row r, -1 when no sequence owns it
+  auto find_seq = [&](int r) -> int {
+    const bool in_smem = p.batch + 1 <= C::MAXOFF;
+    auto off = [&](int k) { return in_smem ? s_rowoff[k] : __ldg(p.row_offsets + k); };
+    int lo = 0, hi = p.batch;  // largest b in [0, batch] with off[b] <= r
+    if (off(0) > (uint32_t)r) return -1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (off(mid) <= (uint32_t)r) lo = mid; else hi = mid - 1;
+    }
+    if (lo >= p.batch || (uint32_t)r >= off(lo + 1)) return -1;
+    return lo;
+  };
+  auto issue_meta = [&](int u) {  // thread 0 only
+    const int r = unit_row(u), m = mslot(u);
+    const int b = find_seq(r);
+    s_meta[m + 2] = b;
+    if (b >= 0) {
+      const bool in_smem = p.batch + 1 <= C::MAXOFF;
+      s_meta[m + 3] = (int32_t)((in_smem ? s_rowoff[b + 1] : __ldg(p.row_offsets + b + 1)) -
+                                (in_smem ? s_rowoff[b] : __ldg(p.row_offsets + b)));
+      cp_async4(smem_addr(&s_meta[m + 0]), p.counts + r);
+      cp_async4(smem_addr(&s_meta[m + 1]), p.cache_lengths + b);
+    } else {
+      s_meta[m + 0] = 0;
+      s_meta[m + 1] = 0;
+      s_meta[m + 3] = 0;
+      bad |= QSA_STATUS_BAD_ROW;
+    }
+  };
+  int meta_issued = u_first, meta_landed = u_first;
+  int hist[H];  // meta_issued at the end of each of the last H iterations
+  auto issue_meta_upto = [&](int u) {
+    u = min(u, u_last);
+    if (tid == 0)
+      for (int v = meta_issued; v <= u; ++v) issue_meta(v);
+    meta_issued = max(meta_issued, u + 1);
+  };
+  // makes unit u's meta readable (a full wait when it has not landed yet)
+  auto ensure_meta = [&](int u) {
+    if (u >= meta_issued) issue_meta_upto(u);
+    if (u >= meta_landed) {
+      cp_async_wait_all();
+      __syncthreads();
+      meta_landed = meta_issued;
+#pragma unroll
+      for (int k = 0; k < H; ++k) hist[k] = meta_issued;
+    }
+  };
+  auto n_of = [&](int u) {
+    const int m = mslot(u);
+    return s_meta[m + 2] < 0 ? 0 : min(max(s_meta[m + 0], 0), p.W);
+  };
+  auto kv_len_of = [&](int u) {
+    const int m = mslot(u);
+    return (int64_t)(uint32_t)s_meta[m + 1] + (int64_t)s_meta[m + 3];
+  };
+
+  // ---------------- tile cursors ----------------
+  // Ordinals run over each unit's real tiles inside this range (at least one
+  // per unit: a unit with none gets one empty tile so it is still finished).
+  auto j_lo = [&](int u) { return u == u_first ? (int)(t0 - (int64_t)u * VT) : 0; };
+  auto j_hi = [&](int u) { return u == u_last ? (int)(t1 - (int64_t)u * VT) : VT; };
+  auto last_j = [&](int u) {
+    const int real_hi = min(j_hi(u), (n_of(u) + TILE - 1) / TILE);
+    return max(j_lo(u), real_hi - 1);
+  };
+  auto next_tile = [&](int64_t x) -> int64_t {  // -1 past the range
+    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+    ensure_meta(u);
+    if (j < last_j(u)) return x + 1;
+    if (u >= u_last) return -1;
+    ensure_meta(u + 1);
+    return (int64_t)(u + 1) * VT;  // j_lo(u + 1) == 0
+  };
+  auto keys_in = [&](int u, int j) { return min(max(n_of(u) - j * TILE, 0), TILE); };
+
+  // ---------------- hops ----------------
+  auto idx_hop = [&](int64_t x, int o) {
+    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
+    const int32_t* src = p.indices + (int64_t)unit_row(u) * p.W + (int64_t)j * TILE;
+    for (int k = tid; k < kt; k += kMmaThreads) cp_async4(smem_addr(&s_pos[slot + k]), src + k);
+  };
+  auto page_hop = [&](int64_t x, int o) {
+    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
+    const int64_t kvl = kv_len_of(u);
+    const uint32_t* trow = p.table + (int64_t)s_meta[mslot(u) + 2] * p.max_pages;
+    for (int k = tid; k < kt; k += kMmaThreads) {
+      const int32_t pos = s_pos[slot + k];
+      uint32_t so = kInvalidOff;
+      if (pos < 0 || (int64_t)pos >= kvl) {
+        bad |= QSA_STATUS_BAD_INDEX;
+      } else {
+        const uint32_t lp = (uint32_t)pos / (uint32_t)p.P;
+        if (lp >= (uint32_t)p.max_pages) {
+          bad |= QSA_STATUS_BAD_PAGE;
+        } else {
+          cp_async4(smem_addr(&s_page[slot + k]), trow + lp);
+          so = (uint32_t)pos - lp * (uint32_t)p.P;  // slot within the page
+        }
+      }
+      s_off[slot + k] = so;
+    }
+  };
+  auto off_hop = [&](int64_t x, int o) {
+    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
+    const int64_t head0 = p.k_layer_bytes + (int64_t)unit_hg(u) * HPU * p.head_bytes;
+    for (int k = tid; k < kt; k += kMmaThreads) {
+      const uint32_t so = s_off[slot + k];
+      if (so == kInvalidOff) continue;
+      const uint32_t page = s_page[slot + k];
+      if (page >= p.num_pages) {
+        bad |= QSA_STATUS_BAD_PAGE;
+        s_off[slot + k] = kInvalidOff;
+      } else {
+        s_off[slot + k] = (uint32_t)(((int64_t)page * p.page_pitch_bytes + head0 + (int64_t)so * p.slot_bytes) >> 4);
+      }
+    }
+  };
+  auto kv_hop = [&](int64_t x, int o) {
+    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
+    unsigned char* sb = smem + (o % S) * C::STAGE_BYTES;
+#pragma unroll 4
+    for (int i = 0; i < C::CHUNKS / kMmaThreads; ++i) {
+      const int c = i * kMmaThreads + tid;
+      const int key = c / C::CPK, w = c - key * C::CPK;
+      const int kv = w / (C::CPK / 2), ch = w - kv * (C::CPK / 2);
+      const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
+      const bool live = off != kInvalidOff;
+      const unsigned char* src = live ? p.kv + (int64_t)off * 16 + (kv ? p.v_minus_k_bytes : 0) + ch * 16 : p.kv;
+      cp_async16(smem_addr(sb + kv * C::KV_BYTES + key * C::SROW + ch * 16), src, live ? 16u : 0u);
+    }
+  };
+
+  // ---------------- per-warp attention state ----------------
+  uint32_t qf[NT][C::KSTEPS][2], qn[NT][C::KSTEPS][2];
+  auto load_q = [&](int u, uint32_t (&dst)[NT][C::KSTEPS][2]) {
+    const int r = unit_row(u), h = unit_hg(u) * HPU + hh;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int head = nt * 8 + gid;
+      const bool live = head < p.group;
+      const unsigned char* qrow =
+          p.q + (((int64_t)r * p.nq + (int64_t)h * p.group + (live ? head : 0)) * C::D) * C::ELEM;
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        const int e0 = KIND == kBF16 ? ks * 16 + 2 * tig : ks * 32 + 4 * tig;
+        const int e1 = KIND == kBF16 ? e0 + 8 : e0 + 16;
+        dst[nt][ks][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + e0 * C::ELEM)) : 0u;
+        dst[nt][ks][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + e1 * C::ELEM)) : 0u;
+      }
+    }
+  };
+  float m_run[NT][2], l_run[NT][2], o[8][NT][4];
+  auto reset_state = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m_run[nt][0] = m_run[nt][1] = -CUDART_INF_F;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    }
+  };
+  const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_col = ((lane >> 4) & 1) * 16;
+  const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8, t_col = ((lane >> 3) & 1) * 16;
+
+  auto compute_tile = [&](int64_t x, int ord) {
+    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+    const int kt = keys_in(u, j), slot = (ord % RT) * TILE;
+    const unsigned char* sb = smem + (ord % S) * C::STAGE_BYTES;
+#pragma unroll
+    for (int sl = 0; sl < C::MSL; ++sl) {
+      const int k0 = kp * C::KPW + sl * 16;
+      const int kA = k0 + gid, kB = kA + 8;
+      const bool vA = kA < kt && s_off[slot + kA] != kInvalidOff;
+      const bool vB = kB < kt && s_off[slot + kB] != kInvalidOff;
+      if (!__any_sync(0xffffffffu, vA || vB)) continue;
+      const uint32_t kbase = smem_addr(sb) + k0 * C::SROW + hh * C::ROWB;
+      const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + k0 * C::SROW + hh * C::ROWB;
+      float s[NT][4], s2[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {  // two accumulator chains halve the dependent-MMA latency
+        uint32_t a[4];
+        ldsm_x4(kbase + a_row * C::SROW + ks * 32 + a_col, a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          if constexpr (KIND == kBF16) {
+            if (ks & 1) mma_bf16(s2[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+            else mma_bf16(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+          } else {
+            if (ks & 1) mma_e4m3(s2[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+            else mma_e4m3(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
+          }
+        }
+      }
+      uint32_t pb[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float pv[4];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const float x0 = vA ? (s[nt][c] + s2[nt][c]) * p.scale_log2 : -CUDART_INF_F;
+          const float x1 = vB ? (s[nt][2 + c] + s2[nt][2 + c]) * p.scale_log2 : -CUDART_INF_F;
+          float mx = fmaxf(x0, x1);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(m_run[nt][c], mx);
+          const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
+          const float alpha = exp2f(m_run[nt][c] - muse);
+          const float p0 = exp2f(x0 - muse), p1 = exp2f(x1 - muse);
+          l_run[nt][c] = l_run[nt][c] * alpha + p0 + p1;
+          m_run[nt][c] = mnew;
+          pv[c] = p0;
+          pv[2 + c] = p1;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[mt][nt][c] *= alpha;
+              o[mt][nt][2 + c] *= alpha;
+            }
+          }
+        }
+        const uint32_t top = KIND == kBF16 ? pack_bf16(pv[0], pv[1]) : pack_f16(pv[0], pv[1]);
+        const uint32_t bot = KIND == kBF16 ? pack_bf16(pv[2], pv[3]) : pack_f16(pv[2], pv[3]);
+        pb[nt][0] = movmatrix_t(top);
+        pb[nt][1] = movmatrix_t(bot);
+      }
+      if constexpr (KIND == kBF16) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          uint32_t a[4];
+          ldsm_x4_t(vbase + t_row * C::SROW + mt * 32 + t_col, a);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+        }
+      } else {
+#pragma unroll
+        for (int pr = 0; pr < 4; ++pr) {
+          uint32_t r4[4];
+          ldsm_x4_t(vbase + t_row * C::SROW + pr * 32 + t_col, r4);
+          uint32_t ae[4], ao[4];
+          const uint32_t q0 = __byte_perm(r4[0], 0, 0x3120), q1 = __byte_perm(r4[1], 0, 0x3120);
+          const uint32_t q2 = __byte_perm(r4[2], 0, 0x3120), q3 = __byte_perm(r4[3], 0, 0x3120);
+          ae[0] = e4m3x2_to_f16x2(q0 & 0xFFFFu);
+          ae[1] = e4m3x2_to_f16x2(q0 >> 16);
+          ae[2] = e4m3x2_to_f16x2(q2 & 0xFFFFu);
+          ae[3] = e4m3x2_to_f16x2(q2 >> 16);
+          ao[0] = e4m3x2_to_f16x2(q1 & 0xFFFFu);
+          ao[1] = e4m3x2_to_f16x2(q1 >> 16);
+          ao[2] = e4m3x2_to_f16x2(q3 & 0xFFFFu);
+          ao[3] = e4m3x2_to_f16x2(q3 >> 16);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_f16(o[2 * pr][nt], ae, pb[nt][0], pb[nt][1]);
+            mma_f16(o[2 * pr + 1][nt], ao, pb[nt][0], pb[nt][1]);
+          }
+        }
+      }
+    }
+  };
+
+  // End of a unit: merge the WPH warps of each head in shared memory, then
+  // write the output (unit owned by this CTA) or this CTA's partial record.
+  int pend[2] = {-1, -1}, npend = 0;
+  auto finish = [&](int u) {
+    float* sm_o = epi;
+    float* sm_m = epi + 4 * GP * C::D;
+    float* sm_l = sm_m + 4 * GP;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float l = l_run[nt][c];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        if (gid == 0) {
+          sm_m[warp * GP + nt * 8 + 2 * tig + c] = m_run[nt][c];
+          sm_l[warp * GP + nt * 8 + 2 * tig + c] = l;
+        }
+      }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int head = nt * 8 + 2 * tig + (c & 1);
+          const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
+          sm_o[(warp * GP + head) * C::D + d] = o[mt][nt][c];
+        }
+    __syncthreads();
+    const int G = p.group, D = C::D;
+    const int r = unit_row(u), hg = unit_hg(u);
+    const bool row_ok = s_meta[mslot(u) + 2] >= 0;
+    const bool own = contributors(u) == 1;
+    float* rec = own ? nullptr : record(blockIdx.x, u);
+    const int64_t stride = partial_stride(G, D);
+    for (int idx = tid; idx < HPU * G * D; idx += kMmaThreads) {
+      const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
+      float M = -CUDART_INF_F;
+#pragma unroll
+      for (int k = 0; k < C::WPH; ++k) M = fmaxf(M, sm_m[(h2 * C::WPH + k) * GP + i]);
+      float L = 0.f, O = 0.f;
+      if (M != -CUDART_INF_F) {
+#pragma unroll
+        for (int k = 0; k < C::WPH; ++k) {
+          const int w = h2 * C::WPH + k;
+          const float e = exp2f(sm_m[w * GP + i] - M);
+          L += sm_l[w * GP + i] * e;
+          O += sm_o[(w * GP + i) * D + d] * e;
+        }
+      }
+      if (own) {
+        store_out(p, ((int64_t)r * p.nq + (int64_t)(hg * HPU + h2) * G + i) * D + d,
+                  row_ok && M != -CUDART_INF_F ? O / L : 0.f);
+      } else {
+        float* part = rec + h2 * stride;
+        part[rem] = O;
+        if (d == 0) {
+          part[G * D + i] = M;
+          part[G * D + G + i] = L;
+        }
+      }
+    }
+    if (!own) pend[npend++] = u;
+    __syncthreads();  // the epilogue buffer is free again
+    reset_state();
+  };
+
+  // ---------------- prologue ----------------
+  if (p.batch + 1 <= C::MAXOFF)
+    for (int k = tid; k <= p.batch; k += kMmaThreads) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
+  cp_async_wait_all();
+  __syncthreads();
+  issue_meta_upto(u_first + H + 1);
+  cp_async_wait_all();
+  __syncthreads();
+  meta_landed = meta_issued;
+#pragma unroll
+  for (int k = 0; k < H; ++k) hist[k] = meta_issued;
+  load_q(u_first, qf);
+  if (u_first < u_last) load_q(u_first + 1, qn);
+  reset_state();
+
+  int64_t xi = t0, xp = t0, xo = t0, xk = t0;
+  int oi = 0, op = 0, oo = 0, ok = 0;
+  for (int n = 0; n <= 3 * H && xi >= 0; ++n) {
+    idx_hop(xi, oi++);
+    xi = next_tile(xi);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int n = 0; n <= 2 * H && xp >= 0; ++n) {
+    page_hop(xp, op++);
+    xp = next_tile(xp);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  for (int n = 0; n <= H && xo >= 0; ++n) {
+    off_hop(xo, oo++);
+    xo = next_tile(xo);
+  }
+  __syncthreads();
+  for (int n = 0; n < H; ++n) {
+    if (xk >= 0) {
+      kv_hop(xk, ok++);
+      xk = next_tile(xk);
+    }
+    cp_async_commit();
+  }
+
+  // ---------------- main loop: one tile per iteration ----------------
+  int64_t xc = t0;
+  int oc = 0;
+  while (xc >= 0) {
+    cp_async_wait<H - 1>();
+    __syncthreads();
+    meta_landed = max(meta_landed, hist[H - 1]);
+    if (xk >= 0) {
+      kv_hop(xk, ok++);
+      xk = next_tile(xk);
+    }
+    if (xo >= 0) {
+      off_hop(xo, oo++);
+      xo = next_tile(xo);
+    }
+    if (xp >= 0) {
+      page_hop(xp, op++);
+      xp = next_tile(xp);
+    }
+    if (xi >= 0) {
+      idx_hop(xi, oi++);
+      issue_meta_upto((int)(xi / VT) + H + 1);
+      xi = next_tile(xi);
+    }
+    cp_async_commit();
+#pragma unroll
+    for (int k = H - 1; k > 0; --k) hist[k] = hist[k - 1];
+    hist[0] = meta_issued;
+
+    compute_tile(xc, oc);
+    const int64_t xn = next_tile(xc);
+    const int u = (int)(xc / VT);
+    if (xn < 0 || (int)(xn / VT) != u) {
+      finish(u);
+      if (xn >= 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int ks = 0; ks < C::KSTEPS; ++ks) {
+            qf[nt][ks][0] = qn[nt][ks][0];
+            qf[nt][ks][1] = qn[nt][ks][1];
+          }
+        if (u + 2 <= u_last) load_q(u + 2, qn);
+      }
+    }
+    xc = xn;
+    ++oc;
+  }
+  cp_async_wait_all();
+  if (bad) atomicOr(p.status, bad);
+
+  // ---------------- shared units: arrive, and merge if last ----------------
+  if (npend == 0) return;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    for (int k = 0; k < 2; ++k) s_merge[k] = -1;
+    for (int k = 0; k < npend; ++k) {
+      const uint32_t t = atomicAdd(p.ws_ticket + pend[k], 1u);
+      if (t == (uint32_t)(contributors(pend[k]) - 1)) s_merge[k] = pend[k];
+    }
+  }
+  __syncthreads();
+  for (int k = 0; k < 2; ++k) {
+    const int u = s_merge[k];
+    if (u < 0) continue;
+    __threadfence();
+    const int G = p.group, D = C::D, K = contributors(u), c0 = first_cta(u);
+    const int r = unit_row(u), hg = unit_hg(u);
+    const int64_t stride = partial_stride(G, D);
+    float* s_w = epi;                      // [K][HPU*G] normalised weights
+    float* s_mm = epi + K * HPU * G;       // [K][HPU*G] maxima
+    for (int q = tid; q < K * HPU * G; q += kMmaThreads) {
+      const int c = q / (HPU * G), hi = q - c * HPU * G, h2 = hi / G, i = hi - h2 * G;
+      const float* part = record(c0 + c, u) + h2 * stride;
+      s_mm[q] = __ldcg(part + G * D + i);
+      s_w[q] = __ldcg(part + G * D + G + i);
+    }
+    __syncthreads();
+    for (int hi = tid; hi < HPU * G; hi += kMmaThreads) {
+      float M = -CUDART_INF_F;
+      for (int c = 0; c < K; ++c) M = fmaxf(M, s_mm[c * HPU * G + hi]);
+      float L = 0.f;
+      if (M != -CUDART_INF_F)
+        for (int c = 0; c < K; ++c) L += s_w[c * HPU * G + hi] * exp2f(s_mm[c * HPU * G + hi] - M);
+      for (int c = 0; c < K; ++c)
+        s_w[c * HPU * G + hi] = M != -CUDART_INF_F ? exp2f(s_mm[c * HPU * G + hi] - M) / L : 0.f;
+    }
+    __syncthreads();
+    for (int q4 = tid; q4 < HPU * G * D / 4; q4 += kMmaThreads) {
+      const int idx = q4 * 4, h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int c = 0; c < K; ++c) {
+        const float w = s_w[c * HPU * G + h2 * G + i];
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(record(c0 + c, u) + h2 * stride + rem));
+        acc.x = fmaf(w, v.x, acc.x);
+        acc.y = fmaf(w, v.y, acc.y);
+        acc.z = fmaf(w, v.z, acc.z);
+        acc.w = fmaf(w, v.w, acc.w);
+      }
+      const int64_t ob = ((int64_t)r * p.nq + (int64_t)(hg * HPU + h2) * G) * D + rem;
+      store_out(p, ob, acc.x);
+      store_out(p, ob + 1, acc.y);
+      store_out(p, ob + 2, acc.z);
+      store_out(p, ob + 3, acc.w);
+    }
+    if (tid == 0) p.ws_ticket[u] = 0u;
+    __syncthreads();
+  }
+}
+
+template <int KIND, int NT, int HPU>
+cudaError_t launch_stream_t(const Params& p, const StreamPlan& sp, cudaStream_t s) {
+  using C = StreamCfg<KIND, NT, HPU>;
+  static int configured_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (!(configured_mask & (1 << (dev & 31)))) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(stream_kernel<KIND, NT, HPU>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    configured_mask |= 1 << (dev & 31);
+  }
+  if (sp.G == 0) return cudaSuccess;
+  stream_kernel<KIND, NT, HPU><<<sp.G, kMmaThreads, C::SMEM, s>>>(p, sp);
+  return cudaGetLastError();
+}
+
+template <int KIND>
+cudaError_t launch_stream_kind(const Params& p, const StreamPlan& sp, cudaStream_t s) {
+  const bool nt2 = p.group > 8;
+  switch (sp.HPU) {
+    case 4: return nt2 ? launch_stream_t<KIND, 2, 4>(p, sp, s) : launch_stream_t<KIND, 1, 4>(p, sp, s);
+    case 2: return nt2 ? launch_stream_t<KIND, 2, 2>(p, sp, s) : launch_stream_t<KIND, 1, 2>(p, sp, s);
+    default: return nt2 ? launch_stream_t<KIND, 2, 1>(p, sp, s) : launch_stream_t<KIND, 1, 1>(p, sp, s);
+  }
+}
+
+}  // namespace qsa

@@ -64,7 +64,11 @@ SMALL["tiny_ragged_fp32"] = wl.tiny_ragged()
 def _launches(dtype):
     if dtype == "f32":
         return [dict(kernel=1)]
-    return [dict(), dict(kernel=1), dict(kernel=2, splits=1), dict(kernel=2, splits=3), dict(kernel=2, splits=8)]
+    # auto (the persistent stream-K kernel), the CUDA-core kernel, the per-unit
+    # tensor-core kernel with and without split-K, and stream-K grids small
+    # and large enough that units are shared by several CTAs
+    return [dict(), dict(kernel=1), dict(kernel=2, splits=1), dict(kernel=2, splits=3), dict(kernel=2, splits=8),
+            dict(kernel=3, ctas=1), dict(kernel=3, ctas=7), dict(kernel=3, ctas=64), dict(kernel=3, ctas=1000)]
 
 
 CASES = [(n, i) for n in sorted(SMALL) for i in range(len(_launches(SMALL[n].dtype)))]
@@ -127,7 +131,7 @@ def _dense_bf16(seed=21):
                        page_perm=perm)
 
 
-@pytest.mark.parametrize("launch", [dict(), dict(kernel=1), dict(kernel=2, splits=2)])
+@pytest.mark.parametrize("launch", [dict(), dict(kernel=1), dict(kernel=2, splits=2), dict(kernel=3, ctas=5)])
 def test_full_selection_bf16(launch):
     x = _dense_bf16()
     assert_close(run_gpu(x, **launch), oracle.sparse_attention(x), "bf16", f"dense {launch}")
@@ -160,8 +164,24 @@ def test_odd_groups_on_tensor_cores_with_split_k():
         spec = wl.bf16_decode(seed=60 + g, batch=4, cache_range=(300, 900), width=384)
         spec.num_kv_heads, spec.num_q_heads = 2, 2 * g
         x = spec.build()
-        for kw in (dict(kernel=2, splits=1), dict(kernel=2, splits=3), dict(kernel=2, splits=6)):
+        for kw in (dict(kernel=2, splits=1), dict(kernel=2, splits=3), dict(kernel=2, splits=6), dict(),
+                   dict(kernel=3, ctas=3)):
             assert_close(run_gpu(x, **kw), oracle.sparse_attention(x), "bf16", f"g{g} {kw}")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "e4m3"])
+@pytest.mark.parametrize("nkv", [1, 2, 3, 4, 6, 8, 12])
+def test_kv_head_groupings(dtype, nkv):
+    """Units of 4, 2 or 1 adjacent kv heads (by divisibility of num_kv_heads)
+    in the persistent kernel, at grid sizes that share units between CTAs."""
+    spec = wl.bf16_decode(seed=70 + nkv, batch=3, cache_range=(200, 700), width=320)
+    spec.num_kv_heads, spec.num_q_heads = nkv, 4 * nkv
+    spec.dtype = dtype
+    x = spec.build()
+    ref = oracle.sparse_attention(x)
+    for kw in (dict(), dict(kernel=3, ctas=2), dict(kernel=3, ctas=11)):
+        assert_close(run_gpu(x, **kw), ref, dtype, f"nkv{nkv} {kw}")
+    assert status_clean()
 
 
 def test_group_16_and_12_on_tensor_cores():
@@ -169,7 +189,7 @@ def test_group_16_and_12_on_tensor_cores():
         spec = wl.bf16_long_decode(seed=40 + g, batch=2, cache_range=(2000, 4000), runs=5)
         spec.num_q_heads = g * spec.num_kv_heads
         x = spec.build()
-        for kw in (dict(), dict(kernel=2, splits=1)):
+        for kw in (dict(), dict(kernel=2, splits=1), dict(kernel=3, ctas=4)):
             assert_close(run_gpu(x, **kw), oracle.sparse_attention(x), "bf16", f"g{g} {kw}")
 
 
@@ -180,7 +200,7 @@ def test_group_16_and_12_on_tensor_cores():
 def test_tail_entries_never_change_a_bit():
     x = SMALL["bf16_decode_small"].build()
     n = x.valid_counts()
-    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=4)):
+    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=4), dict(kernel=3, ctas=5)):
         base = run_gpu(x, **launch)
         y = SMALL["bf16_decode_small"].build()
         rng = np.random.default_rng(9)
@@ -225,7 +245,7 @@ def test_empty_and_clamped_counts():
     x.token_indices[4, n4:] = np.resize(x.token_indices[4, :n4], x.selection_width - n4)
     x.counts[4] = x.selection_width + 1000
     ref = oracle.sparse_attention(x)
-    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=5)):
+    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=5), dict(kernel=3, ctas=9), dict(kernel=3, ctas=2)):
         got = run_gpu(x, **launch)
         assert np.array_equal(got[:4], np.zeros_like(got[:4]))
         assert_close(got, ref, "e4m3", str(launch))
@@ -255,7 +275,7 @@ def test_out_of_range_positions_are_skipped_and_reported():
         y.token_indices[r, : len(sel)] = sel
         y.counts[r] = len(sel)
     ref = oracle.sparse_attention(y)
-    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=3)):
+    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=3), dict(kernel=3, ctas=4)):
         B.qsa_read_device_status(clear=True)
         got = run_gpu(x, **launch)
         assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_INDEX
@@ -269,10 +289,26 @@ def test_bad_page_table_entry_is_skipped_and_reported():
     p = int(x.token_indices[r, 0])
     lp = p // x.kv_shape[3]
     x.kv_lookup_table[b, lp] = 0xFFFFFFF0  # names no page
-    B.qsa_read_device_status(clear=True)
-    got = run_gpu(x)
-    assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_PAGE
-    assert np.isfinite(got).all()
+    for launch in (dict(), dict(kernel=2), dict(kernel=1)):
+        B.qsa_read_device_status(clear=True)
+        got = run_gpu(x, **launch)
+        assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_PAGE
+        assert np.isfinite(got).all()
+
+
+def test_rows_outside_every_sequence_are_zero_and_reported():
+    """input_row_offsets that stop short of total_q: the trailing rows belong
+    to no sequence, come out zero and raise QSA_STATUS_BAD_ROW."""
+    x = SMALL["bf16_prefill_small"].build()  # its last sequence has 23 rows
+    x.input_row_offsets[-1] -= 2  # still nondecreasing: rows total_q-2, total_q-1 are orphaned
+    assert (np.diff(x.input_row_offsets.astype(np.int64)) >= 0).all()
+    ref = oracle.sparse_attention(x, np.arange(x.total_q - 2))
+    for launch in (dict(), dict(kernel=2), dict(kernel=1)):
+        B.qsa_read_device_status(clear=True)
+        got = run_gpu(x, **launch)
+        assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_ROW
+        assert np.array_equal(got[-2:], np.zeros_like(got[-2:]))
+        assert_close(got[:-2], ref, "bf16", str(launch))
 
 
 # ---------------------------------------------------------------------------
