@@ -440,6 +440,9 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
   p.group = group;
   p.D = (int32_t)R.D;
   p.P = (int32_t)R.P;
+  p.log2P = -1;
+  for (int k = 0; k < 31; ++k)
+    if ((int64_t)1 << k == R.P) p.log2P = k;
   p.W = (int32_t)R.W;
   p.max_pages = (int32_t)R.max_pages;
   p.num_pages = (uint32_t)R.num_pages;

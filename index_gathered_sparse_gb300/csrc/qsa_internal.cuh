@@ -29,6 +29,7 @@ struct Params {
   int64_t head_bytes;        // D * elem
 
   int32_t total_q, batch, nq, nkv, group, D, P, W, max_pages;
+  int32_t log2P;     // log2(page_size) when it is a power of two, else -1
   uint32_t num_pages;
   float scale_log2;  // scale * log2(e): the softmax runs in base 2
   int32_t out_bf16;

@@ -69,10 +69,19 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 
+// A cursor over this CTA's tiles: unit u (its row r, kv-head group hg, valid
+// count n and last tile jl inside the range), tile j, ordinal o.  Every thread
+// holds the same cursor values, so every branch on them is block-uniform.
+struct TileCursor {
+  int u, j, o, r, hg, n, jl;
+  bool live;
+};
+
 template <int KIND, int NT, int HPU>
 __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, const StreamPlan sp) {
   using C = StreamCfg<KIND, NT, HPU>;
   constexpr int H = C::H, S = C::STAGES, TILE = C::TILE, RT = C::RT, MR = C::MR, GP = C::GP;
+  static_assert((RT & (RT - 1)) == 0 && (MR & (MR - 1)) == 0, "rings are powers of two");
   extern __shared__ __align__(128) unsigned char smem[];
   float* epi = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);  // [4][GP][D] + m[4][GP] + l[4][GP]
   int32_t* s_pos = reinterpret_cast<int32_t*>(epi + C::EPI_FLOATS);  // [RT][TILE]
@@ -88,10 +97,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
   if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
   const int u_first = (int)(t0 / VT), u_last = (int)((t1 - 1) / VT);
+  const int jlo_first = (int)(t0 - (int64_t)u_first * VT);  // first tile of the first unit in range
+  const int jhi_last = (int)(t1 - (int64_t)u_last * VT);    // end tile of the last unit in range
   uint32_t bad = 0;
 
-  auto unit_row = [&](int u) { return p.total_q - 1 - u / sp.NG; };
-  auto unit_hg = [&](int u) { return u % sp.NG; };
   // the CTA whose range holds virtual tile x, and a unit's contributing CTAs
   auto cta_of = [&](int64_t x) { return (int)(((x + 1) * sp.G - 1) / sp.T); };
   auto first_cta = [&](int u) { return cta_of((int64_t)u * VT); };
@@ -103,9 +112,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   };
 
   // ---------------- unit meta ----------------
-  auto mslot = [&](int u) { return ((u - u_first) % MR) * 4; };
-  // sequence of row r, -1 when no sequence owns it
-  auto find_seq = [&](int r) -> int {
+  auto mslot = [&](int u) { return ((u - u_first) & (MR - 1)) * 4; };
+  auto find_seq = [&](int r) -> int {  // sequence of row r, -1 when no sequence owns it
     const bool in_smem = p.batch + 1 <= C::MAXOFF;
     auto off = [&](int k) { return in_smem ? s_rowoff[k] : __ldg(p.row_offsets + k); };
     int lo = 0, hi = p.batch;  // largest b in [0, batch] with off[b] <= r
@@ -118,7 +126,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     return lo;
   };
   auto issue_meta = [&](int u) {  // thread 0 only
-    const int r = unit_row(u), m = mslot(u);
+    const int r = p.total_q - 1 - u / sp.NG, m = mslot(u);
     const int b = find_seq(r);
     s_meta[m + 2] = b;
     if (b >= 0) {
@@ -138,9 +146,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   int hist[H];  // meta_issued at the end of each of the last H iterations
   auto issue_meta_upto = [&](int u) {
     u = min(u, u_last);
+    if (u < meta_issued) return;
     if (tid == 0)
       for (int v = meta_issued; v <= u; ++v) issue_meta(v);
-    meta_issued = max(meta_issued, u + 1);
+    meta_issued = u + 1;
   };
   // makes unit u's meta readable (a full wait when it has not landed yet)
   auto ensure_meta = [&](int u) {
@@ -153,53 +162,60 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       for (int k = 0; k < H; ++k) hist[k] = meta_issued;
     }
   };
-  auto n_of = [&](int u) {
-    const int m = mslot(u);
-    return s_meta[m + 2] < 0 ? 0 : min(max(s_meta[m + 0], 0), p.W);
-  };
-  auto kv_len_of = [&](int u) {
-    const int m = mslot(u);
-    return (int64_t)(uint32_t)s_meta[m + 1] + (int64_t)s_meta[m + 3];
-  };
 
   // ---------------- tile cursors ----------------
   // Ordinals run over each unit's real tiles inside this range (at least one
   // per unit: a unit with none gets one empty tile so it is still finished).
-  auto j_lo = [&](int u) { return u == u_first ? (int)(t0 - (int64_t)u * VT) : 0; };
-  auto j_hi = [&](int u) { return u == u_last ? (int)(t1 - (int64_t)u * VT) : VT; };
-  auto last_j = [&](int u) {
-    const int real_hi = min(j_hi(u), (n_of(u) + TILE - 1) / TILE);
-    return max(j_lo(u), real_hi - 1);
-  };
-  auto next_tile = [&](int64_t x) -> int64_t {  // -1 past the range
-    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
+  auto enter = [&](TileCursor& c, int u) {
     ensure_meta(u);
-    if (j < last_j(u)) return x + 1;
-    if (u >= u_last) return -1;
-    ensure_meta(u + 1);
-    return (int64_t)(u + 1) * VT;  // j_lo(u + 1) == 0
+    const int m = mslot(u);
+    c.u = u;
+    const int q = u / sp.NG;
+    c.r = p.total_q - 1 - q;
+    c.hg = u - q * sp.NG;
+    c.n = s_meta[m + 2] < 0 ? 0 : min(max(s_meta[m + 0], 0), p.W);
+    const int jlo = u == u_first ? jlo_first : 0, jhi = u == u_last ? jhi_last : VT;
+    c.jl = max(jlo, min(jhi, (c.n + TILE - 1) / TILE) - 1);
+    c.j = jlo;
   };
-  auto keys_in = [&](int u, int j) { return min(max(n_of(u) - j * TILE, 0), TILE); };
+  auto start = [&](TileCursor& c) {
+    enter(c, u_first);
+    c.o = 0;
+    c.live = true;
+  };
+  auto advance = [&](TileCursor& c) {
+    ++c.o;
+    if (c.j < c.jl) {
+      ++c.j;
+    } else if (c.u < u_last) {
+      enter(c, c.u + 1);
+    } else {
+      c.live = false;
+    }
+  };
+  auto keys_in = [&](const TileCursor& c) { return min(max(c.n - c.j * TILE, 0), TILE); };
 
   // ---------------- hops ----------------
-  auto idx_hop = [&](int64_t x, int o) {
-    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
-    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
-    const int32_t* src = p.indices + (int64_t)unit_row(u) * p.W + (int64_t)j * TILE;
-    for (int k = tid; k < kt; k += kMmaThreads) cp_async4(smem_addr(&s_pos[slot + k]), src + k);
+  auto idx_hop = [&](const TileCursor& c) {
+    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
+    if (tid < kt)
+      cp_async4(smem_addr(&s_pos[slot + tid]), p.indices + (int64_t)c.r * p.W + c.j * TILE + tid);
+    for (int k = tid + kMmaThreads; k < kt; k += kMmaThreads)
+      cp_async4(smem_addr(&s_pos[slot + k]), p.indices + (int64_t)c.r * p.W + c.j * TILE + k);
   };
-  auto page_hop = [&](int64_t x, int o) {
-    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
-    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
-    const int64_t kvl = kv_len_of(u);
-    const uint32_t* trow = p.table + (int64_t)s_meta[mslot(u) + 2] * p.max_pages;
+  auto page_hop = [&](const TileCursor& c) {
+    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
+    if (kt == 0) return;
+    const int m = mslot(c.u);
+    const int64_t kvl = (int64_t)(uint32_t)s_meta[m + 1] + (int64_t)s_meta[m + 3];
+    const uint32_t* trow = p.table + (int64_t)s_meta[m + 2] * p.max_pages;
     for (int k = tid; k < kt; k += kMmaThreads) {
       const int32_t pos = s_pos[slot + k];
       uint32_t so = kInvalidOff;
       if (pos < 0 || (int64_t)pos >= kvl) {
         bad |= QSA_STATUS_BAD_INDEX;
       } else {
-        const uint32_t lp = (uint32_t)pos / (uint32_t)p.P;
+        const uint32_t lp = p.log2P >= 0 ? (uint32_t)pos >> p.log2P : (uint32_t)pos / (uint32_t)p.P;
         if (lp >= (uint32_t)p.max_pages) {
           bad |= QSA_STATUS_BAD_PAGE;
         } else {
@@ -210,10 +226,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       s_off[slot + k] = so;
     }
   };
-  auto off_hop = [&](int64_t x, int o) {
-    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
-    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
-    const int64_t head0 = p.k_layer_bytes + (int64_t)unit_hg(u) * HPU * p.head_bytes;
+  auto off_hop = [&](const TileCursor& c) {
+    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
+    const int64_t head0 = p.k_layer_bytes + (int64_t)c.hg * HPU * p.head_bytes;
     for (int k = tid; k < kt; k += kMmaThreads) {
       const uint32_t so = s_off[slot + k];
       if (so == kInvalidOff) continue;
@@ -226,26 +241,29 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       }
     }
   };
-  auto kv_hop = [&](int64_t x, int o) {
-    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
-    const int kt = keys_in(u, j), slot = (o % RT) * TILE;
-    unsigned char* sb = smem + (o % S) * C::STAGE_BYTES;
+  // this thread's fixed role in a stage copy: key offset, K or V, 16-byte chunk
+  constexpr int KPI = kMmaThreads / C::CPK;  // keys per copy instruction round
+  const int my_key = tid / C::CPK, my_w = tid - my_key * C::CPK;
+  const int my_kv = my_w / (C::CPK / 2), my_ch = my_w - my_kv * (C::CPK / 2);
+  const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
+  const int my_dst = my_kv * C::KV_BYTES + my_key * C::SROW + my_ch * 16;
+  auto kv_hop = [&](const TileCursor& c) {
+    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
+    const uint32_t sb = smem_addr(smem + (c.o % S) * C::STAGE_BYTES) + my_dst;
 #pragma unroll 4
-    for (int i = 0; i < C::CHUNKS / kMmaThreads; ++i) {
-      const int c = i * kMmaThreads + tid;
-      const int key = c / C::CPK, w = c - key * C::CPK;
-      const int kv = w / (C::CPK / 2), ch = w - kv * (C::CPK / 2);
+    for (int i = 0; i < TILE / KPI; ++i) {
+      const int key = i * KPI + my_key;
       const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
       const bool live = off != kInvalidOff;
-      const unsigned char* src = live ? p.kv + (int64_t)off * 16 + (kv ? p.v_minus_k_bytes : 0) + ch * 16 : p.kv;
-      cp_async16(smem_addr(sb + kv * C::KV_BYTES + key * C::SROW + ch * 16), src, live ? 16u : 0u);
+      cp_async16(sb + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
     }
   };
 
   // ---------------- per-warp attention state ----------------
   uint32_t qf[NT][C::KSTEPS][2], qn[NT][C::KSTEPS][2];
   auto load_q = [&](int u, uint32_t (&dst)[NT][C::KSTEPS][2]) {
-    const int r = unit_row(u), h = unit_hg(u) * HPU + hh;
+    const int q = u / sp.NG;
+    const int r = p.total_q - 1 - q, h = (u - q * sp.NG) * HPU + hh;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int head = nt * 8 + gid;
@@ -274,10 +292,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_col = ((lane >> 4) & 1) * 16;
   const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8, t_col = ((lane >> 3) & 1) * 16;
 
-  auto compute_tile = [&](int64_t x, int ord) {
-    const int u = (int)(x / VT), j = (int)(x - (int64_t)u * VT);
-    const int kt = keys_in(u, j), slot = (ord % RT) * TILE;
-    const unsigned char* sb = smem + (ord % S) * C::STAGE_BYTES;
+  auto compute_tile = [&](const TileCursor& cur) {
+    const int kt = keys_in(cur), slot = (cur.o & (RT - 1)) * TILE;
+    const unsigned char* sb = smem + (cur.o % S) * C::STAGE_BYTES;
 #pragma unroll
     for (int sl = 0; sl < C::MSL; ++sl) {
       const int k0 = kp * C::KPW + sl * 16;
@@ -375,8 +392,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
 
   // End of a unit: merge the WPH warps of each head in shared memory, then
   // write the output (unit owned by this CTA) or this CTA's partial record.
-  int pend[2] = {-1, -1}, npend = 0;
-  auto finish = [&](int u) {
+  int pend0 = -1, pend1 = -1;
+  auto finish = [&](const TileCursor& cur) {
     float* sm_o = epi;
     float* sm_m = epi + 4 * GP * C::D;
     float* sm_l = sm_m + 4 * GP;
@@ -404,12 +421,12 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
           sm_o[(warp * GP + head) * C::D + d] = o[mt][nt][c];
         }
     __syncthreads();
-    const int G = p.group, D = C::D;
-    const int r = unit_row(u), hg = unit_hg(u);
+    const int G = p.group, D = C::D, u = cur.u;
     const bool row_ok = s_meta[mslot(u) + 2] >= 0;
     const bool own = contributors(u) == 1;
     float* rec = own ? nullptr : record(blockIdx.x, u);
     const int64_t stride = partial_stride(G, D);
+    const int64_t out0 = ((int64_t)cur.r * p.nq + (int64_t)cur.hg * HPU * G) * D;
     for (int idx = tid; idx < HPU * G * D; idx += kMmaThreads) {
       const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
       float M = -CUDART_INF_F;
@@ -426,8 +443,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
         }
       }
       if (own) {
-        store_out(p, ((int64_t)r * p.nq + (int64_t)(hg * HPU + h2) * G + i) * D + d,
-                  row_ok && M != -CUDART_INF_F ? O / L : 0.f);
+        store_out(p, out0 + idx, row_ok && M != -CUDART_INF_F ? O / L : 0.f);
       } else {
         float* part = rec + h2 * stride;
         part[rem] = O;
@@ -437,7 +453,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
         }
       }
     }
-    if (!own) pend[npend++] = u;
+    if (!own) {
+      if (pend0 < 0) pend0 = u; else pend1 = u;
+    }
     __syncthreads();  // the epilogue buffer is free again
     reset_state();
   };
@@ -457,68 +475,74 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   if (u_first < u_last) load_q(u_first + 1, qn);
   reset_state();
 
-  int64_t xi = t0, xp = t0, xo = t0, xk = t0;
-  int oi = 0, op = 0, oo = 0, ok = 0;
-  for (int n = 0; n <= 3 * H && xi >= 0; ++n) {
-    idx_hop(xi, oi++);
-    xi = next_tile(xi);
+  TileCursor ci, cpg, cof, ckv, cc;
+  start(ci);
+  cpg = ci;
+  cof = ci;
+  ckv = ci;
+  cc = ci;
+  for (int n = 0; n <= 3 * H && ci.live; ++n) {
+    idx_hop(ci);
+    advance(ci);
   }
   cp_async_wait_all();
   __syncthreads();
-  for (int n = 0; n <= 2 * H && xp >= 0; ++n) {
-    page_hop(xp, op++);
-    xp = next_tile(xp);
+  for (int n = 0; n <= 2 * H && cpg.live; ++n) {
+    page_hop(cpg);
+    advance(cpg);
   }
   cp_async_wait_all();
   __syncthreads();
-  for (int n = 0; n <= H && xo >= 0; ++n) {
-    off_hop(xo, oo++);
-    xo = next_tile(xo);
+  for (int n = 0; n <= H && cof.live; ++n) {
+    off_hop(cof);
+    advance(cof);
   }
   __syncthreads();
   for (int n = 0; n < H; ++n) {
-    if (xk >= 0) {
-      kv_hop(xk, ok++);
-      xk = next_tile(xk);
+    if (ckv.live) {
+      kv_hop(ckv);
+      advance(ckv);
     }
     cp_async_commit();
   }
 
   // ---------------- main loop: one tile per iteration ----------------
-  int64_t xc = t0;
-  int oc = 0;
-  while (xc >= 0) {
+  while (cc.live) {
     cp_async_wait<H - 1>();
     __syncthreads();
     meta_landed = max(meta_landed, hist[H - 1]);
-    if (xk >= 0) {
-      kv_hop(xk, ok++);
-      xk = next_tile(xk);
+    if (ckv.live) {
+      kv_hop(ckv);
+      advance(ckv);
     }
-    if (xo >= 0) {
-      off_hop(xo, oo++);
-      xo = next_tile(xo);
+    if (cof.live) {
+      off_hop(cof);
+      advance(cof);
     }
-    if (xp >= 0) {
-      page_hop(xp, op++);
-      xp = next_tile(xp);
+    if (cpg.live) {
+      page_hop(cpg);
+      advance(cpg);
     }
-    if (xi >= 0) {
-      idx_hop(xi, oi++);
-      issue_meta_upto((int)(xi / VT) + H + 1);
-      xi = next_tile(xi);
+    if (ci.live) {
+      idx_hop(ci);
+      issue_meta_upto(ci.u + H + 1);
+      advance(ci);
     }
     cp_async_commit();
 #pragma unroll
     for (int k = H - 1; k > 0; --k) hist[k] = hist[k - 1];
     hist[0] = meta_issued;
 
-    compute_tile(xc, oc);
-    const int64_t xn = next_tile(xc);
-    const int u = (int)(xc / VT);
-    if (xn < 0 || (int)(xn / VT) != u) {
-      finish(u);
-      if (xn >= 0) {
+    compute_tile(cc);
+    const int u = cc.u;
+    advance(cc);
+    if (!cc.live || cc.u != u) {
+      TileCursor done = cc;
+      done.u = u;
+      done.r = p.total_q - 1 - u / sp.NG;
+      done.hg = u - (u / sp.NG) * sp.NG;
+      finish(done);
+      if (cc.live) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -529,19 +553,19 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
         if (u + 2 <= u_last) load_q(u + 2, qn);
       }
     }
-    xc = xn;
-    ++oc;
   }
   cp_async_wait_all();
   if (bad) atomicOr(p.status, bad);
 
   // ---------------- shared units: arrive, and merge if last ----------------
-  if (npend == 0) return;
+  if (pend0 < 0) return;
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    for (int k = 0; k < 2; ++k) s_merge[k] = -1;
-    for (int k = 0; k < npend; ++k) {
+    s_merge[0] = s_merge[1] = -1;
+    const int pend[2] = {pend0, pend1};
+    for (int k = 0; k < 2; ++k) {
+      if (pend[k] < 0) continue;
       const uint32_t t = atomicAdd(p.ws_ticket + pend[k], 1u);
       if (t == (uint32_t)(contributors(pend[k]) - 1)) s_merge[k] = pend[k];
     }
@@ -552,15 +576,16 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     if (u < 0) continue;
     __threadfence();
     const int G = p.group, D = C::D, K = contributors(u), c0 = first_cta(u);
-    const int r = unit_row(u), hg = unit_hg(u);
+    const int q = u / sp.NG;
+    const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
     const int64_t stride = partial_stride(G, D);
     float* s_w = epi;                      // [K][HPU*G] normalised weights
     float* s_mm = epi + K * HPU * G;       // [K][HPU*G] maxima
-    for (int q = tid; q < K * HPU * G; q += kMmaThreads) {
-      const int c = q / (HPU * G), hi = q - c * HPU * G, h2 = hi / G, i = hi - h2 * G;
+    for (int qq = tid; qq < K * HPU * G; qq += kMmaThreads) {
+      const int c = qq / (HPU * G), hi = qq - c * HPU * G, h2 = hi / G, i = hi - h2 * G;
       const float* part = record(c0 + c, u) + h2 * stride;
-      s_mm[q] = __ldcg(part + G * D + i);
-      s_w[q] = __ldcg(part + G * D + G + i);
+      s_mm[qq] = __ldcg(part + G * D + i);
+      s_w[qq] = __ldcg(part + G * D + G + i);
     }
     __syncthreads();
     for (int hi = tid; hi < HPU * G; hi += kMmaThreads) {
