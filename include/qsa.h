@@ -90,6 +90,7 @@ typedef enum qsa_status {
 #define QSA_STATUS_BAD_INDEX 1u /* a position inside counts outside [0, kv_len) */
 #define QSA_STATUS_BAD_PAGE 2u  /* p / page_size >= max_pages or a table entry >= num_pages */
 #define QSA_STATUS_BAD_ROW 4u   /* a query row owned by no sequence (bad input_row_offsets) */
+#define QSA_STATUS_TIMEOUT 8u   /* a kernel gave up waiting for its own copies (never expected) */
 
 /*
  * qsa_sparse_attention_ragged_paged - one layer of QSA sparse attention.

@@ -12,9 +12,11 @@
 // the load is balanced to a tile and at most the first and the last unit of a
 // range are shared with other CTAs.  Tiles past a unit's count are skipped.
 //
-// Pipeline.  Everything a tile needs is fetched by cp.async in hops spaced H =
-// STAGES - 1 loop iterations apart, so each hop has landed when the next one
-// reads it and no CTA ever waits on a dependent load in steady state:
+// Pipeline.  Everything a tile needs is fetched asynchronously in hops spaced
+// H = STAGES - 1 loop iterations apart, so each hop has landed when the next
+// one reads it and no CTA ever waits on a dependent load in steady state
+// (meta, indices and page entries by cp.async; K/V by one bulk copy per key
+// and K or V, completing on the stage's mbarrier):
 //     unit meta (counts, cache_lengths)   ~ H + 1 units ahead of the index hop
 //     indices  (token_indices)            3H + 1 tiles ahead of compute
 //     page     (kv_lookup_table entries)  2H + 1 tiles ahead
@@ -64,6 +66,38 @@ struct StreamCfg {
   static_assert(SMEM <= 232448, "shared memory");
 };
 
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `bar` with this parity; false after kSpinLimit polls
+// (each poll may block for a while in hardware), which never happens unless a
+// copy was lost.
+constexpr int kSpinLimit = 1 << 20;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// One-dimensional bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
 }
@@ -90,12 +124,18 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
   uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
   __shared__ int s_merge[2];
+  __shared__ __align__(8) uint64_t s_full[S];  // one per stage: its K/V bulk copies have landed
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
   const int hh = warp / C::WPH, kp = warp % C::WPH;
   const int VT = sp.VT;
   const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
   if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
+  if (tid == 0) {
+    for (int k = 0; k < S; ++k) mbar_init(smem_addr(&s_full[k]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
   const int u_first = (int)(t0 / VT), u_last = (int)((t1 - 1) / VT);
   const int jlo_first = (int)(t0 - (int64_t)u_first * VT);  // first tile of the first unit in range
   const int jhi_last = (int)(t1 - (int64_t)u_last * VT);    // end tile of the last unit in range
@@ -241,22 +281,46 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       }
     }
   };
-  // this thread's fixed role in a stage copy: key offset, K or V, 16-byte chunk
-  constexpr int KPI = kMmaThreads / C::CPK;  // keys per copy instruction round
-  const int my_key = tid / C::CPK, my_w = tid - my_key * C::CPK;
-  const int my_kv = my_w / (C::CPK / 2), my_ch = my_w - my_kv * (C::CPK / 2);
-  const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
-  const int my_dst = my_kv * C::KV_BYTES + my_key * C::SROW + my_ch * 16;
+  // K/V of a tile: warp 0 moves each valid key's K and V chunk (HPU heads,
+  // contiguous) with one bulk copy each and zeroes the V rows of every other
+  // key slot (their scores are masked to -inf, but 0 * NaN would not vanish).
   auto kv_hop = [&](const TileCursor& c) {
-    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
-    const uint32_t sb = smem_addr(smem + (c.o % S) * C::STAGE_BYTES) + my_dst;
-#pragma unroll 4
-    for (int i = 0; i < TILE / KPI; ++i) {
-      const int key = i * KPI + my_key;
-      const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
-      const bool live = off != kInvalidOff;
-      cp_async16(sb + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
+    if (warp != 0) return;
+    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
+    unsigned char* sb = smem + st * C::STAGE_BYTES;
+    uint32_t valid_keys = 0;
+#pragma unroll
+    for (int i = 0; i < (TILE + 31) / 32; ++i) {
+      const int key = i * 32 + lane;
+      const bool v = key < kt && s_off[slot + key] != kInvalidOff;
+      valid_keys += __popc(__ballot_sync(0xffffffffu, v));
+      if (key < TILE && !v) {
+        uint4* row = reinterpret_cast<uint4*>(sb + C::KV_BYTES + key * C::SROW);
+        for (int q = 0; q < C::KEYB / 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
+    fence_proxy_async_smem();  // order this warp's generic writes before the async copies
+    __syncwarp();
+    const uint32_t bar = smem_addr(&s_full[st]);
+    if (lane == 0) mbar_arrive_expect_tx(bar, valid_keys * 2u * (uint32_t)C::KEYB);
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < (TILE + 31) / 32; ++i) {
+      const int key = i * 32 + lane;
+      if (key < kt) {
+        const uint32_t off = s_off[slot + key];
+        if (off != kInvalidOff) {
+          const unsigned char* src = p.kv + (int64_t)off * 16;
+          bulk_g2s(smem_addr(sb + key * C::SROW), src, C::KEYB, bar);
+          bulk_g2s(smem_addr(sb + C::KV_BYTES + key * C::SROW), src + p.v_minus_k_bytes, C::KEYB, bar);
+        }
+      }
+    }
+  };
+  bool timed_out = false;
+  auto wait_tile = [&](const TileCursor& c) {  // every thread; block-uniform result
+    const bool ok = mbar_wait(smem_addr(&s_full[c.o % S]), (uint32_t)((c.o / S) & 1));
+    timed_out = __syncthreads_or(!ok) != 0;
   };
 
   // ---------------- per-warp attention state ----------------
@@ -503,7 +567,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       kv_hop(ckv);
       advance(ckv);
     }
-    cp_async_commit();
+    cp_async_commit();  // empty groups keep the index/page hop accounting of the main loop
   }
 
   // ---------------- main loop: one tile per iteration ----------------
@@ -533,6 +597,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     for (int k = H - 1; k > 0; --k) hist[k] = hist[k - 1];
     hist[0] = meta_issued;
 
+    wait_tile(cc);
+    if (timed_out) break;
     compute_tile(cc);
     const int u = cc.u;
     advance(cc);
@@ -555,6 +621,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     }
   }
   cp_async_wait_all();
+  if (timed_out) {
+    // drain (bounded) the stages still owed bulk copies, then leave; the
+    // status word tells the host the output is not valid
+    for (int o2 = cc.o; o2 < ckv.o; ++o2) mbar_wait(smem_addr(&s_full[o2 % S]), (uint32_t)((o2 / S) & 1));
+    if (tid == 0) atomicOr(p.status, QSA_STATUS_TIMEOUT);
+    return;
+  }
   if (bad) atomicOr(p.status, bad);
 
   // ---------------- shared units: arrive, and merge if last ----------------
