@@ -50,6 +50,10 @@ struct StreamCfg {
   static constexpr int GP = 8 * NT;                 // padded query heads per kv head
   static constexpr int KSTEPS = KIND == kBF16 ? 8 : 4;
   static constexpr int CPK = 2 * KEYB / 16;         // 16-byte chunks per key (K and V)
+  // K/V copy mechanism: one bulk copy per key chunk when chunks are large
+  // (each bulk copy costs its warp a fixed issue time), else 16-byte cp.async
+  // spread over every thread
+  static constexpr bool BULK = KEYB >= 512;
   static constexpr int CHUNKS = TILE * CPK;         // per stage
   static constexpr int RT = 16;                     // tile-record ring (positions, pages, offsets)
   static constexpr int MR = 32;                     // unit-meta ring
@@ -132,7 +136,7 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
   if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
   if (tid == 0) {
-    for (int k = 0; k < S; ++k) mbar_init(smem_addr(&s_full[k]), 1);
+    for (int k = 0; k < S; ++k) mbar_init(smem_addr(&s_full[k]), kMmaThreads / 32);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();
@@ -236,20 +240,22 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   auto keys_in = [&](const TileCursor& c) { return min(max(c.n - c.j * TILE, 0), TILE); };
 
   // ---------------- hops ----------------
+  // The hops of one iteration run on different warps, in parallel: indices on
+  // warp 1, page entries on warp 2, offsets on warp 3, K/V copies on all.
   auto idx_hop = [&](const TileCursor& c) {
+    if (warp != 1) return;
     const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
-    if (tid < kt)
-      cp_async4(smem_addr(&s_pos[slot + tid]), p.indices + (int64_t)c.r * p.W + c.j * TILE + tid);
-    for (int k = tid + kMmaThreads; k < kt; k += kMmaThreads)
-      cp_async4(smem_addr(&s_pos[slot + k]), p.indices + (int64_t)c.r * p.W + c.j * TILE + k);
+    const int32_t* src = p.indices + (int64_t)c.r * p.W + c.j * TILE;
+    for (int k = lane; k < kt; k += 32) cp_async4(smem_addr(&s_pos[slot + k]), src + k);
   };
   auto page_hop = [&](const TileCursor& c) {
+    if (warp != 2) return;
     const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
     if (kt == 0) return;
     const int m = mslot(c.u);
     const int64_t kvl = (int64_t)(uint32_t)s_meta[m + 1] + (int64_t)s_meta[m + 3];
     const uint32_t* trow = p.table + (int64_t)s_meta[m + 2] * p.max_pages;
-    for (int k = tid; k < kt; k += kMmaThreads) {
+    for (int k = lane; k < kt; k += 32) {
       const int32_t pos = s_pos[slot + k];
       uint32_t so = kInvalidOff;
       if (pos < 0 || (int64_t)pos >= kvl) {
@@ -267,9 +273,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     }
   };
   auto off_hop = [&](const TileCursor& c) {
+    if (warp != 3) return;
     const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
     const int64_t head0 = p.k_layer_bytes + (int64_t)c.hg * HPU * p.head_bytes;
-    for (int k = tid; k < kt; k += kMmaThreads) {
+    for (int k = lane; k < kt; k += 32) {
       const uint32_t so = s_off[slot + k];
       if (so == kInvalidOff) continue;
       const uint32_t page = s_page[slot + k];
@@ -281,46 +288,57 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       }
     }
   };
-  // K/V of a tile: warp 0 moves each valid key's K and V chunk (HPU heads,
-  // contiguous) with one bulk copy each and zeroes the V rows of every other
-  // key slot (their scores are masked to -inf, but 0 * NaN would not vanish).
+  // K/V of a tile.  Bulk: warp w moves keys w, w+4, ... with one bulk copy per
+  // K or V chunk (HPU heads, contiguous) completing on the stage's mbarrier
+  // (one arrival per warp), and zeroes the V rows of its key slots that hold
+  // no valid key (their scores are masked, but 0 * NaN would not vanish).
+  // Otherwise: 16-byte cp.async over every thread, zero-filled for those
+  // slots, completing with the iteration's cp.async group.
+  constexpr int KPI = kMmaThreads / C::CPK;  // keys per cp.async round (non-bulk)
+  const int my_key = tid / C::CPK, my_w = tid - my_key * C::CPK;
+  const int my_kv = my_w / (C::CPK / 2), my_ch = my_w - my_kv * (C::CPK / 2);
+  const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
+  const int my_dst = my_kv * C::KV_BYTES + my_key * C::SROW + my_ch * 16;
   auto kv_hop = [&](const TileCursor& c) {
-    if (warp != 0) return;
     const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
     unsigned char* sb = smem + st * C::STAGE_BYTES;
-    uint32_t valid_keys = 0;
-#pragma unroll
-    for (int i = 0; i < (TILE + 31) / 32; ++i) {
-      const int key = i * 32 + lane;
-      const bool v = key < kt && s_off[slot + key] != kInvalidOff;
-      valid_keys += __popc(__ballot_sync(0xffffffffu, v));
-      if (key < TILE && !v) {
+    if constexpr (C::BULK) {
+      constexpr int KPWARP = (TILE + 3) / 4;  // key slots per warp
+      const int key = warp + 4 * (lane % KPWARP);
+      const bool mine = lane < KPWARP && key < TILE;
+      const bool v = mine && key < kt && s_off[slot + key] != kInvalidOff;
+      const uint32_t nv = __popc(__ballot_sync(0xffffffffu, v));
+      if (mine && !v) {
         uint4* row = reinterpret_cast<uint4*>(sb + C::KV_BYTES + key * C::SROW);
         for (int q = 0; q < C::KEYB / 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
       }
-    }
-    fence_proxy_async_smem();  // order this warp's generic writes before the async copies
-    __syncwarp();
-    const uint32_t bar = smem_addr(&s_full[st]);
-    if (lane == 0) mbar_arrive_expect_tx(bar, valid_keys * 2u * (uint32_t)C::KEYB);
-    __syncwarp();
-#pragma unroll
-    for (int i = 0; i < (TILE + 31) / 32; ++i) {
-      const int key = i * 32 + lane;
-      if (key < kt) {
-        const uint32_t off = s_off[slot + key];
-        if (off != kInvalidOff) {
-          const unsigned char* src = p.kv + (int64_t)off * 16;
-          bulk_g2s(smem_addr(sb + key * C::SROW), src, C::KEYB, bar);
-          bulk_g2s(smem_addr(sb + C::KV_BYTES + key * C::SROW), src + p.v_minus_k_bytes, C::KEYB, bar);
-        }
+      fence_proxy_async_smem();  // this warp's generic writes before its async copies
+      __syncwarp();
+      const uint32_t bar = smem_addr(&s_full[st]);
+      if (lane == 0) mbar_arrive_expect_tx(bar, nv * 2u * (uint32_t)C::KEYB);
+      __syncwarp();
+      if (v) {
+        const unsigned char* src = p.kv + (int64_t)s_off[slot + key] * 16;
+        bulk_g2s(smem_addr(sb + key * C::SROW), src, C::KEYB, bar);
+        bulk_g2s(smem_addr(sb + C::KV_BYTES + key * C::SROW), src + p.v_minus_k_bytes, C::KEYB, bar);
+      }
+    } else {
+      const uint32_t sbase = smem_addr(sb) + my_dst;
+#pragma unroll 4
+      for (int i = 0; i < TILE / KPI; ++i) {
+        const int key = i * KPI + my_key;
+        const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
+        const bool live = off != kInvalidOff;
+        cp_async16(sbase + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
       }
     }
   };
   bool timed_out = false;
   auto wait_tile = [&](const TileCursor& c) {  // every thread; block-uniform result
-    const bool ok = mbar_wait(smem_addr(&s_full[c.o % S]), (uint32_t)((c.o / S) & 1));
-    timed_out = __syncthreads_or(!ok) != 0;
+    if constexpr (C::BULK) {
+      const bool ok = mbar_wait(smem_addr(&s_full[c.o % S]), (uint32_t)((c.o / S) & 1));
+      timed_out = __syncthreads_or(!ok) != 0;
+    }
   };
 
   // ---------------- per-warp attention state ----------------
@@ -624,7 +642,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   if (timed_out) {
     // drain (bounded) the stages still owed bulk copies, then leave; the
     // status word tells the host the output is not valid
-    for (int o2 = cc.o; o2 < ckv.o; ++o2) mbar_wait(smem_addr(&s_full[o2 % S]), (uint32_t)((o2 / S) & 1));
+    if constexpr (C::BULK)
+      for (int o2 = cc.o; o2 < ckv.o; ++o2) mbar_wait(smem_addr(&s_full[o2 % S]), (uint32_t)((o2 / S) & 1));
     if (tid == 0) atomicOr(p.status, QSA_STATUS_TIMEOUT);
     return;
   }
