@@ -12,21 +12,22 @@
 // the load is balanced to a tile and at most the first and the last unit of a
 // range are shared with other CTAs.  Tiles past a unit's count are skipped.
 //
-// Pipeline.  Everything a tile needs is fetched asynchronously in hops spaced
-// H = STAGES - 1 loop iterations apart, so each hop has landed when the next
-// one reads it and no CTA ever waits on a dependent load in steady state
-// (meta, indices and page entries by cp.async; K/V by one bulk copy per key
-// and K or V, completing on the stage's mbarrier):
+// Roles.  Warps 0-3 produce, warps 4-7 consume, linked per stage by a "full"
+// and an "empty" mbarrier.  Producers fetch everything a tile needs in hops
+// spaced H = STAGES - 1 producer iterations apart, so each hop has landed when
+// the next one reads it and nothing waits on a dependent load in steady state:
 //     unit meta (counts, cache_lengths)   ~ H + 1 units ahead of the index hop
-//     indices  (token_indices)            3H + 1 tiles ahead of compute
-//     page     (kv_lookup_table entries)  2H + 1 tiles ahead
+//     indices  (token_indices)            3H + 1 tiles ahead of the K/V hop's
+//     page     (kv_lookup_table entries)  2H + 1 tiles ahead         ... tile
 //     offsets  (computed from both)        H + 1 tiles ahead
-//     K and V rows                         H     tiles ahead (the stage ring)
-// Warps own heads (WPH = 4 / HPU warps per head split a tile's keys) and run
-// the keys-on-M / heads-on-N mma.sync scheme: S^T = K Q^T, online softmax in
-// base 2, P^T by movmatrix, O^T += V^T P^T.  A unit's end merges the warps in
-// shared memory and writes the output, or — for a shared unit — a partial
-// record; after its range, each CTA arrives on the shared units' tickets and
+// and the K/V rows by 16-byte cp.async (zero-filled for slots without a valid
+// key), each producer thread arriving on the stage's full barrier when its
+// copies land.  Consumers own heads (WPH = 4 / HPU warps per head split a
+// tile's keys) and run the keys-on-M / heads-on-N mma.sync scheme: S^T = K Q^T,
+// online softmax in base 2, P^T by movmatrix, O^T += V^T P^T; they release each
+// stage on its empty barrier.  A unit's end merges the consumer warps in
+// shared memory and writes the output, or, for a shared unit, a partial
+// record; after its range each CTA arrives on the shared units' tickets and
 // the last arrival merges the records (no CTA ever waits for another).
 #pragma once
 
@@ -50,10 +51,6 @@ struct StreamCfg {
   static constexpr int GP = 8 * NT;                 // padded query heads per kv head
   static constexpr int KSTEPS = KIND == kBF16 ? 8 : 4;
   static constexpr int CPK = 2 * KEYB / 16;         // 16-byte chunks per key (K and V)
-  // K/V copy mechanism: one bulk copy per key chunk when chunks are large
-  // (each bulk copy costs its warp a fixed issue time), else 16-byte cp.async
-  // spread over every thread
-  static constexpr bool BULK = KEYB >= 512;
   static constexpr int CHUNKS = TILE * CPK;         // per stage
   static constexpr int RT = 16;                     // tile-record ring (positions, pages, offsets)
   static constexpr int MR = 32;                     // unit-meta ring
@@ -63,18 +60,17 @@ struct StreamCfg {
   static constexpr int STAGES = (5 * STAGE_BYTES + FIXED <= 232448) ? 5 : 4;
   static constexpr int H = STAGES - 1;
   static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
-  static_assert(CHUNKS % kMmaThreads == 0, "stage copy split");
+  static_assert(CHUNKS % 128 == 0, "stage copy split over the producer warps");
   static_assert(KPW % 16 == 0, "warp key slices are 16 keys");
-  static_assert(3 * H + 2 <= RT, "tile-record ring too small");
-  static_assert(4 * H + 4 <= MR, "unit-meta ring too small");
+  // producers run up to STAGES tiles ahead of consumers with hops up to 3H+1
+  // tiles further; the consumers still read a tile's offsets and meta then
+  static_assert(2 * H + 1 + STAGES < RT, "tile-record ring too small");
+  static_assert(3 * H + 1 + STAGES + H + 2 < MR, "unit-meta ring too small");
   static_assert(SMEM <= 232448, "shared memory");
 };
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -94,13 +90,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
-// One-dimensional bulk copy global -> this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
-               "l"(src), "r"(bytes), "r"(bar)
-               : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+// The arrive fires on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+// Barrier over the 128 threads of one role (id 1: producers, id 2: consumers).
+__device__ __forceinline__ void role_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
@@ -109,14 +107,16 @@ __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wai
 
 // A cursor over this CTA's tiles: unit u (its row r, kv-head group hg, valid
 // count n and last tile jl inside the range), tile j, ordinal o.  Every thread
-// holds the same cursor values, so every branch on them is block-uniform.
+// of a role holds the same cursor values, so branches on them are uniform.
 struct TileCursor {
   int u, j, o, r, hg, n, jl;
   bool live;
 };
 
+constexpr int kStreamThreads = 256;  // 4 producer + 4 consumer warps
+
 template <int KIND, int NT, int HPU>
-__global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, const StreamPlan sp) {
+__global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params p, const StreamPlan sp) {
   using C = StreamCfg<KIND, NT, HPU>;
   constexpr int H = C::H, S = C::STAGES, TILE = C::TILE, RT = C::RT, MR = C::MR, GP = C::GP;
   static_assert((RT & (RT - 1)) == 0 && (MR & (MR - 1)) == 0, "rings are powers of two");
@@ -128,24 +128,258 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
   uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
   __shared__ int s_merge[2];
-  __shared__ __align__(8) uint64_t s_full[S];  // one per stage: its K/V bulk copies have landed
+  // A role gave up waiting (never expected).  Each flag is written only by its
+  // own role before that role's barrier, so the role decides uniformly.
+  __shared__ int s_pabort, s_cabort;
+  __shared__ __align__(8) uint64_t s_full[S];    // stage landed: 128 cp.async arrivals + 1 release arrival
+  __shared__ __align__(8) uint64_t s_empty[S];   // stage consumed: one arrival per consumer warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  const int hh = warp / C::WPH, kp = warp % C::WPH;
+  const int rw = warp & 3;                      // warp within its role
   const int VT = sp.VT;
   const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
   if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
-  if (tid == 0) {
-    for (int k = 0; k < S; ++k) mbar_init(smem_addr(&s_full[k]), kMmaThreads / 32);
-    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-  }
-  __syncthreads();
   const int u_first = (int)(t0 / VT), u_last = (int)((t1 - 1) / VT);
   const int jlo_first = (int)(t0 - (int64_t)u_first * VT);  // first tile of the first unit in range
   const int jhi_last = (int)(t1 - (int64_t)u_last * VT);    // end tile of the last unit in range
-  uint32_t bad = 0;
+  if (tid == 0) {
+    for (int k = 0; k < S; ++k) {
+      mbar_init(smem_addr(&s_full[k]), 129);
+      mbar_init(smem_addr(&s_empty[k]), 4);
+    }
+    s_pabort = 0;
+    s_cabort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();  // the last block-wide barrier: the roles part here
 
-  // the CTA whose range holds virtual tile x, and a unit's contributing CTAs
+  auto mslot = [&](int u) { return ((u - u_first) & (MR - 1)) * 4; };
+  // tile j of unit u: jl = last tile inside the range that holds keys (or the
+  // first tile in range when none does: that unit still gets one empty tile)
+  auto unit_jl = [&](int u, int n) {
+    const int jlo = u == u_first ? jlo_first : 0, jhi = u == u_last ? jhi_last : VT;
+    return max(jlo, min(jhi, (n + TILE - 1) / TILE) - 1);
+  };
+  auto unit_n = [&](int u) {
+    const int m = mslot(u);
+    return s_meta[m + 2] < 0 ? 0 : min(max(s_meta[m + 0], 0), p.W);
+  };
+  auto keys_in = [&](int n, int j) { return min(max(n - j * TILE, 0), TILE); };
+
+  if (warp < 4) {
+    // =====================================================================
+    // producers
+    // =====================================================================
+    uint32_t bad = 0;
+    auto find_seq = [&](int r) -> int {  // sequence of row r, -1 when no sequence owns it
+      const bool in_smem = p.batch + 1 <= C::MAXOFF;
+      auto off = [&](int k) { return in_smem ? s_rowoff[k] : __ldg(p.row_offsets + k); };
+      int lo = 0, hi = p.batch;  // largest b in [0, batch] with off[b] <= r
+      if (off(0) > (uint32_t)r) return -1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (off(mid) <= (uint32_t)r) lo = mid; else hi = mid - 1;
+      }
+      if (lo >= p.batch || (uint32_t)r >= off(lo + 1)) return -1;
+      return lo;
+    };
+    auto issue_meta = [&](int u) {  // producer thread 0 only
+      const int r = p.total_q - 1 - u / sp.NG, m = mslot(u);
+      const int b = find_seq(r);
+      s_meta[m + 2] = b;
+      if (b >= 0) {
+        const bool in_smem = p.batch + 1 <= C::MAXOFF;
+        s_meta[m + 3] = (int32_t)((in_smem ? s_rowoff[b + 1] : __ldg(p.row_offsets + b + 1)) -
+                                  (in_smem ? s_rowoff[b] : __ldg(p.row_offsets + b)));
+        cp_async4(smem_addr(&s_meta[m + 0]), p.counts + r);
+        cp_async4(smem_addr(&s_meta[m + 1]), p.cache_lengths + b);
+      } else {
+        s_meta[m + 0] = 0;
+        s_meta[m + 1] = 0;
+        s_meta[m + 3] = 0;
+        bad |= QSA_STATUS_BAD_ROW;
+      }
+    };
+    int meta_issued = u_first, meta_landed = u_first;
+    int hist[H];  // meta_issued at the end of each of the last H iterations
+    auto issue_meta_upto = [&](int u) {
+      u = min(u, u_last);
+      if (u < meta_issued) return;
+      if (tid == 0)
+        for (int v = meta_issued; v <= u; ++v) issue_meta(v);
+      meta_issued = u + 1;
+    };
+    auto ensure_meta = [&](int u) {  // makes unit u's meta readable (a full wait when it has not landed)
+      if (u >= meta_issued) issue_meta_upto(u);
+      if (u >= meta_landed) {
+        cp_async_wait_all();
+        role_sync(1);
+        meta_landed = meta_issued;
+#pragma unroll
+        for (int k = 0; k < H; ++k) hist[k] = meta_issued;
+      }
+    };
+    auto enter = [&](TileCursor& c, int u) {
+      ensure_meta(u);
+      c.u = u;
+      const int q = u / sp.NG;
+      c.r = p.total_q - 1 - q;
+      c.hg = u - q * sp.NG;
+      c.n = unit_n(u);
+      c.jl = unit_jl(u, c.n);
+      c.j = u == u_first ? jlo_first : 0;
+    };
+    auto advance = [&](TileCursor& c) {
+      ++c.o;
+      if (c.j < c.jl) ++c.j;
+      else if (c.u < u_last) enter(c, c.u + 1);
+      else c.live = false;
+    };
+    // hops: indices on warp 1, page entries on warp 2, offsets on warp 3,
+    // K/V copies on all four producer warps
+    auto idx_hop = [&](const TileCursor& c) {
+      if (rw != 1) return;
+      const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE;
+      const int32_t* src = p.indices + (int64_t)c.r * p.W + c.j * TILE;
+      for (int k = lane; k < kt; k += 32) cp_async4(smem_addr(&s_pos[slot + k]), src + k);
+    };
+    auto page_hop = [&](const TileCursor& c) {
+      if (rw != 2) return;
+      const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE;
+      if (kt == 0) return;
+      const int m = mslot(c.u);
+      const int64_t kvl = (int64_t)(uint32_t)s_meta[m + 1] + (int64_t)s_meta[m + 3];
+      const uint32_t* trow = p.table + (int64_t)s_meta[m + 2] * p.max_pages;
+      for (int k = lane; k < kt; k += 32) {
+        const int32_t pos = s_pos[slot + k];
+        uint32_t so = kInvalidOff;
+        if (pos < 0 || (int64_t)pos >= kvl) {
+          bad |= QSA_STATUS_BAD_INDEX;
+        } else {
+          const uint32_t lp = p.log2P >= 0 ? (uint32_t)pos >> p.log2P : (uint32_t)pos / (uint32_t)p.P;
+          if (lp >= (uint32_t)p.max_pages) {
+            bad |= QSA_STATUS_BAD_PAGE;
+          } else {
+            cp_async4(smem_addr(&s_page[slot + k]), trow + lp);
+            so = (uint32_t)pos - lp * (uint32_t)p.P;  // slot within the page
+          }
+        }
+        s_off[slot + k] = so;
+      }
+    };
+    auto off_hop = [&](const TileCursor& c) {
+      if (rw != 3) return;
+      const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE;
+      const int64_t head0 = p.k_layer_bytes + (int64_t)c.hg * HPU * p.head_bytes;
+      for (int k = lane; k < kt; k += 32) {
+        const uint32_t so = s_off[slot + k];
+        if (so == kInvalidOff) continue;
+        const uint32_t page = s_page[slot + k];
+        if (page >= p.num_pages) {
+          bad |= QSA_STATUS_BAD_PAGE;
+          s_off[slot + k] = kInvalidOff;
+        } else {
+          s_off[slot + k] =
+              (uint32_t)(((int64_t)page * p.page_pitch_bytes + head0 + (int64_t)so * p.slot_bytes) >> 4);
+        }
+      }
+    };
+    // this thread's fixed role in a stage copy: key offset, K or V, 16-byte chunk
+    constexpr int KPI = 128 / C::CPK;  // keys per copy round
+    const int my_key = tid / C::CPK, my_w = tid - my_key * C::CPK;
+    const int my_kv = my_w / (C::CPK / 2), my_ch = my_w - my_kv * (C::CPK / 2);
+    const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
+    const int my_dst = my_kv * C::KV_BYTES + my_key * C::SROW + my_ch * 16;
+    // K/V of a tile into its stage, once the consumers have released it;
+    // false when that wait gave up
+    auto kv_hop = [&](const TileCursor& c) -> bool {
+      const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
+      if (c.o >= S) {
+        if (tid == 0) s_pabort = !mbar_wait(smem_addr(&s_empty[st]), (uint32_t)((c.o / S - 1) & 1));
+        role_sync(1);
+        if (s_pabort) return false;
+      }
+      const uint32_t sbase = smem_addr(smem + st * C::STAGE_BYTES) + my_dst;
+#pragma unroll 4
+      for (int i = 0; i < TILE / KPI; ++i) {
+        const int key = i * KPI + my_key;
+        const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
+        const bool live = off != kInvalidOff;
+        cp_async16(sbase + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
+      }
+      cp_async_mbar_arrive(smem_addr(&s_full[st]));
+      // publishes this tile's offsets (consumers mask with them) and every unit
+      // meta written so far: all were written before the last role_sync
+      if (tid == 0) mbar_arrive(smem_addr(&s_full[st]));
+      return true;
+    };
+
+    // prologue
+    if (p.batch + 1 <= C::MAXOFF)
+      for (int k = tid; k <= p.batch; k += 128) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
+    cp_async_wait_all();
+    role_sync(1);
+    issue_meta_upto(u_first + H + 1);
+    cp_async_wait_all();
+    role_sync(1);
+    meta_landed = meta_issued;
+#pragma unroll
+    for (int k = 0; k < H; ++k) hist[k] = meta_issued;
+    TileCursor ci;
+    ci.o = 0;
+    ci.live = true;
+    enter(ci, u_first);
+    TileCursor cpg = ci, cof = ci, ckv = ci;
+    for (int n = 0; n <= 2 * H && ci.live; ++n) {
+      idx_hop(ci);
+      advance(ci);
+    }
+    cp_async_wait_all();
+    role_sync(1);
+    for (int n = 0; n <= H && cpg.live; ++n) {
+      page_hop(cpg);
+      advance(cpg);
+    }
+    cp_async_wait_all();
+    role_sync(1);
+    off_hop(cof);
+    advance(cof);
+    // main loop: one K/V tile per iteration; the hop for the tile t + 1 + kH
+    // lands k iterations later
+    while (ckv.live) {
+      cp_async_wait<H - 1>();
+      role_sync(1);
+      meta_landed = max(meta_landed, hist[H - 1]);
+      if (!kv_hop(ckv)) break;
+      advance(ckv);
+      if (cof.live) {
+        off_hop(cof);
+        advance(cof);
+      }
+      if (cpg.live) {
+        page_hop(cpg);
+        advance(cpg);
+      }
+      if (ci.live) {
+        idx_hop(ci);
+        issue_meta_upto(ci.u + H + 1);
+        advance(ci);
+      }
+      cp_async_commit();
+#pragma unroll
+      for (int k = H - 1; k > 0; --k) hist[k] = hist[k - 1];
+      hist[0] = meta_issued;
+    }
+    cp_async_wait_all();  // no copy of ours may land after we leave
+    if (s_pabort) bad |= QSA_STATUS_TIMEOUT;
+    if (bad) atomicOr(p.status, bad);
+    return;
+  }
+
+  // =========================================================================
+  // consumers
+  // =========================================================================
+  const int hh = rw / C::WPH, kp = rw % C::WPH;
   auto cta_of = [&](int64_t x) { return (int)(((x + 1) * sp.G - 1) / sp.T); };
   auto first_cta = [&](int u) { return cta_of((int64_t)u * VT); };
   auto contributors = [&](int u) { return cta_of((int64_t)(u + 1) * VT - 1) - first_cta(u) + 1; };
@@ -154,194 +388,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     const int uf = (int)((int64_t)c * sp.T / sp.G / VT);
     return p.ws_partial + ((int64_t)2 * c + (u == uf ? 0 : 1)) * sp.rec_floats;
   };
+  const int ctid = tid - 128;
 
-  // ---------------- unit meta ----------------
-  auto mslot = [&](int u) { return ((u - u_first) & (MR - 1)) * 4; };
-  auto find_seq = [&](int r) -> int {  // sequence of row r, -1 when no sequence owns it
-    const bool in_smem = p.batch + 1 <= C::MAXOFF;
-    auto off = [&](int k) { return in_smem ? s_rowoff[k] : __ldg(p.row_offsets + k); };
-    int lo = 0, hi = p.batch;  // largest b in [0, batch] with off[b] <= r
-    if (off(0) > (uint32_t)r) return -1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (off(mid) <= (uint32_t)r) lo = mid; else hi = mid - 1;
-    }
-    if (lo >= p.batch || (uint32_t)r >= off(lo + 1)) return -1;
-    return lo;
-  };
-  auto issue_meta = [&](int u) {  // thread 0 only
-    const int r = p.total_q - 1 - u / sp.NG, m = mslot(u);
-    const int b = find_seq(r);
-    s_meta[m + 2] = b;
-    if (b >= 0) {
-      const bool in_smem = p.batch + 1 <= C::MAXOFF;
-      s_meta[m + 3] = (int32_t)((in_smem ? s_rowoff[b + 1] : __ldg(p.row_offsets + b + 1)) -
-                                (in_smem ? s_rowoff[b] : __ldg(p.row_offsets + b)));
-      cp_async4(smem_addr(&s_meta[m + 0]), p.counts + r);
-      cp_async4(smem_addr(&s_meta[m + 1]), p.cache_lengths + b);
-    } else {
-      s_meta[m + 0] = 0;
-      s_meta[m + 1] = 0;
-      s_meta[m + 3] = 0;
-      bad |= QSA_STATUS_BAD_ROW;
-    }
-  };
-  int meta_issued = u_first, meta_landed = u_first;
-  int hist[H];  // meta_issued at the end of each of the last H iterations
-  auto issue_meta_upto = [&](int u) {
-    u = min(u, u_last);
-    if (u < meta_issued) return;
-    if (tid == 0)
-      for (int v = meta_issued; v <= u; ++v) issue_meta(v);
-    meta_issued = u + 1;
-  };
-  // makes unit u's meta readable (a full wait when it has not landed yet)
-  auto ensure_meta = [&](int u) {
-    if (u >= meta_issued) issue_meta_upto(u);
-    if (u >= meta_landed) {
-      cp_async_wait_all();
-      __syncthreads();
-      meta_landed = meta_issued;
-#pragma unroll
-      for (int k = 0; k < H; ++k) hist[k] = meta_issued;
-    }
-  };
-
-  // ---------------- tile cursors ----------------
-  // Ordinals run over each unit's real tiles inside this range (at least one
-  // per unit: a unit with none gets one empty tile so it is still finished).
-  auto enter = [&](TileCursor& c, int u) {
-    ensure_meta(u);
-    const int m = mslot(u);
-    c.u = u;
-    const int q = u / sp.NG;
-    c.r = p.total_q - 1 - q;
-    c.hg = u - q * sp.NG;
-    c.n = s_meta[m + 2] < 0 ? 0 : min(max(s_meta[m + 0], 0), p.W);
-    const int jlo = u == u_first ? jlo_first : 0, jhi = u == u_last ? jhi_last : VT;
-    c.jl = max(jlo, min(jhi, (c.n + TILE - 1) / TILE) - 1);
-    c.j = jlo;
-  };
-  auto start = [&](TileCursor& c) {
-    enter(c, u_first);
-    c.o = 0;
-    c.live = true;
-  };
-  auto advance = [&](TileCursor& c) {
-    ++c.o;
-    if (c.j < c.jl) {
-      ++c.j;
-    } else if (c.u < u_last) {
-      enter(c, c.u + 1);
-    } else {
-      c.live = false;
-    }
-  };
-  auto keys_in = [&](const TileCursor& c) { return min(max(c.n - c.j * TILE, 0), TILE); };
-
-  // ---------------- hops ----------------
-  // The hops of one iteration run on different warps, in parallel: indices on
-  // warp 1, page entries on warp 2, offsets on warp 3, K/V copies on all.
-  auto idx_hop = [&](const TileCursor& c) {
-    if (warp != 1) return;
-    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
-    const int32_t* src = p.indices + (int64_t)c.r * p.W + c.j * TILE;
-    for (int k = lane; k < kt; k += 32) cp_async4(smem_addr(&s_pos[slot + k]), src + k);
-  };
-  auto page_hop = [&](const TileCursor& c) {
-    if (warp != 2) return;
-    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
-    if (kt == 0) return;
-    const int m = mslot(c.u);
-    const int64_t kvl = (int64_t)(uint32_t)s_meta[m + 1] + (int64_t)s_meta[m + 3];
-    const uint32_t* trow = p.table + (int64_t)s_meta[m + 2] * p.max_pages;
-    for (int k = lane; k < kt; k += 32) {
-      const int32_t pos = s_pos[slot + k];
-      uint32_t so = kInvalidOff;
-      if (pos < 0 || (int64_t)pos >= kvl) {
-        bad |= QSA_STATUS_BAD_INDEX;
-      } else {
-        const uint32_t lp = p.log2P >= 0 ? (uint32_t)pos >> p.log2P : (uint32_t)pos / (uint32_t)p.P;
-        if (lp >= (uint32_t)p.max_pages) {
-          bad |= QSA_STATUS_BAD_PAGE;
-        } else {
-          cp_async4(smem_addr(&s_page[slot + k]), trow + lp);
-          so = (uint32_t)pos - lp * (uint32_t)p.P;  // slot within the page
-        }
-      }
-      s_off[slot + k] = so;
-    }
-  };
-  auto off_hop = [&](const TileCursor& c) {
-    if (warp != 3) return;
-    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE;
-    const int64_t head0 = p.k_layer_bytes + (int64_t)c.hg * HPU * p.head_bytes;
-    for (int k = lane; k < kt; k += 32) {
-      const uint32_t so = s_off[slot + k];
-      if (so == kInvalidOff) continue;
-      const uint32_t page = s_page[slot + k];
-      if (page >= p.num_pages) {
-        bad |= QSA_STATUS_BAD_PAGE;
-        s_off[slot + k] = kInvalidOff;
-      } else {
-        s_off[slot + k] = (uint32_t)(((int64_t)page * p.page_pitch_bytes + head0 + (int64_t)so * p.slot_bytes) >> 4);
-      }
-    }
-  };
-  // K/V of a tile.  Bulk: warp w moves keys w, w+4, ... with one bulk copy per
-  // K or V chunk (HPU heads, contiguous) completing on the stage's mbarrier
-  // (one arrival per warp), and zeroes the V rows of its key slots that hold
-  // no valid key (their scores are masked, but 0 * NaN would not vanish).
-  // Otherwise: 16-byte cp.async over every thread, zero-filled for those
-  // slots, completing with the iteration's cp.async group.
-  constexpr int KPI = kMmaThreads / C::CPK;  // keys per cp.async round (non-bulk)
-  const int my_key = tid / C::CPK, my_w = tid - my_key * C::CPK;
-  const int my_kv = my_w / (C::CPK / 2), my_ch = my_w - my_kv * (C::CPK / 2);
-  const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
-  const int my_dst = my_kv * C::KV_BYTES + my_key * C::SROW + my_ch * 16;
-  auto kv_hop = [&](const TileCursor& c) {
-    const int kt = keys_in(c), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
-    unsigned char* sb = smem + st * C::STAGE_BYTES;
-    if constexpr (C::BULK) {
-      constexpr int KPWARP = (TILE + 3) / 4;  // key slots per warp
-      const int key = warp + 4 * (lane % KPWARP);
-      const bool mine = lane < KPWARP && key < TILE;
-      const bool v = mine && key < kt && s_off[slot + key] != kInvalidOff;
-      const uint32_t nv = __popc(__ballot_sync(0xffffffffu, v));
-      if (mine && !v) {
-        uint4* row = reinterpret_cast<uint4*>(sb + C::KV_BYTES + key * C::SROW);
-        for (int q = 0; q < C::KEYB / 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
-      }
-      fence_proxy_async_smem();  // this warp's generic writes before its async copies
-      __syncwarp();
-      const uint32_t bar = smem_addr(&s_full[st]);
-      if (lane == 0) mbar_arrive_expect_tx(bar, nv * 2u * (uint32_t)C::KEYB);
-      __syncwarp();
-      if (v) {
-        const unsigned char* src = p.kv + (int64_t)s_off[slot + key] * 16;
-        bulk_g2s(smem_addr(sb + key * C::SROW), src, C::KEYB, bar);
-        bulk_g2s(smem_addr(sb + C::KV_BYTES + key * C::SROW), src + p.v_minus_k_bytes, C::KEYB, bar);
-      }
-    } else {
-      const uint32_t sbase = smem_addr(sb) + my_dst;
-#pragma unroll 4
-      for (int i = 0; i < TILE / KPI; ++i) {
-        const int key = i * KPI + my_key;
-        const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
-        const bool live = off != kInvalidOff;
-        cp_async16(sbase + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
-      }
-    }
-  };
-  bool timed_out = false;
-  auto wait_tile = [&](const TileCursor& c) {  // every thread; block-uniform result
-    if constexpr (C::BULK) {
-      const bool ok = mbar_wait(smem_addr(&s_full[c.o % S]), (uint32_t)((c.o / S) & 1));
-      timed_out = __syncthreads_or(!ok) != 0;
-    }
-  };
-
-  // ---------------- per-warp attention state ----------------
   uint32_t qf[NT][C::KSTEPS][2], qn[NT][C::KSTEPS][2];
   auto load_q = [&](int u, uint32_t (&dst)[NT][C::KSTEPS][2]) {
     const int q = u / sp.NG;
@@ -374,9 +422,9 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
   const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_col = ((lane >> 4) & 1) * 16;
   const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8, t_col = ((lane >> 3) & 1) * 16;
 
-  auto compute_tile = [&](const TileCursor& cur) {
-    const int kt = keys_in(cur), slot = (cur.o & (RT - 1)) * TILE;
-    const unsigned char* sb = smem + (cur.o % S) * C::STAGE_BYTES;
+  auto compute_tile = [&](int kt, int ord) {
+    const int slot = (ord & (RT - 1)) * TILE;
+    const unsigned char* sb = smem + (ord % S) * C::STAGE_BYTES;
 #pragma unroll
     for (int sl = 0; sl < C::MSL; ++sl) {
       const int k0 = kp * C::KPW + sl * 16;
@@ -472,10 +520,10 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     }
   };
 
-  // End of a unit: merge the WPH warps of each head in shared memory, then
+  // End of unit u: merge the WPH warps of each head in shared memory, then
   // write the output (unit owned by this CTA) or this CTA's partial record.
   int pend0 = -1, pend1 = -1;
-  auto finish = [&](const TileCursor& cur) {
+  auto finish = [&](int u, bool row_ok) {
     float* sm_o = epi;
     float* sm_m = epi + 4 * GP * C::D;
     float* sm_l = sm_m + 4 * GP;
@@ -488,8 +536,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
         l += __shfl_xor_sync(0xffffffffu, l, 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         if (gid == 0) {
-          sm_m[warp * GP + nt * 8 + 2 * tig + c] = m_run[nt][c];
-          sm_l[warp * GP + nt * 8 + 2 * tig + c] = l;
+          sm_m[rw * GP + nt * 8 + 2 * tig + c] = m_run[nt][c];
+          sm_l[rw * GP + nt * 8 + 2 * tig + c] = l;
         }
       }
 #pragma unroll
@@ -500,16 +548,17 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
         for (int c = 0; c < 4; ++c) {
           const int head = nt * 8 + 2 * tig + (c & 1);
           const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
-          sm_o[(warp * GP + head) * C::D + d] = o[mt][nt][c];
+          sm_o[(rw * GP + head) * C::D + d] = o[mt][nt][c];
         }
-    __syncthreads();
-    const int G = p.group, D = C::D, u = cur.u;
-    const bool row_ok = s_meta[mslot(u) + 2] >= 0;
+    role_sync(2);
+    const int G = p.group, D = C::D;
+    const int q = u / sp.NG;
+    const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
     const bool own = contributors(u) == 1;
     float* rec = own ? nullptr : record(blockIdx.x, u);
     const int64_t stride = partial_stride(G, D);
-    const int64_t out0 = ((int64_t)cur.r * p.nq + (int64_t)cur.hg * HPU * G) * D;
-    for (int idx = tid; idx < HPU * G * D; idx += kMmaThreads) {
+    const int64_t out0 = ((int64_t)r * p.nq + (int64_t)hg * HPU * G) * D;
+    for (int idx = ctid; idx < HPU * G * D; idx += 128) {
       const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
       float M = -CUDART_INF_F;
 #pragma unroll
@@ -538,122 +587,62 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
     if (!own) {
       if (pend0 < 0) pend0 = u; else pend1 = u;
     }
-    __syncthreads();  // the epilogue buffer is free again
+    role_sync(2);  // the epilogue buffer is free again
     reset_state();
   };
 
-  // ---------------- prologue ----------------
-  if (p.batch + 1 <= C::MAXOFF)
-    for (int k = tid; k <= p.batch; k += kMmaThreads) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
-  cp_async_wait_all();
-  __syncthreads();
-  issue_meta_upto(u_first + H + 1);
-  cp_async_wait_all();
-  __syncthreads();
-  meta_landed = meta_issued;
-#pragma unroll
-  for (int k = 0; k < H; ++k) hist[k] = meta_issued;
+  // main loop: wait for a tile, compute it, release its stage
   load_q(u_first, qf);
   if (u_first < u_last) load_q(u_first + 1, qn);
   reset_state();
-
-  TileCursor ci, cpg, cof, ckv, cc;
-  start(ci);
-  cpg = ci;
-  cof = ci;
-  ckv = ci;
-  cc = ci;
-  for (int n = 0; n <= 3 * H && ci.live; ++n) {
-    idx_hop(ci);
-    advance(ci);
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  for (int n = 0; n <= 2 * H && cpg.live; ++n) {
-    page_hop(cpg);
-    advance(cpg);
-  }
-  cp_async_wait_all();
-  __syncthreads();
-  for (int n = 0; n <= H && cof.live; ++n) {
-    off_hop(cof);
-    advance(cof);
-  }
-  __syncthreads();
-  for (int n = 0; n < H; ++n) {
-    if (ckv.live) {
-      kv_hop(ckv);
-      advance(ckv);
+  int u = u_first, j = jlo_first, n = 0, jl = 0, ord = 0;
+  bool entered = false, row_ok = false, aborted = false;
+  while (true) {
+    const int st = ord % S;
+    if (!mbar_wait(smem_addr(&s_full[st]), (uint32_t)((ord / S) & 1))) s_cabort = 1;
+    role_sync(2);
+    if (s_cabort) {
+      aborted = true;
+      break;
     }
-    cp_async_commit();  // empty groups keep the index/page hop accounting of the main loop
-  }
-
-  // ---------------- main loop: one tile per iteration ----------------
-  while (cc.live) {
-    cp_async_wait<H - 1>();
-    __syncthreads();
-    meta_landed = max(meta_landed, hist[H - 1]);
-    if (ckv.live) {
-      kv_hop(ckv);
-      advance(ckv);
+    if (!entered) {  // the unit's meta was published with its first tile
+      n = unit_n(u);
+      jl = unit_jl(u, n);
+      row_ok = s_meta[mslot(u) + 2] >= 0;
+      entered = true;
     }
-    if (cof.live) {
-      off_hop(cof);
-      advance(cof);
+    compute_tile(keys_in(n, j), ord);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&s_empty[st]));
+    ++ord;
+    if (j < jl) {
+      ++j;
+      continue;
     }
-    if (cpg.live) {
-      page_hop(cpg);
-      advance(cpg);
-    }
-    if (ci.live) {
-      idx_hop(ci);
-      issue_meta_upto(ci.u + H + 1);
-      advance(ci);
-    }
-    cp_async_commit();
+    finish(u, row_ok);
+    if (u >= u_last) break;
+    ++u;
+    j = 0;
+    entered = false;
 #pragma unroll
-    for (int k = H - 1; k > 0; --k) hist[k] = hist[k - 1];
-    hist[0] = meta_issued;
-
-    wait_tile(cc);
-    if (timed_out) break;
-    compute_tile(cc);
-    const int u = cc.u;
-    advance(cc);
-    if (!cc.live || cc.u != u) {
-      TileCursor done = cc;
-      done.u = u;
-      done.r = p.total_q - 1 - u / sp.NG;
-      done.hg = u - (u / sp.NG) * sp.NG;
-      finish(done);
-      if (cc.live) {
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int ks = 0; ks < C::KSTEPS; ++ks) {
-            qf[nt][ks][0] = qn[nt][ks][0];
-            qf[nt][ks][1] = qn[nt][ks][1];
-          }
-        if (u + 2 <= u_last) load_q(u + 2, qn);
+      for (int ks = 0; ks < C::KSTEPS; ++ks) {
+        qf[nt][ks][0] = qn[nt][ks][0];
+        qf[nt][ks][1] = qn[nt][ks][1];
       }
-    }
+    if (u + 1 <= u_last) load_q(u + 1, qn);
   }
-  cp_async_wait_all();
-  if (timed_out) {
-    // drain (bounded) the stages still owed bulk copies, then leave; the
-    // status word tells the host the output is not valid
-    if constexpr (C::BULK)
-      for (int o2 = cc.o; o2 < ckv.o; ++o2) mbar_wait(smem_addr(&s_full[o2 % S]), (uint32_t)((o2 / S) & 1));
-    if (tid == 0) atomicOr(p.status, QSA_STATUS_TIMEOUT);
+  if (aborted) {
+    if (ctid == 0) atomicOr(p.status, QSA_STATUS_TIMEOUT);
     return;
   }
-  if (bad) atomicOr(p.status, bad);
 
-  // ---------------- shared units: arrive, and merge if last ----------------
+  // shared units: arrive, and merge if last
   if (pend0 < 0) return;
   __threadfence();
-  __syncthreads();
-  if (tid == 0) {
+  role_sync(2);
+  if (ctid == 0) {
     s_merge[0] = s_merge[1] = -1;
     const int pend[2] = {pend0, pend1};
     for (int k = 0; k < 2; ++k) {
@@ -662,25 +651,25 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       if (t == (uint32_t)(contributors(pend[k]) - 1)) s_merge[k] = pend[k];
     }
   }
-  __syncthreads();
+  role_sync(2);
   for (int k = 0; k < 2; ++k) {
-    const int u = s_merge[k];
-    if (u < 0) continue;
+    const int um = s_merge[k];
+    if (um < 0) continue;
     __threadfence();
-    const int G = p.group, D = C::D, K = contributors(u), c0 = first_cta(u);
-    const int q = u / sp.NG;
-    const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
+    const int G = p.group, D = C::D, K = contributors(um), c0 = first_cta(um);
+    const int q = um / sp.NG;
+    const int r = p.total_q - 1 - q, hg = um - q * sp.NG;
     const int64_t stride = partial_stride(G, D);
     float* s_w = epi;                      // [K][HPU*G] normalised weights
     float* s_mm = epi + K * HPU * G;       // [K][HPU*G] maxima
-    for (int qq = tid; qq < K * HPU * G; qq += kMmaThreads) {
+    for (int qq = ctid; qq < K * HPU * G; qq += 128) {
       const int c = qq / (HPU * G), hi = qq - c * HPU * G, h2 = hi / G, i = hi - h2 * G;
-      const float* part = record(c0 + c, u) + h2 * stride;
+      const float* part = record(c0 + c, um) + h2 * stride;
       s_mm[qq] = __ldcg(part + G * D + i);
       s_w[qq] = __ldcg(part + G * D + G + i);
     }
-    __syncthreads();
-    for (int hi = tid; hi < HPU * G; hi += kMmaThreads) {
+    role_sync(2);
+    for (int hi = ctid; hi < HPU * G; hi += 128) {
       float M = -CUDART_INF_F;
       for (int c = 0; c < K; ++c) M = fmaxf(M, s_mm[c * HPU * G + hi]);
       float L = 0.f;
@@ -689,13 +678,13 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       for (int c = 0; c < K; ++c)
         s_w[c * HPU * G + hi] = M != -CUDART_INF_F ? exp2f(s_mm[c * HPU * G + hi] - M) / L : 0.f;
     }
-    __syncthreads();
-    for (int q4 = tid; q4 < HPU * G * D / 4; q4 += kMmaThreads) {
+    role_sync(2);
+    for (int q4 = ctid; q4 < HPU * G * D / 4; q4 += 128) {
       const int idx = q4 * 4, h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 0; c < K; ++c) {
         const float w = s_w[c * HPU * G + h2 * G + i];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(record(c0 + c, u) + h2 * stride + rem));
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(record(c0 + c, um) + h2 * stride + rem));
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
@@ -707,8 +696,8 @@ __global__ void __launch_bounds__(kMmaThreads, 1) stream_kernel(const Params p, 
       store_out(p, ob + 2, acc.z);
       store_out(p, ob + 3, acc.w);
     }
-    if (tid == 0) p.ws_ticket[u] = 0u;
-    __syncthreads();
+    if (ctid == 0) p.ws_ticket[um] = 0u;
+    role_sync(2);
   }
 }
 
@@ -725,7 +714,7 @@ cudaError_t launch_stream_t(const Params& p, const StreamPlan& sp, cudaStream_t 
     configured_mask |= 1 << (dev & 31);
   }
   if (sp.G == 0) return cudaSuccess;
-  stream_kernel<KIND, NT, HPU><<<sp.G, kMmaThreads, C::SMEM, s>>>(p, sp);
+  stream_kernel<KIND, NT, HPU><<<sp.G, kStreamThreads, C::SMEM, s>>>(p, sp);
   return cudaGetLastError();
 }
 
