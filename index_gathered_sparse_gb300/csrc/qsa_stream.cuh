@@ -52,14 +52,21 @@ struct StreamCfg {
   static constexpr int KSTEPS = KIND == kBF16 ? 8 : 4;
   static constexpr int CPK = 2 * KEYB / 16;         // 16-byte chunks per key (K and V)
   static constexpr int CHUNKS = TILE * CPK;         // per stage
-  static constexpr int RT = 16;                     // tile-record ring (positions, pages, offsets)
-  static constexpr int MR = 32;                     // unit-meta ring
+  static constexpr int RT = TILE <= 32 ? 32 : 16;   // tile-record ring (positions, pages, offsets)
+  static constexpr int MR = 64;                     // unit-meta ring
   static constexpr int MAXOFF = 1024;               // input_row_offsets entries kept in shared memory
-  static constexpr int EPI_FLOATS = 4 * GP * D + 2 * 4 * GP;
+  // Warps that share a head merge through shared memory; a warp that owns its
+  // head writes straight from registers and needs no epilogue buffer.
+  static constexpr int EPI_FLOATS = WPH > 1 ? 4 * GP * D + 2 * 4 * GP : 0;
   static constexpr int FIXED = EPI_FLOATS * 4 + 3 * RT * TILE * 4 + MR * 16 + MAXOFF * 4;
-  static constexpr int STAGES = (5 * STAGE_BYTES + FIXED <= 232448) ? 5 : 4;
+  static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
+  static constexpr int STAGES_CAP = TILE <= 32 ? 8 : 5;
+  static constexpr int STAGES = STAGES_FIT < STAGES_CAP ? STAGES_FIT : STAGES_CAP;
   static constexpr int H = STAGES - 1;
   static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
+  // Consumers copy a tile's K/V fragments to registers and release the stage
+  // before computing, when one 8-head N tile leaves them the registers.
+  static constexpr bool EARLY = NT == 1;
   static_assert(CHUNKS % 128 == 0, "stage copy split over the producer warps");
   static_assert(KPW % 16 == 0, "warp key slices are 16 keys");
   // producers run up to STAGES tiles ahead of consumers with hops up to 3H+1
@@ -67,6 +74,7 @@ struct StreamCfg {
   static_assert(2 * H + 1 + STAGES < RT, "tile-record ring too small");
   static_assert(3 * H + 1 + STAGES + H + 2 < MR, "unit-meta ring too small");
   static_assert(SMEM <= 232448, "shared memory");
+  static_assert(STAGES >= 3, "stage ring");
 };
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -99,6 +107,16 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
 }
 // Barrier over the 128 threads of one role (id 1: producers, id 2: consumers).
 __device__ __forceinline__ void role_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
+// The same barrier, returning whether any of the role's threads passed true.
+__device__ __forceinline__ bool role_any(int id, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)pred), "r"(id)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(dst), "l"(src));
@@ -121,16 +139,14 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   constexpr int H = C::H, S = C::STAGES, TILE = C::TILE, RT = C::RT, MR = C::MR, GP = C::GP;
   static_assert((RT & (RT - 1)) == 0 && (MR & (MR - 1)) == 0, "rings are powers of two");
   extern __shared__ __align__(128) unsigned char smem[];
-  float* epi = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);  // [4][GP][D] + m[4][GP] + l[4][GP]
-  int32_t* s_pos = reinterpret_cast<int32_t*>(epi + C::EPI_FLOATS);  // [RT][TILE]
+  // epilogue buffer [4][GP][D] + m[4][GP] + l[4][GP] (warps sharing a head)
+  float* epi_buf = reinterpret_cast<float*>(smem + S * C::STAGE_BYTES);
+  int32_t* s_pos = reinterpret_cast<int32_t*>(epi_buf + C::EPI_FLOATS);  // [RT][TILE]
   uint32_t* s_page = reinterpret_cast<uint32_t*>(s_pos + RT * TILE); // [RT][TILE]
   uint32_t* s_off = s_page + RT * TILE;                               // [RT][TILE]
   int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
   uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
   __shared__ int s_merge[2];
-  // A role gave up waiting (never expected).  Each flag is written only by its
-  // own role before that role's barrier, so the role decides uniformly.
-  __shared__ int s_pabort, s_cabort;
   __shared__ __align__(8) uint64_t s_full[S];    // stage landed: 128 cp.async arrivals + 1 release arrival
   __shared__ __align__(8) uint64_t s_empty[S];   // stage consumed: one arrival per consumer warp
 
@@ -147,8 +163,6 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       mbar_init(smem_addr(&s_full[k]), 129);
       mbar_init(smem_addr(&s_empty[k]), 4);
     }
-    s_pabort = 0;
-    s_cabort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   __syncthreads();  // the last block-wide barrier: the roles part here
@@ -294,10 +308,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     // false when that wait gave up
     auto kv_hop = [&](const TileCursor& c) -> bool {
       const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
-      if (c.o >= S) {
-        if (tid == 0) s_pabort = !mbar_wait(smem_addr(&s_empty[st]), (uint32_t)((c.o / S - 1) & 1));
-        role_sync(1);
-        if (s_pabort) return false;
+      if (c.o >= S) {  // a give-up by thread 0 becomes every producer's decision
+        const bool lost = tid == 0 && !mbar_wait(smem_addr(&s_empty[st]), (uint32_t)((c.o / S - 1) & 1));
+        if (role_any(1, lost)) return false;
       }
       const uint32_t sbase = smem_addr(smem + st * C::STAGE_BYTES) + my_dst;
 #pragma unroll 4
@@ -346,11 +359,15 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     advance(cof);
     // main loop: one K/V tile per iteration; the hop for the tile t + 1 + kH
     // lands k iterations later
+    bool aborted = false;
     while (ckv.live) {
       cp_async_wait<H - 1>();
       role_sync(1);
       meta_landed = max(meta_landed, hist[H - 1]);
-      if (!kv_hop(ckv)) break;
+      if (!kv_hop(ckv)) {
+        aborted = true;
+        break;
+      }
       advance(ckv);
       if (cof.live) {
         off_hop(cof);
@@ -371,7 +388,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       hist[0] = meta_issued;
     }
     cp_async_wait_all();  // no copy of ours may land after we leave
-    if (s_pabort) bad |= QSA_STATUS_TIMEOUT;
+    if (aborted) bad |= QSA_STATUS_TIMEOUT;
     if (bad) atomicOr(p.status, bad);
     return;
   }
@@ -389,6 +406,9 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     return p.ws_partial + ((int64_t)2 * c + (u == uf ? 0 : 1)) * sp.rec_floats;
   };
   const int ctid = tid - 128;
+  // the epilogue buffer, or, when there is none, the stage ring, which only the
+  // final merge of shared units uses, after every stage has been consumed
+  float* epi = C::EPI_FLOATS ? epi_buf : reinterpret_cast<float*>(smem);
 
   uint32_t qf[NT][C::KSTEPS][2], qn[NT][C::KSTEPS][2];
   auto load_q = [&](int u, uint32_t (&dst)[NT][C::KSTEPS][2]) {
@@ -421,112 +441,165 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   };
   const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_col = ((lane >> 4) & 1) * 16;
   const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8, t_col = ((lane >> 3) & 1) * 16;
+  constexpr int VLD = KIND == kBF16 ? 8 : 4;  // transposing ldmatrix.x4 per 16-key slice of V
 
-  auto compute_tile = [&](int kt, int ord) {
+  // One 16-key slice of this warp: its K and V fragments and key masks.
+  struct Slice {
+    uint32_t k[C::KSTEPS][4];
+    uint32_t v[C::EARLY ? VLD : 1][4];  // without EARLY, V is read from the stage during PV
+    uint32_t vbase;
+    bool vA, vB, any;
+  };
+  auto load_slice = [&](Slice& f, int kt, int ord, int sl) {
     const int slot = (ord & (RT - 1)) * TILE;
     const unsigned char* sb = smem + (ord % S) * C::STAGE_BYTES;
+    const int k0 = kp * C::KPW + sl * 16;
+    const int kA = k0 + gid, kB = kA + 8;
+    f.vA = kA < kt && s_off[slot + kA] != kInvalidOff;
+    f.vB = kB < kt && s_off[slot + kB] != kInvalidOff;
+    f.any = __any_sync(0xffffffffu, f.vA || f.vB);
+    if (!f.any) return;
+    const uint32_t kbase = smem_addr(sb) + k0 * C::SROW + hh * C::ROWB;
+    const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + k0 * C::SROW + hh * C::ROWB;
 #pragma unroll
-    for (int sl = 0; sl < C::MSL; ++sl) {
-      const int k0 = kp * C::KPW + sl * 16;
-      const int kA = k0 + gid, kB = kA + 8;
-      const bool vA = kA < kt && s_off[slot + kA] != kInvalidOff;
-      const bool vB = kB < kt && s_off[slot + kB] != kInvalidOff;
-      if (!__any_sync(0xffffffffu, vA || vB)) continue;
-      const uint32_t kbase = smem_addr(sb) + k0 * C::SROW + hh * C::ROWB;
-      const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + k0 * C::SROW + hh * C::ROWB;
-      float s[NT][4], s2[NT][4];
+    for (int ks = 0; ks < C::KSTEPS; ++ks) ldsm_x4(kbase + a_row * C::SROW + ks * 32 + a_col, f.k[ks]);
+    f.vbase = vbase + t_row * C::SROW + t_col;
+    if constexpr (C::EARLY) {
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+      for (int mt = 0; mt < VLD; ++mt) ldsm_x4_t(f.vbase + mt * 32, f.v[mt]);
+    }
+  };
+  auto v_frag = [&](const Slice& f, int mt, uint32_t (&a)[4]) {
+    if constexpr (C::EARLY) {
 #pragma unroll
-      for (int ks = 0; ks < C::KSTEPS; ++ks) {  // two accumulator chains halve the dependent-MMA latency
-        uint32_t a[4];
-        ldsm_x4(kbase + a_row * C::SROW + ks * 32 + a_col, a);
+      for (int k = 0; k < 4; ++k) a[k] = f.v[C::EARLY ? mt : 0][k];
+    } else {
+      ldsm_x4_t(f.vbase + mt * 32, a);
+    }
+  };
+  auto compute_slice = [&](const Slice& f) {
+    if (!f.any) return;
+    float s[NT][4], s2[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          if constexpr (KIND == kBF16) {
-            if (ks & 1) mma_bf16(s2[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
-            else mma_bf16(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
-          } else {
-            if (ks & 1) mma_e4m3(s2[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
-            else mma_e4m3(s[nt], a, qf[nt][ks][0], qf[nt][ks][1]);
-          }
-        }
-      }
-      uint32_t pb[NT][2];
+    for (int nt = 0; nt < NT; ++nt)
+      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {  // two accumulator chains halve the dependent-MMA latency
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float pv[4];
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const float x0 = vA ? (s[nt][c] + s2[nt][c]) * p.scale_log2 : -CUDART_INF_F;
-          const float x1 = vB ? (s[nt][2 + c] + s2[nt][2 + c]) * p.scale_log2 : -CUDART_INF_F;
-          float mx = fmaxf(x0, x1);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mnew = fmaxf(m_run[nt][c], mx);
-          const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
-          const float alpha = exp2f(m_run[nt][c] - muse);
-          const float p0 = exp2f(x0 - muse), p1 = exp2f(x1 - muse);
-          l_run[nt][c] = l_run[nt][c] * alpha + p0 + p1;
-          m_run[nt][c] = mnew;
-          pv[c] = p0;
-          pv[2 + c] = p1;
-          if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-              o[mt][nt][c] *= alpha;
-              o[mt][nt][2 + c] *= alpha;
-            }
-          }
+        if constexpr (KIND == kBF16) {
+          if (ks & 1) mma_bf16(s2[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
+          else mma_bf16(s[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
+        } else {
+          if (ks & 1) mma_e4m3(s2[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
+          else mma_e4m3(s[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
         }
-        const uint32_t top = KIND == kBF16 ? pack_bf16(pv[0], pv[1]) : pack_f16(pv[0], pv[1]);
-        const uint32_t bot = KIND == kBF16 ? pack_bf16(pv[2], pv[3]) : pack_f16(pv[2], pv[3]);
-        pb[nt][0] = movmatrix_t(top);
-        pb[nt][1] = movmatrix_t(bot);
       }
-      if constexpr (KIND == kBF16) {
+    }
+    uint32_t pb[NT][2];
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          uint32_t a[4];
-          ldsm_x4_t(vbase + t_row * C::SROW + mt * 32 + t_col, a);
+    for (int nt = 0; nt < NT; ++nt) {
+      float pv[4];
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-        }
-      } else {
+      for (int c = 0; c < 2; ++c) {
+        const float x0 = f.vA ? (s[nt][c] + s2[nt][c]) * p.scale_log2 : -CUDART_INF_F;
+        const float x1 = f.vB ? (s[nt][2 + c] + s2[nt][2 + c]) * p.scale_log2 : -CUDART_INF_F;
+        float mx = fmaxf(x0, x1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m_run[nt][c], mx);
+        const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
+        const float alpha = exp2f(m_run[nt][c] - muse);
+        const float p0 = exp2f(x0 - muse), p1 = exp2f(x1 - muse);
+        l_run[nt][c] = l_run[nt][c] * alpha + p0 + p1;
+        m_run[nt][c] = mnew;
+        pv[c] = p0;
+        pv[2 + c] = p1;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-        for (int pr = 0; pr < 4; ++pr) {
-          uint32_t r4[4];
-          ldsm_x4_t(vbase + t_row * C::SROW + pr * 32 + t_col, r4);
-          uint32_t ae[4], ao[4];
-          const uint32_t q0 = __byte_perm(r4[0], 0, 0x3120), q1 = __byte_perm(r4[1], 0, 0x3120);
-          const uint32_t q2 = __byte_perm(r4[2], 0, 0x3120), q3 = __byte_perm(r4[3], 0, 0x3120);
-          ae[0] = e4m3x2_to_f16x2(q0 & 0xFFFFu);
-          ae[1] = e4m3x2_to_f16x2(q0 >> 16);
-          ae[2] = e4m3x2_to_f16x2(q2 & 0xFFFFu);
-          ae[3] = e4m3x2_to_f16x2(q2 >> 16);
-          ao[0] = e4m3x2_to_f16x2(q1 & 0xFFFFu);
-          ao[1] = e4m3x2_to_f16x2(q1 >> 16);
-          ao[2] = e4m3x2_to_f16x2(q3 & 0xFFFFu);
-          ao[3] = e4m3x2_to_f16x2(q3 >> 16);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            mma_f16(o[2 * pr][nt], ae, pb[nt][0], pb[nt][1]);
-            mma_f16(o[2 * pr + 1][nt], ao, pb[nt][0], pb[nt][1]);
+          for (int mt = 0; mt < 8; ++mt) {
+            o[mt][nt][c] *= alpha;
+            o[mt][nt][2 + c] *= alpha;
           }
+        }
+      }
+      const uint32_t top = KIND == kBF16 ? pack_bf16(pv[0], pv[1]) : pack_f16(pv[0], pv[1]);
+      const uint32_t bot = KIND == kBF16 ? pack_bf16(pv[2], pv[3]) : pack_f16(pv[2], pv[3]);
+      pb[nt][0] = movmatrix_t(top);
+      pb[nt][1] = movmatrix_t(bot);
+    }
+    if constexpr (KIND == kBF16) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        uint32_t a[4];
+        v_frag(f, mt, a);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a, pb[nt][0], pb[nt][1]);
+      }
+    } else {
+#pragma unroll
+      for (int pr = 0; pr < 4; ++pr) {
+        // e4m3 rows are read as byte pairs: the transposing ldmatrix hands this
+        // thread (key 2tig, 2tig+1) x (d 2gid, 2gid+1) of each 16-byte column
+        // block; output rows of an M tile are d = 16mt + 2gid and 16mt + 2gid + 1
+        uint32_t r4[4];
+        v_frag(f, pr, r4);
+        uint32_t ae[4], ao[4];
+        const uint32_t q0 = __byte_perm(r4[0], 0, 0x3120), q1 = __byte_perm(r4[1], 0, 0x3120);
+        const uint32_t q2 = __byte_perm(r4[2], 0, 0x3120), q3 = __byte_perm(r4[3], 0, 0x3120);
+        ae[0] = e4m3x2_to_f16x2(q0 & 0xFFFFu);
+        ae[1] = e4m3x2_to_f16x2(q0 >> 16);
+        ae[2] = e4m3x2_to_f16x2(q2 & 0xFFFFu);
+        ae[3] = e4m3x2_to_f16x2(q2 >> 16);
+        ao[0] = e4m3x2_to_f16x2(q1 & 0xFFFFu);
+        ao[1] = e4m3x2_to_f16x2(q1 >> 16);
+        ao[2] = e4m3x2_to_f16x2(q3 & 0xFFFFu);
+        ao[3] = e4m3x2_to_f16x2(q3 >> 16);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_f16(o[2 * pr][nt], ae, pb[nt][0], pb[nt][1]);
+          mma_f16(o[2 * pr + 1][nt], ao, pb[nt][0], pb[nt][1]);
         }
       }
     }
   };
+  // A tile: with EARLY, every slice's fragments come to registers and the
+  // stage is released before any math; otherwise slice by slice, then release.
+  auto consume_tile = [&](int kt, int ord) {
+    const uint32_t empty = smem_addr(&s_empty[ord % S]);
+    if constexpr (C::EARLY) {
+      Slice f[C::MSL];
+#pragma unroll
+      for (int sl = 0; sl < C::MSL; ++sl) load_slice(f[sl], kt, ord, sl);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty);
+#pragma unroll
+      for (int sl = 0; sl < C::MSL; ++sl) compute_slice(f[sl]);
+    } else {
+#pragma unroll
+      for (int sl = 0; sl < C::MSL; ++sl) {
+        Slice f;
+        load_slice(f, kt, ord, sl);
+        compute_slice(f);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty);
+    }
+  };
 
-  // End of unit u: merge the WPH warps of each head in shared memory, then
-  // write the output (unit owned by this CTA) or this CTA's partial record.
+  // End of unit u: output (unit owned by this CTA) or this CTA's partial
+  // record.  A warp that owns its head writes from registers; warps sharing a
+  // head merge in shared memory first.
   int pend0 = -1, pend1 = -1;
   auto finish = [&](int u, bool row_ok) {
-    float* sm_o = epi;
-    float* sm_m = epi + 4 * GP * C::D;
-    float* sm_l = sm_m + 4 * GP;
+    const int G = p.group, D = C::D;
+    const int q = u / sp.NG;
+    const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
+    const bool own = contributors(u) == 1;
+    float* rec = own ? nullptr : record(blockIdx.x, u);
+    const int64_t stride = partial_stride(G, D);
+    float lsum[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -535,73 +608,101 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
         l += __shfl_xor_sync(0xffffffffu, l, 4);
         l += __shfl_xor_sync(0xffffffffu, l, 8);
         l += __shfl_xor_sync(0xffffffffu, l, 16);
-        if (gid == 0) {
-          sm_m[rw * GP + nt * 8 + 2 * tig + c] = m_run[nt][c];
-          sm_l[rw * GP + nt * 8 + 2 * tig + c] = l;
-        }
+        lsum[nt][c] = l;
       }
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
+    if constexpr (C::WPH == 1) {
+      const int h = hg * HPU + hh;
+      const int64_t out0 = ((int64_t)r * p.nq + (int64_t)h * G) * D;
+      float* part = own ? nullptr : rec + hh * stride;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int head = nt * 8 + 2 * tig + (c & 1);
-          const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
-          sm_o[(rw * GP + head) * C::D + d] = o[mt][nt][c];
+        for (int c = 0; c < 2; ++c) {
+          const int head = nt * 8 + 2 * tig + c;
+          if (head >= G) continue;
+          const bool live = row_ok && m_run[nt][c] != -CUDART_INF_F;
+          const float inv = live ? 1.f / lsum[nt][c] : 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int hi = 0; hi < 2; ++hi) {
+              const int d = KIND == kBF16 ? mt * 16 + gid + hi * 8 : mt * 16 + 2 * gid + hi;
+              const float v = o[mt][nt][2 * hi + c];
+              if (own) store_out(p, out0 + (int64_t)head * D + d, live ? v * inv : 0.f);
+              else part[head * D + d] = v;
+            }
+          if (!own && gid == 0) {
+            part[G * D + head] = m_run[nt][c];
+            part[G * D + G + head] = lsum[nt][c];
+          }
         }
-    role_sync(2);
-    const int G = p.group, D = C::D;
-    const int q = u / sp.NG;
-    const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
-    const bool own = contributors(u) == 1;
-    float* rec = own ? nullptr : record(blockIdx.x, u);
-    const int64_t stride = partial_stride(G, D);
-    const int64_t out0 = ((int64_t)r * p.nq + (int64_t)hg * HPU * G) * D;
-    for (int idx = ctid; idx < HPU * G * D; idx += 128) {
-      const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
-      float M = -CUDART_INF_F;
+    } else {
+      float* sm_o = epi;
+      float* sm_m = epi + 4 * GP * C::D;
+      float* sm_l = sm_m + 4 * GP;
 #pragma unroll
-      for (int k = 0; k < C::WPH; ++k) M = fmaxf(M, sm_m[(h2 * C::WPH + k) * GP + i]);
-      float L = 0.f, O = 0.f;
-      if (M != -CUDART_INF_F) {
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int k = 0; k < C::WPH; ++k) {
-          const int w = h2 * C::WPH + k;
-          const float e = exp2f(sm_m[w * GP + i] - M);
-          L += sm_l[w * GP + i] * e;
-          O += sm_o[(w * GP + i) * D + d] * e;
+        for (int c = 0; c < 2; ++c)
+          if (gid == 0) {
+            sm_m[rw * GP + nt * 8 + 2 * tig + c] = m_run[nt][c];
+            sm_l[rw * GP + nt * 8 + 2 * tig + c] = lsum[nt][c];
+          }
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const int head = nt * 8 + 2 * tig + (c & 1);
+            const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
+            sm_o[(rw * GP + head) * C::D + d] = o[mt][nt][c];
+          }
+      role_sync(2);
+      const int64_t out0 = ((int64_t)r * p.nq + (int64_t)hg * HPU * G) * D;
+      for (int idx = ctid; idx < HPU * G * D; idx += 128) {
+        const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
+        float M = -CUDART_INF_F;
+#pragma unroll
+        for (int k = 0; k < C::WPH; ++k) M = fmaxf(M, sm_m[(h2 * C::WPH + k) * GP + i]);
+        float L = 0.f, O = 0.f;
+        if (M != -CUDART_INF_F) {
+#pragma unroll
+          for (int k = 0; k < C::WPH; ++k) {
+            const int w = h2 * C::WPH + k;
+            const float e = exp2f(sm_m[w * GP + i] - M);
+            L += sm_l[w * GP + i] * e;
+            O += sm_o[(w * GP + i) * D + d] * e;
+          }
+        }
+        if (own) {
+          store_out(p, out0 + idx, row_ok && M != -CUDART_INF_F ? O / L : 0.f);
+        } else {
+          float* part = rec + h2 * stride;
+          part[rem] = O;
+          if (d == 0) {
+            part[G * D + i] = M;
+            part[G * D + G + i] = L;
+          }
         }
       }
-      if (own) {
-        store_out(p, out0 + idx, row_ok && M != -CUDART_INF_F ? O / L : 0.f);
-      } else {
-        float* part = rec + h2 * stride;
-        part[rem] = O;
-        if (d == 0) {
-          part[G * D + i] = M;
-          part[G * D + G + i] = L;
-        }
-      }
+      role_sync(2);  // the epilogue buffer is free again
     }
     if (!own) {
       if (pend0 < 0) pend0 = u; else pend1 = u;
     }
-    role_sync(2);  // the epilogue buffer is free again
     reset_state();
   };
 
-  // main loop: wait for a tile, compute it, release its stage
+  // main loop: wait for a tile, consume it (releasing its stage), finish units
   load_q(u_first, qf);
   if (u_first < u_last) load_q(u_first + 1, qn);
   reset_state();
   int u = u_first, j = jlo_first, n = 0, jl = 0, ord = 0;
   bool entered = false, row_ok = false, aborted = false;
   while (true) {
-    const int st = ord % S;
-    if (!mbar_wait(smem_addr(&s_full[st]), (uint32_t)((ord / S) & 1))) s_cabort = 1;
-    role_sync(2);
-    if (s_cabort) {
+    const bool ok = mbar_wait(smem_addr(&s_full[ord % S]), (uint32_t)((ord / S) & 1));
+    if (role_any(2, !ok)) {  // a give-up by any consumer is every consumer's decision
       aborted = true;
       break;
     }
@@ -611,9 +712,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       row_ok = s_meta[mslot(u) + 2] >= 0;
       entered = true;
     }
-    compute_tile(keys_in(n, j), ord);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&s_empty[st]));
+    consume_tile(keys_in(n, j), ord);
     ++ord;
     if (j < jl) {
       ++j;
