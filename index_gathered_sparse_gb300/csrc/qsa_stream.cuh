@@ -12,8 +12,9 @@
 // the load is balanced to a tile and at most the first and the last unit of a
 // range are shared with other CTAs.  Tiles past a unit's count are skipped.
 //
-// Roles.  Warps 0-3 produce, warps 4-7 consume, linked per stage by a "full"
-// and an "empty" mbarrier.  Producers fetch everything a tile needs in hops
+// Roles.  The first PW warps produce (eight with one 8-head N tile, else
+// four), the last four consume, linked per stage by a "full" and an "empty"
+// mbarrier.  Producers fetch everything a tile needs in hops
 // spaced H = STAGES - 1 producer iterations apart, so each hop has landed when
 // the next one reads it and nothing waits on a dependent load in steady state:
 //     unit meta (counts, cache_lengths)   ~ H + 1 units ahead of the index hop
@@ -66,8 +67,14 @@ struct StreamCfg {
   static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
   // Consumers copy a tile's K/V fragments to registers and release the stage
   // before computing, when one 8-head N tile leaves them the registers.
-  static constexpr bool EARLY = NT == 1;
-  static_assert(CHUNKS % 128 == 0, "stage copy split over the producer warps");
+  // Producer warps: eight when the consumers fit the 168 registers a thread of
+  // a 384-thread CTA gets (one 8-head N tile), else four; more producers keep
+  // more copies in flight while some of them translate.
+  static constexpr int PW = NT == 1 ? 8 : 4;
+  static constexpr int PT = PW * 32;
+  static constexpr int THREADS = PT + 128;
+  static constexpr bool EARLY = NT == 1 && PW == 4;
+  static_assert(CHUNKS % PT == 0, "stage copy split over the producer warps");
   static_assert(KPW % 16 == 0, "warp key slices are 16 keys");
   // producers run up to STAGES tiles ahead of consumers with hops up to 3H+1
   // tiles further; the consumers still read a tile's offsets and meta then
@@ -105,15 +112,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
 }
-// Barrier over the 128 threads of one role (id 1: producers, id 2: consumers).
-__device__ __forceinline__ void role_sync(int id) { asm volatile("bar.sync %0, 128;\n" ::"r"(id) : "memory"); }
+// Barrier over the `n` threads of one role (id 1: producers, id 2: consumers).
+__device__ __forceinline__ void role_sync(int id, int n) { asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(n) : "memory"); }
 // The same barrier, returning whether any of the role's threads passed true.
-__device__ __forceinline__ bool role_any(int id, bool pred) {
+__device__ __forceinline__ bool role_any(int id, int n, bool pred) {
   uint32_t r;
   asm volatile(
-      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, 128, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %1, 0;\n bar.red.or.pred po, %2, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
       : "=r"(r)
-      : "r"((uint32_t)pred), "r"(id)
+      : "r"((uint32_t)pred), "r"(id), "r"(n)
       : "memory");
   return r != 0;
 }
@@ -131,10 +138,8 @@ struct TileCursor {
   bool live;
 };
 
-constexpr int kStreamThreads = 256;  // 4 producer + 4 consumer warps
-
 template <int KIND, int NT, int HPU>
-__global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params p, const StreamPlan sp) {
+__global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_kernel(const Params p, const StreamPlan sp) {
   using C = StreamCfg<KIND, NT, HPU>;
   constexpr int H = C::H, S = C::STAGES, TILE = C::TILE, RT = C::RT, MR = C::MR, GP = C::GP;
   static_assert((RT & (RT - 1)) == 0 && (MR & (MR - 1)) == 0, "rings are powers of two");
@@ -147,11 +152,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
   uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
   __shared__ int s_merge[2];
-  __shared__ __align__(8) uint64_t s_full[S];    // stage landed: 128 cp.async arrivals + 1 release arrival
+  __shared__ __align__(8) uint64_t s_full[S];    // stage landed: PT cp.async arrivals + 1 release arrival
   __shared__ __align__(8) uint64_t s_empty[S];   // stage consumed: one arrival per consumer warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
-  const int rw = warp & 3;                      // warp within its role
+  constexpr int PT = C::PT;
+  const int rw = warp < C::PW ? warp : warp - C::PW;  // warp within its role
   const int VT = sp.VT;
   const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
   if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
@@ -160,7 +166,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   const int jhi_last = (int)(t1 - (int64_t)u_last * VT);    // end tile of the last unit in range
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
-      mbar_init(smem_addr(&s_full[k]), 129);
+      mbar_init(smem_addr(&s_full[k]), PT + 1);
       mbar_init(smem_addr(&s_empty[k]), 4);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -180,7 +186,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   };
   auto keys_in = [&](int n, int j) { return min(max(n - j * TILE, 0), TILE); };
 
-  if (warp < 4) {
+  if (warp < C::PW) {
     // =====================================================================
     // producers
     // =====================================================================
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       if (u >= meta_issued) issue_meta_upto(u);
       if (u >= meta_landed) {
         cp_async_wait_all();
-        role_sync(1);
+        role_sync(1, PT);
         meta_landed = meta_issued;
 #pragma unroll
         for (int k = 0; k < H; ++k) hist[k] = meta_issued;
@@ -299,7 +305,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       }
     };
     // this thread's fixed role in a stage copy: key offset, K or V, 16-byte chunk
-    constexpr int KPI = 128 / C::CPK;  // keys per copy round
+    constexpr int KPI = PT / C::CPK;  // keys per copy round
     const int my_key = tid / C::CPK, my_w = tid - my_key * C::CPK;
     const int my_kv = my_w / (C::CPK / 2), my_ch = my_w - my_kv * (C::CPK / 2);
     const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
       if (c.o >= S) {  // a give-up by thread 0 becomes every producer's decision
         const bool lost = tid == 0 && !mbar_wait(smem_addr(&s_empty[st]), (uint32_t)((c.o / S - 1) & 1));
-        if (role_any(1, lost)) return false;
+        if (role_any(1, PT, lost)) return false;
       }
       const uint32_t sbase = smem_addr(smem + st * C::STAGE_BYTES) + my_dst;
 #pragma unroll 4
@@ -329,12 +335,12 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
 
     // prologue
     if (p.batch + 1 <= C::MAXOFF)
-      for (int k = tid; k <= p.batch; k += 128) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
+      for (int k = tid; k <= p.batch; k += PT) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
     cp_async_wait_all();
-    role_sync(1);
+    role_sync(1, PT);
     issue_meta_upto(u_first + H + 1);
     cp_async_wait_all();
-    role_sync(1);
+    role_sync(1, PT);
     meta_landed = meta_issued;
 #pragma unroll
     for (int k = 0; k < H; ++k) hist[k] = meta_issued;
@@ -348,13 +354,13 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       advance(ci);
     }
     cp_async_wait_all();
-    role_sync(1);
+    role_sync(1, PT);
     for (int n = 0; n <= H && cpg.live; ++n) {
       page_hop(cpg);
       advance(cpg);
     }
     cp_async_wait_all();
-    role_sync(1);
+    role_sync(1, PT);
     off_hop(cof);
     advance(cof);
     // main loop: one K/V tile per iteration; the hop for the tile t + 1 + kH
@@ -362,7 +368,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     bool aborted = false;
     while (ckv.live) {
       cp_async_wait<H - 1>();
-      role_sync(1);
+      role_sync(1, PT);
       meta_landed = max(meta_landed, hist[H - 1]);
       if (!kv_hop(ckv)) {
         aborted = true;
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
     const int uf = (int)((int64_t)c * sp.T / sp.G / VT);
     return p.ws_partial + ((int64_t)2 * c + (u == uf ? 0 : 1)) * sp.rec_floats;
   };
-  const int ctid = tid - 128;
+  const int ctid = tid - PT;
   // the epilogue buffer, or, when there is none, the stage ring, which only the
   // final merge of shared units uses, after every stage has been consumed
   float* epi = C::EPI_FLOATS ? epi_buf : reinterpret_cast<float*>(smem);
@@ -658,7 +664,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
             const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
             sm_o[(rw * GP + head) * C::D + d] = o[mt][nt][c];
           }
-      role_sync(2);
+      role_sync(2, 128);
       const int64_t out0 = ((int64_t)r * p.nq + (int64_t)hg * HPU * G) * D;
       for (int idx = ctid; idx < HPU * G * D; idx += 128) {
         const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
@@ -686,7 +692,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
           }
         }
       }
-      role_sync(2);  // the epilogue buffer is free again
+      role_sync(2, 128);  // the epilogue buffer is free again
     }
     if (!own) {
       if (pend0 < 0) pend0 = u; else pend1 = u;
@@ -702,7 +708,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   bool entered = false, row_ok = false, aborted = false;
   while (true) {
     const bool ok = mbar_wait(smem_addr(&s_full[ord % S]), (uint32_t)((ord / S) & 1));
-    if (role_any(2, !ok)) {  // a give-up by any consumer is every consumer's decision
+    if (role_any(2, 128, !ok)) {  // a give-up by any consumer is every consumer's decision
       aborted = true;
       break;
     }
@@ -740,7 +746,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
   // shared units: arrive, and merge if last
   if (pend0 < 0) return;
   __threadfence();
-  role_sync(2);
+  role_sync(2, 128);
   if (ctid == 0) {
     s_merge[0] = s_merge[1] = -1;
     const int pend[2] = {pend0, pend1};
@@ -750,7 +756,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       if (t == (uint32_t)(contributors(pend[k]) - 1)) s_merge[k] = pend[k];
     }
   }
-  role_sync(2);
+  role_sync(2, 128);
   for (int k = 0; k < 2; ++k) {
     const int um = s_merge[k];
     if (um < 0) continue;
@@ -767,7 +773,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       s_mm[qq] = __ldcg(part + G * D + i);
       s_w[qq] = __ldcg(part + G * D + G + i);
     }
-    role_sync(2);
+    role_sync(2, 128);
     for (int hi = ctid; hi < HPU * G; hi += 128) {
       float M = -CUDART_INF_F;
       for (int c = 0; c < K; ++c) M = fmaxf(M, s_mm[c * HPU * G + hi]);
@@ -777,7 +783,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       for (int c = 0; c < K; ++c)
         s_w[c * HPU * G + hi] = M != -CUDART_INF_F ? exp2f(s_mm[c * HPU * G + hi] - M) / L : 0.f;
     }
-    role_sync(2);
+    role_sync(2, 128);
     for (int q4 = ctid; q4 < HPU * G * D / 4; q4 += 128) {
       const int idx = q4 * 4, h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -796,7 +802,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1) stream_kernel(const Params 
       store_out(p, ob + 3, acc.w);
     }
     if (ctid == 0) p.ws_ticket[um] = 0u;
-    role_sync(2);
+    role_sync(2, 128);
   }
 }
 
@@ -813,7 +819,7 @@ cudaError_t launch_stream_t(const Params& p, const StreamPlan& sp, cudaStream_t 
     configured_mask |= 1 << (dev & 31);
   }
   if (sp.G == 0) return cudaSuccess;
-  stream_kernel<KIND, NT, HPU><<<sp.G, kStreamThreads, C::SMEM, s>>>(p, sp);
+  stream_kernel<KIND, NT, HPU><<<sp.G, C::THREADS, C::SMEM, s>>>(p, sp);
   return cudaGetLastError();
 }
 
