@@ -74,6 +74,11 @@ struct StreamCfg {
   static constexpr int PT = PW * 32;
   static constexpr int THREADS = PT + 128;
   static constexpr bool EARLY = NT == 1 && PW == 4;
+  // K/V copies: one bulk copy per key chunk when chunks are 512 B or more (a
+  // warp pays a fixed issue time per bulk copy), else 16-byte cp.async, whose
+  // outstanding copies are limited per thread.
+  static constexpr bool BULK = KEYB >= 512;
+  static constexpr int FULL_ARRIVALS = BULK ? PW : PT + 1;
   static_assert(CHUNKS % PT == 0, "stage copy split over the producer warps");
   static_assert(KPW % 16 == 0, "warp key slices are 16 keys");
   // producers run up to STAGES tiles ahead of consumers with hops up to 3H+1
@@ -105,6 +110,16 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+// One-dimensional bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
@@ -152,7 +167,9 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
   uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
   __shared__ int s_merge[2];
-  __shared__ __align__(8) uint64_t s_full[S];    // stage landed: PT cp.async arrivals + 1 release arrival
+  // stage landed: one expect-tx arrival per producer warp (bulk copies), or one
+  // cp.async arrival per producer thread plus one release arrival
+  __shared__ __align__(8) uint64_t s_full[S];
   __shared__ __align__(8) uint64_t s_empty[S];   // stage consumed: one arrival per consumer warp
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, gid = lane >> 2, tig = lane & 3;
@@ -166,7 +183,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   const int jhi_last = (int)(t1 - (int64_t)u_last * VT);    // end tile of the last unit in range
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
-      mbar_init(smem_addr(&s_full[k]), PT + 1);
+      mbar_init(smem_addr(&s_full[k]), C::FULL_ARRIVALS);
       mbar_init(smem_addr(&s_empty[k]), 4);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
@@ -311,25 +328,53 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     const int64_t my_src = (my_kv ? p.v_minus_k_bytes : 0) + my_ch * 16;
     const int my_dst = my_kv * C::KV_BYTES + my_key * C::SROW + my_ch * 16;
     // K/V of a tile into its stage, once the consumers have released it;
-    // false when that wait gave up
+    // false when that wait gave up.  Slots without a valid key hold zeros:
+    // their scores are masked, but 0 * NaN would not vanish.
     auto kv_hop = [&](const TileCursor& c) -> bool {
       const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
       if (c.o >= S) {  // a give-up by thread 0 becomes every producer's decision
         const bool lost = tid == 0 && !mbar_wait(smem_addr(&s_empty[st]), (uint32_t)((c.o / S - 1) & 1));
         if (role_any(1, PT, lost)) return false;
       }
-      const uint32_t sbase = smem_addr(smem + st * C::STAGE_BYTES) + my_dst;
+      const uint32_t bar = smem_addr(&s_full[st]);
+      if constexpr (C::BULK) {
+        // producer warp w moves keys w, w + PW, ...: one bulk copy per K and per
+        // V chunk; its lane 0 then arrives with the bytes to expect (and so
+        // also publishes the tile's offsets and the unit meta, written before
+        // the last producer barrier)
+        constexpr int KPWARP = (TILE + C::PW - 1) / C::PW;
+        unsigned char* sb = smem + st * C::STAGE_BYTES;
+        const int key = rw + C::PW * lane;
+        const bool mine = lane < KPWARP && key < TILE;
+        const bool v = mine && key < kt && s_off[slot + key] != kInvalidOff;
+        const uint32_t nv = __popc(__ballot_sync(0xffffffffu, v));
+        if (mine && !v) {
+          uint4* row = reinterpret_cast<uint4*>(sb + C::KV_BYTES + key * C::SROW);
+          for (int q = 0; q < C::KEYB / 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();  // generic writes to the ring before later async copies into it
+        __syncwarp();
+        if (lane == 0) mbar_arrive_expect_tx(bar, nv * 2u * (uint32_t)C::KEYB);
+        __syncwarp();
+        if (v) {
+          const unsigned char* src = p.kv + (int64_t)s_off[slot + key] * 16;
+          bulk_g2s(smem_addr(sb + key * C::SROW), src, C::KEYB, bar);
+          bulk_g2s(smem_addr(sb + C::KV_BYTES + key * C::SROW), src + p.v_minus_k_bytes, C::KEYB, bar);
+        }
+      } else {
+        const uint32_t sbase = smem_addr(smem + st * C::STAGE_BYTES) + my_dst;
 #pragma unroll 4
-      for (int i = 0; i < TILE / KPI; ++i) {
-        const int key = i * KPI + my_key;
-        const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
-        const bool live = off != kInvalidOff;
-        cp_async16(sbase + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
+        for (int i = 0; i < TILE / KPI; ++i) {
+          const int key = i * KPI + my_key;
+          const uint32_t off = key < kt ? s_off[slot + key] : kInvalidOff;
+          const bool live = off != kInvalidOff;
+          cp_async16(sbase + i * KPI * C::SROW, live ? p.kv + (int64_t)off * 16 + my_src : p.kv, live ? 16u : 0u);
+        }
+        cp_async_mbar_arrive(bar);
+        // publishes this tile's offsets (consumers mask with them) and every unit
+        // meta written so far: all were written before the last producer barrier
+        if (tid == 0) mbar_arrive(bar);
       }
-      cp_async_mbar_arrive(smem_addr(&s_full[st]));
-      // publishes this tile's offsets (consumers mask with them) and every unit
-      // meta written so far: all were written before the last role_sync
-      if (tid == 0) mbar_arrive(smem_addr(&s_full[st]));
       return true;
     };
 
