@@ -220,7 +220,12 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       if (lo >= p.batch || (uint32_t)r >= off(lo + 1)) return -1;
       return lo;
     };
-    auto issue_meta = [&](int u) {  // producer thread 0 only
+    // unit meta in two parts: the row's count (needs nothing), then its
+    // sequence, that sequence's rows and cached length (needs the offsets)
+    auto issue_meta_count = [&](int u) {  // producer thread 0 only
+      cp_async4(smem_addr(&s_meta[mslot(u) + 0]), p.counts + (p.total_q - 1 - u / sp.NG));
+    };
+    auto issue_meta_seq = [&](int u) {  // producer thread 0 only
       const int r = p.total_q - 1 - u / sp.NG, m = mslot(u);
       const int b = find_seq(r);
       s_meta[m + 2] = b;
@@ -228,14 +233,16 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
         const bool in_smem = p.batch + 1 <= C::MAXOFF;
         s_meta[m + 3] = (int32_t)((in_smem ? s_rowoff[b + 1] : __ldg(p.row_offsets + b + 1)) -
                                   (in_smem ? s_rowoff[b] : __ldg(p.row_offsets + b)));
-        cp_async4(smem_addr(&s_meta[m + 0]), p.counts + r);
         cp_async4(smem_addr(&s_meta[m + 1]), p.cache_lengths + b);
       } else {
-        s_meta[m + 0] = 0;
         s_meta[m + 1] = 0;
         s_meta[m + 3] = 0;
         bad |= QSA_STATUS_BAD_ROW;
       }
+    };
+    auto issue_meta = [&](int u) {
+      issue_meta_count(u);
+      issue_meta_seq(u);
     };
     int meta_issued = u_first, meta_landed = u_first;
     int hist[H];  // meta_issued at the end of each of the last H iterations
@@ -378,14 +385,20 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       return true;
     };
 
-    // prologue
+    // prologue: offsets and the first counts, then the sequences' meta
+    // together with the first index hops (which need only counts), then page
+    // entries, then K/V
+    const int u_pro = min(u_first + H + 1, u_last);
     if (p.batch + 1 <= C::MAXOFF)
       for (int k = tid; k <= p.batch; k += PT) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
+    if (tid == 0)
+      for (int v = u_first; v <= u_pro; ++v) issue_meta_count(v);
     cp_async_wait_all();
     role_sync(1, PT);
-    issue_meta_upto(u_first + H + 1);
-    cp_async_wait_all();
-    role_sync(1, PT);
+    if (tid == 0)
+      for (int v = u_first; v <= u_pro; ++v) issue_meta_seq(v);
+    meta_issued = u_pro + 1;
+    role_sync(1, PT);  // the sequence ids are plain stores; cached lengths land with the index hops
     meta_landed = meta_issued;
 #pragma unroll
     for (int k = 0; k < H; ++k) hist[k] = meta_issued;
@@ -451,10 +464,15 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   auto cta_of = [&](int64_t x) { return (int)(((x + 1) * sp.G - 1) / sp.T); };
   auto first_cta = [&](int u) { return cta_of((int64_t)u * VT); };
   auto contributors = [&](int u) { return cta_of((int64_t)(u + 1) * VT - 1) - first_cta(u) + 1; };
-  // a shared unit's partial record: two per CTA (its first and its last unit)
-  auto record = [&](int c, int u) {
-    const int uf = (int)((int64_t)c * sp.T / sp.G / VT);
-    return p.ws_partial + ((int64_t)2 * c + (u == uf ? 0 : 1)) * sp.rec_floats;
+  // A shared unit's partial records: two per CTA, slot 0 for the CTA's first
+  // unit and slot 1 for its last.  Every contributor after a unit's first
+  // starts its range inside that unit, so only the first one can hold the
+  // unit in slot 1 (when its range starts before the unit).
+  auto own_record = [&](int u) { return p.ws_partial + ((int64_t)2 * blockIdx.x + (u == u_first ? 0 : 1)) * sp.rec_floats; };
+  auto record_of = [&](int c0, int c, int u) {  // contributor c0 + c of unit u
+    int slot = 0;
+    if (c == 0) slot = (int64_t)c0 * sp.T / sp.G == (int64_t)u * VT ? 0 : 1;
+    return p.ws_partial + ((int64_t)2 * (c0 + c) + slot) * sp.rec_floats;
   };
   const int ctid = tid - PT;
   // the epilogue buffer, or, when there is none, the stage ring, which only the
@@ -648,7 +666,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     const int q = u / sp.NG;
     const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
     const bool own = contributors(u) == 1;
-    float* rec = own ? nullptr : record(blockIdx.x, u);
+    float* rec = own ? nullptr : own_record(u);
     const int64_t stride = partial_stride(G, D);
     float lsum[NT][2];
 #pragma unroll
@@ -812,9 +830,12 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     const int64_t stride = partial_stride(G, D);
     float* s_w = epi;                      // [K][HPU*G] normalised weights
     float* s_mm = epi + K * HPU * G;       // [K][HPU*G] maxima
+    const float* rec0 = record_of(c0, 0, um);
+    const float* rec1 = record_of(c0, 1, um);  // contributors 1.. are 2 * rec_floats apart
+    auto rec_c = [&](int c) { return c == 0 ? rec0 : rec1 + (int64_t)2 * (c - 1) * sp.rec_floats; };
     for (int qq = ctid; qq < K * HPU * G; qq += 128) {
       const int c = qq / (HPU * G), hi = qq - c * HPU * G, h2 = hi / G, i = hi - h2 * G;
-      const float* part = record(c0 + c, um) + h2 * stride;
+      const float* part = rec_c(c) + h2 * stride;
       s_mm[qq] = __ldcg(part + G * D + i);
       s_w[qq] = __ldcg(part + G * D + G + i);
     }
@@ -834,7 +855,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
       for (int c = 0; c < K; ++c) {
         const float w = s_w[c * HPU * G + h2 * G + i];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(record(c0 + c, um) + h2 * stride + rem));
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(rec_c(c) + h2 * stride + rem));
         acc.x = fmaf(w, v.x, acc.x);
         acc.y = fmaf(w, v.y, acc.y);
         acc.z = fmaf(w, v.z, acc.z);
