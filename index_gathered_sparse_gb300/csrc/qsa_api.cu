@@ -235,7 +235,7 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     qsa::StreamPlan& sp = R.sp;
     sp.HPU = R.nkv % 4 == 0 ? 4 : R.nkv % 2 == 0 ? 2 : 1;
     sp.NG = (int32_t)(R.nkv / sp.HPU);
-    const int64_t tile = (R.elem == qsa::kBF16 ? 16 : 32) * (4 / sp.HPU);
+    const int64_t tile = qsa::stream_tile(R.elem == qsa::kBF16 ? 2 : 1, sp.HPU);
     sp.VT = (int32_t)std::max<int64_t>(1, (R.W + tile - 1) / tile);
     sp.U = (int32_t)(R.total_q * sp.NG);
     sp.T = (int64_t)sp.U * sp.VT;

@@ -48,6 +48,12 @@ struct StreamPlan {
   int32_t rec_floats; // floats of one partial record (HPU heads)
 };
 
+// Keys per stage of the stream-K kernel for head_dim 128: 64 KB of K+V when
+// each consumer warp owns a head (HPU == 4), else 32 KB.
+__host__ __device__ constexpr int stream_tile(int elem_bytes, int hpu) {
+  return (hpu == 4 ? 65536 : 32768) / (2 * hpu * 128 * elem_bytes);
+}
+
 // Element type tags.
 enum Elem { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
 

@@ -43,8 +43,10 @@ struct StreamCfg {
   static constexpr int ROWB = D * ELEM;             // one head's K (or V) row
   static constexpr int KEYB = HPU * ROWB;           // a unit's K (or V) bytes per key, contiguous
   static constexpr int SROW = KEYB + 16;            // padded shared-memory row (conflict-free ldmatrix)
-  static constexpr int TILE = (KIND == kBF16 ? 16 : 32) * (4 / HPU);  // keys per stage: 32 KB of K+V
   static constexpr int WPH = 4 / HPU;               // warps per head
+  // keys per stage: 64 KB of K+V when each warp owns a head (no epilogue
+  // buffer competes for shared memory), else 32 KB
+  static constexpr int TILE = stream_tile(ELEM, HPU);
   static constexpr int KPW = TILE / WPH;            // keys per warp per tile
   static constexpr int MSL = KPW / 16;              // 16-key MMA slices per warp per tile
   static constexpr int KV_BYTES = TILE * SROW;
