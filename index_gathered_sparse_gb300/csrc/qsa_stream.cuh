@@ -339,12 +339,15 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     // K/V of a tile into its stage, once the consumers have released it;
     // false when that wait gave up.  Slots without a valid key hold zeros:
     // their scores are masked, but 0 * NaN would not vanish.
-    auto kv_hop = [&](const TileCursor& c) -> bool {
+    // Thread 0 waits until the consumers have released the stage of K/V tile
+    // c (the other producers learn of it, or of a give-up, at the next
+    // producer barrier); false after a give-up.
+    auto stage_free = [&](const TileCursor& c) -> bool {
+      if (tid != 0 || c.o < S) return true;
+      return mbar_wait(smem_addr(&s_empty[c.o % S]), (uint32_t)((c.o / S - 1) & 1));
+    };
+    auto kv_hop = [&](const TileCursor& c) {
       const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
-      if (c.o >= S) {  // a give-up by thread 0 becomes every producer's decision
-        const bool lost = tid == 0 && !mbar_wait(smem_addr(&s_empty[st]), (uint32_t)((c.o / S - 1) & 1));
-        if (role_any(1, PT, lost)) return false;
-      }
       const uint32_t bar = smem_addr(&s_full[st]);
       if constexpr (C::BULK) {
         // producer warp w moves keys w, w + PW, ...: one bulk copy per K and per
@@ -384,7 +387,6 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
         // meta written so far: all were written before the last producer barrier
         if (tid == 0) mbar_arrive(bar);
       }
-      return true;
     };
 
     // prologue: offsets and the first counts, then the sequences' meta
@@ -428,12 +430,13 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     bool aborted = false;
     while (ckv.live) {
       cp_async_wait<H - 1>();
-      role_sync(1, PT);
-      meta_landed = max(meta_landed, hist[H - 1]);
-      if (!kv_hop(ckv)) {
+      const bool lost = !stage_free(ckv);
+      if (role_any(1, PT, lost)) {  // one barrier per tile: hops landed, stage free
         aborted = true;
         break;
       }
+      meta_landed = max(meta_landed, hist[H - 1]);
+      kv_hop(ckv);
       advance(ckv);
       if (cof.live) {
         off_hop(cof);
