@@ -665,7 +665,8 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   // End of unit u: output (unit owned by this CTA) or this CTA's partial
   // record.  A warp that owns its head writes from registers; warps sharing a
   // head merge in shared memory first.
-  int pend0 = -1, pend1 = -1;
+  uint32_t first_ticket = 0xFFFFFFFFu;  // consumer thread 0: ticket taken for u_first
+  int pend_last = -1;                   // shared unit still to arrive on at the end
   auto finish = [&](int u, bool row_ok) {
     const int G = p.group, D = C::D;
     const int q = u / sp.NG;
@@ -763,7 +764,16 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       role_sync(2, 128);  // the epilogue buffer is free again
     }
     if (!own) {
-      if (pend0 < 0) pend0 = u; else pend1 = u;
+      // publish the partial; arrive on the unit's ticket now when it is this
+      // CTA's first unit (the CTA before finishes it late, so it is rarely
+      // the last arrival) and keep the answer for the end of the range
+      __threadfence();
+      role_sync(2, 128);
+      if (u == u_first && u != u_last) {
+        if (ctid == 0) first_ticket = atomicAdd(p.ws_ticket + u, 1u);
+      } else {
+        pend_last = u;
+      }
     }
     reset_state();
   };
@@ -811,18 +821,13 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     return;
   }
 
-  // shared units: arrive, and merge if last
-  if (pend0 < 0) return;
-  __threadfence();
-  role_sync(2, 128);
+  // Shared units: arrive on the last one's ticket, then merge every shared
+  // unit this CTA arrived on last (no CTA ever waits for another).
   if (ctid == 0) {
     s_merge[0] = s_merge[1] = -1;
-    const int pend[2] = {pend0, pend1};
-    for (int k = 0; k < 2; ++k) {
-      if (pend[k] < 0) continue;
-      const uint32_t t = atomicAdd(p.ws_ticket + pend[k], 1u);
-      if (t == (uint32_t)(contributors(pend[k]) - 1)) s_merge[k] = pend[k];
-    }
+    if (first_ticket != 0xFFFFFFFFu && first_ticket == (uint32_t)(contributors(u_first) - 1)) s_merge[0] = u_first;
+    if (pend_last >= 0 && atomicAdd(p.ws_ticket + pend_last, 1u) == (uint32_t)(contributors(pend_last) - 1))
+      s_merge[1] = pend_last;
   }
   role_sync(2, 128);
   for (int k = 0; k < 2; ++k) {
@@ -833,47 +838,51 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     const int q = um / sp.NG;
     const int r = p.total_q - 1 - q, hg = um - q * sp.NG;
     const int64_t stride = partial_stride(G, D);
-    float* s_w = epi;                      // [K][HPU*G] normalised weights
-    float* s_mm = epi + K * HPU * G;       // [K][HPU*G] maxima
     const float* rec0 = record_of(c0, 0, um);
     const float* rec1 = record_of(c0, 1, um);  // contributors 1.. are 2 * rec_floats apart
     auto rec_c = [&](int c) { return c == 0 ? rec0 : rec1 + (int64_t)2 * (c - 1) * sp.rec_floats; };
-    for (int qq = ctid; qq < K * HPU * G; qq += 128) {
-      const int c = qq / (HPU * G), hi = qq - c * HPU * G, h2 = hi / G, i = hi - h2 * G;
-      const float* part = rec_c(c) + h2 * stride;
-      s_mm[qq] = __ldcg(part + G * D + i);
-      s_w[qq] = __ldcg(part + G * D + G + i);
-    }
-    role_sync(2, 128);
-    for (int hi = ctid; hi < HPU * G; hi += 128) {
-      float M = -CUDART_INF_F;
-      for (int c = 0; c < K; ++c) M = fmaxf(M, s_mm[c * HPU * G + hi]);
-      float L = 0.f;
-      if (M != -CUDART_INF_F)
-        for (int c = 0; c < K; ++c) L += s_w[c * HPU * G + hi] * exp2f(s_mm[c * HPU * G + hi] - M);
-      for (int c = 0; c < K; ++c)
-        s_w[c * HPU * G + hi] = M != -CUDART_INF_F ? exp2f(s_mm[c * HPU * G + hi] - M) / L : 0.f;
-    }
-    role_sync(2, 128);
+    // online merge over the contributors, four records' loads in flight at a time
     for (int q4 = ctid; q4 < HPU * G * D / 4; q4 += 128) {
       const int idx = q4 * 4, h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D;
+      float M = -CUDART_INF_F, L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int c = 0; c < K; ++c) {
-        const float w = s_w[c * HPU * G + h2 * G + i];
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(rec_c(c) + h2 * stride + rem));
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+      for (int cb = 0; cb < K; cb += 4) {
+        float mm[4], ll[4];
+        float4 oo[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          if (cb + c < K) {
+            const float* part = rec_c(cb + c) + h2 * stride;
+            mm[c] = __ldcg(part + G * D + i);
+            ll[c] = __ldcg(part + G * D + G + i);
+            oo[c] = __ldcg(reinterpret_cast<const float4*>(part + rem));
+          } else {
+            mm[c] = -CUDART_INF_F;
+            ll[c] = 0.f;
+            oo[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const float Mn = fmaxf(M, mm[c]);
+          if (Mn == -CUDART_INF_F) continue;  // nothing seen yet
+          const float a = exp2f(M - Mn), b = exp2f(mm[c] - Mn);
+          acc.x = acc.x * a + oo[c].x * b;
+          acc.y = acc.y * a + oo[c].y * b;
+          acc.z = acc.z * a + oo[c].z * b;
+          acc.w = acc.w * a + oo[c].w * b;
+          L = L * a + ll[c] * b;
+          M = Mn;
+        }
       }
+      const float inv = M != -CUDART_INF_F ? 1.f / L : 0.f;
       const int64_t ob = ((int64_t)r * p.nq + (int64_t)(hg * HPU + h2) * G) * D + rem;
-      store_out(p, ob, acc.x);
-      store_out(p, ob + 1, acc.y);
-      store_out(p, ob + 2, acc.z);
-      store_out(p, ob + 3, acc.w);
+      store_out(p, ob, acc.x * inv);
+      store_out(p, ob + 1, acc.y * inv);
+      store_out(p, ob + 2, acc.z * inv);
+      store_out(p, ob + 3, acc.w * inv);
     }
     if (ctid == 0) p.ws_ticket[um] = 0u;
-    role_sync(2, 128);
   }
 }
 
