@@ -184,6 +184,54 @@ QSA_API qsa_status qsa_release_device_state(void);
  * Synchronises `stream`; for tests and debugging, not the hot path. */
 QSA_API qsa_status qsa_read_device_status(void* stream, int32_t clear, uint32_t* flags);
 
+/* Bytes of the fixed device scratch used by
+ * qsa_sparse_attention_ragged_paged_noalloc (16 MiB). */
+#define QSA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * qsa_sparse_attention_ragged_paged_noalloc - the same operation, arguments
+ * and result as qsa_sparse_attention_ragged_paged, for callers that cannot
+ * let a library allocate device memory: an engine that reserves nearly all of
+ * the GPU's memory for its own pools at start-up and passes plugins only
+ * buffers it owns, or a latency-bound loop that cannot take the device-wide
+ * synchronisation cudaMalloc/cudaFree imply.  This entry point is a library
+ * addition; the paper has no counterpart.
+ *
+ * It never calls cudaMalloc, cudaFree or any allocating routine.  It always
+ * runs the persistent stream-K tensor-core kernel, so q / kv_blocks must be
+ * BF16 or F8E4M3 with head_dim 128 (else QSA_ERR_UNSUPPORTED).  That kernel's
+ * scratch (records of (row, kv-head group) units that two or more CTAs share,
+ * and their arrival tickets) lives in a fixed array of
+ * QSA_NOALLOC_SCRATCH_BYTES inside the library's device image, which every
+ * GPU that loads the library holds until the process exits.  A call whose
+ * scratch would not fit (roughly total_q * num_kv_heads beyond a few million)
+ * returns QSA_ERR_UNSUPPORTED with the sizes in qsa_last_error_message, before
+ * anything is enqueued.
+ *
+ *   status_flags  optional DEVICE pointer to a uint32 (4-byte aligned) that
+ *                 kernels OR QSA_STATUS_* bits into; the caller zeroes and
+ *                 reads it.  NULL sends the bits to a word in the scratch that
+ *                 nothing reports.  qsa_read_device_status does not see
+ *                 either.
+ *
+ * Set-up: the first call on a device (with that device current) looks up the
+ * scratch array's device address once and keeps it; make that first call
+ * before any stream capture begins.  Each call then enqueues a clear of the
+ * tickets and the kernel on `stream`.
+ *
+ * Every call on a device uses the same scratch, which keeps what the last
+ * call left there: calls whose GPU work overlaps (different streams, or
+ * different host threads without ordering between their streams) race on it
+ * and may produce wrong outputs.  Order such calls on one stream or with
+ * events.
+ */
+QSA_API qsa_status qsa_sparse_attention_ragged_paged_noalloc(
+    qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks,
+    int64_t page_stride, qsa_tensor cache_lengths, qsa_tensor kv_lookup_table,
+    uint32_t max_prompt_length, uint32_t max_cache_length, uint32_t layer_idx,
+    qsa_tensor token_indices, qsa_tensor counts, float scale, int32_t group, void* stream,
+    uint32_t* status_flags);
+
 /* Human-readable name of a status code (static storage). */
 QSA_API const char* qsa_status_string(qsa_status status);
 

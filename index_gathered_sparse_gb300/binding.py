@@ -209,3 +209,41 @@ def qsa_status_string(status: int) -> str:
 
 def qsa_version() -> int:
     return load_library().qsa_version()
+
+
+_noalloc_ready = False
+
+
+def qsa_sparse_attention_ragged_paged_noalloc(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
+                                              kv_lookup_table, max_prompt_length, max_cache_length, layer_idx,
+                                              token_indices, counts, scale, group, stream=None,
+                                              status_flags: Optional[torch.Tensor] = None) -> None:
+    """The allocation-free variant: same operation, enqueued on ``stream``
+    with the library's fixed device scratch instead of a cudaMalloc'd
+    workspace (persistent stream-K kernel; BF16/F8E4M3 with head_dim 128).
+    ``status_flags`` is an optional one-element int32 device tensor that
+    receives the QSA_STATUS_* bits.  Calls that overlap on the GPU share the
+    scratch and race; the first call on a device should come before any
+    stream capture."""
+    global _noalloc_ready
+    lib = load_library()
+    fn = lib.qsa_sparse_attention_ragged_paged_noalloc
+    if not _noalloc_ready:
+        T, P, i32, i64, u32 = qsa_tensor, ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32
+        fn.argtypes = [T, T, T, T, i64, T, T, u32, u32, u32, T, T, ctypes.c_float, i32, P, P]
+        fn.restype = ctypes.c_int
+        _noalloc_ready = True
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    flags = None
+    if status_flags is not None:
+        if status_flags.dtype not in (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ()) \
+                or status_flags.numel() < 1 or not status_flags.is_cuda:
+            raise ValueError("status_flags must be a CUDA tensor of at least one 32-bit integer")
+        flags = status_flags.data_ptr()
+    _check(fn(_contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets),
+              _kv_desc(kv_blocks, int(page_stride)), int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table),
+              int(max_prompt_length), int(max_cache_length), int(layer_idx), _contig(token_indices, "token_indices"),
+              _contig(counts, "counts"), float(scale), int(group), ctypes.c_void_p(stream), ctypes.c_void_p(flags)))

@@ -575,3 +575,127 @@ const char* qsa_last_error_message(void) { return g_last_error.c_str(); }
 int32_t qsa_version(void) { return (0 << 16) | 1; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Some callers cannot let a library call cudaMalloc: an engine that reserves
+// nearly all of the device's memory for its own pools (KV cache, activations)
+// at start-up and hands plugins only buffers it owns, or a serving loop that
+// must not pay cudaMalloc/cudaFree's implicit device synchronisation.  For
+// them qsa_sparse_attention_ragged_paged_noalloc runs the persistent stream-K
+// kernel with its scratch (shared-unit partial records, arrival tickets and a
+// fallback status word) in the fixed array below instead of a per-stream
+// workspace.  The array is part of the library's device image, so every GPU
+// that loads the library holds it until the process exits.
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[QSA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNoallocMaxDevices = 64;
+constexpr size_t kNoallocStatusBytes = 256;  // [0, 256): status word when the caller passes none
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_base[kNoallocMaxDevices];  // device address of g_noalloc_scratch, per device
+
+// Once per device, with that device current: the scratch array's device
+// address.  In host code the name g_noalloc_scratch is only a stand-in for
+// the symbol, so the address has to be asked for.
+qsa_status noalloc_base(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kNoallocMaxDevices)
+    return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_attention_ragged_paged_noalloc: device ordinal above 63");
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  if (!g_noalloc_base[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static scratch)");
+    g_noalloc_base[dev] = ptr;
+  }
+  *out = static_cast<unsigned char*>(g_noalloc_base[dev]);
+  return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" qsa_status qsa_sparse_attention_ragged_paged_noalloc(
+    qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks, int64_t page_stride,
+    qsa_tensor cache_lengths, qsa_tensor kv_lookup_table, uint32_t max_prompt_length, uint32_t max_cache_length,
+    uint32_t layer_idx, qsa_tensor token_indices, qsa_tensor counts, float scale, int32_t group, void* stream,
+    uint32_t* status_flags) {
+  (void)max_prompt_length;
+  (void)max_cache_length;
+  if (reinterpret_cast<uintptr_t>(status_flags) & 3u)
+    return fail(QSA_ERR_ARG, "qsa_sparse_attention_ragged_paged_noalloc: status_flags must be 4-byte aligned");
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  unsigned char* base = nullptr;
+  qsa_status s = noalloc_base(dev, &base);
+  if (s != QSA_OK) return s;
+
+  qsa_options opt;
+  std::memset(&opt, 0, sizeof(opt));
+  opt.kernel = 3;
+  Resolved R;
+  s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table, layer_idx,
+                 token_indices, counts, group, &opt, R);
+  if (s != QSA_OK) return s;
+  if (R.total_q == 0) return QSA_OK;
+  s = plan_launch(R, group, &opt, dev);
+  if (s != QSA_OK) return s;
+
+  // scratch layout: status word | partial records | tickets
+  const size_t ticket_bytes = (R.ws_tickets * sizeof(uint32_t) + 255) / 256 * 256;
+  const size_t need = kNoallocStatusBytes + R.ws_partial_bytes + ticket_bytes;
+  if (need > (size_t)QSA_NOALLOC_SCRATCH_BYTES)
+    return fail(QSA_ERR_UNSUPPORTED,
+                "qsa_sparse_attention_ragged_paged_noalloc: this call needs " + std::to_string(need) +
+                    " bytes of scratch (total_q * num_kv_heads too large); the static scratch holds " +
+                    std::to_string((size_t)QSA_NOALLOC_SCRATCH_BYTES) + " (use qsa_sparse_attention_ragged_paged)");
+  float* partial = reinterpret_cast<float*>(base + kNoallocStatusBytes);
+  uint32_t* tickets = reinterpret_cast<uint32_t*>(base + kNoallocStatusBytes + R.ws_partial_bytes);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array keeps whatever the last call left; tickets must start at zero
+  e = cudaMemsetAsync(tickets, 0, R.ws_tickets * sizeof(uint32_t), st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(static scratch tickets)");
+
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.status = status_flags ? status_flags : reinterpret_cast<uint32_t*>(base);
+  p.ws_partial = partial;
+  p.ws_ticket = tickets;
+  const int64_t eb = elem_bytes(q.dtype);
+  p.out = output.data;
+  p.q = static_cast<const unsigned char*>(q.data);
+  p.row_offsets = static_cast<const uint32_t*>(input_row_offsets.data);
+  p.kv = static_cast<const unsigned char*>(kv_blocks.data);
+  p.cache_lengths = static_cast<const uint32_t*>(cache_lengths.data);
+  p.table = static_cast<const uint32_t*>(kv_lookup_table.data);
+  p.indices = static_cast<const int32_t*>(token_indices.data);
+  p.counts = static_cast<const int32_t*>(counts.data);
+  p.page_pitch_bytes = R.pitch * eb;
+  p.k_layer_bytes = (int64_t)layer_idx * R.P * R.nkv * R.D * eb;
+  p.v_minus_k_bytes = R.L * R.P * R.nkv * R.D * eb;
+  p.slot_bytes = R.nkv * R.D * eb;
+  p.head_bytes = R.D * eb;
+  p.total_q = (int32_t)R.total_q;
+  p.batch = (int32_t)R.batch;
+  p.nq = (int32_t)R.nq;
+  p.nkv = (int32_t)R.nkv;
+  p.group = group;
+  p.D = (int32_t)R.D;
+  p.P = (int32_t)R.P;
+  p.log2P = -1;
+  for (int k = 0; k < 31; ++k)
+    if ((int64_t)1 << k == R.P) p.log2P = k;
+  p.W = (int32_t)R.W;
+  p.max_pages = (int32_t)R.max_pages;
+  p.num_pages = (uint32_t)R.num_pages;
+  p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax in base 2
+  p.out_bf16 = R.out_bf16;
+  p.splits = R.splits;
+  p.band = R.band;
+  e = R.elem == qsa::kBF16 ? qsa::launch_stream_bf16(p, R.sp, st) : qsa::launch_stream_e4m3(p, R.sp, st);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return QSA_OK;
+}
