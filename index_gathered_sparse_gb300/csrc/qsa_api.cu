@@ -250,11 +250,11 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
       G = st.sms;
     }
     G = std::min<int64_t>(G, sp.T);
-    // a unit is shared by at most kmax CTAs; the last one merges their records in
-    // shared memory sized for 32, so spread less when ranges get too short
-    auto kmax = [&](int64_t g) { return (sp.VT + sp.T / g - 1) / (sp.T / g) + 1; };
-    while (G > 1 && kmax(G) > 32) G = std::max<int64_t>(1, G / 2);
     sp.G = (int32_t)std::max<int64_t>(G, 1);
+    // With more units than CTAs, split the tiles that hold keys (the kernel
+    // scans the counts); with fewer, each unit spreads over CTAs anyway and
+    // the scan's extra dependent read costs more than the balance gains.
+    sp.scan = sp.U > sp.G ? 1 : 0;
     sp.rec_floats = (int32_t)(sp.HPU * qsa::partial_stride(group, R.D));
     R.splits = 1;
     R.ctas = sp.G;

@@ -39,13 +39,16 @@ struct Params {
 
 // Launch plan of the persistent stream-K kernel (computed on the host).
 struct StreamPlan {
-  int64_t T;          // virtual key tiles over all units
+  int64_t T;          // most key tiles the units can hold (U * VT); the kernel splits the real ones
   int32_t U;          // units: query row x group of HPU kv heads
-  int32_t VT;         // virtual tiles per unit (selection_width / TILE, rounded up)
+  int32_t VT;         // most tiles per unit (selection_width / TILE, rounded up)
   int32_t G;          // CTAs (one per SM at most)
   int32_t NG;         // kv-head groups per row (num_kv_heads / HPU)
   int32_t HPU;        // kv heads per unit: 4, 2 or 1
   int32_t rec_floats; // floats of one partial record (HPU heads)
+  int32_t scan;       // 1: split the tiles that hold keys (a scan of the counts in
+                      // every CTA) in interleaved row order; 0: split all U * VT
+                      // tiles in row order, no scan (when U <= G)
 };
 
 // Keys per stage of the stream-K kernel for head_dim 128: 64 KB of K+V when
@@ -63,6 +66,8 @@ cudaError_t launch_mma_bf16(const Params& p, cudaStream_t stream);
 cudaError_t launch_mma_e4m3(const Params& p, cudaStream_t stream);
 cudaError_t launch_stream_bf16(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_e4m3(const Params& p, const StreamPlan& sp, cudaStream_t stream);
+cudaError_t launch_stream_bf16_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
+cudaError_t launch_stream_e4m3_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 // CTAs of the tensor-core kernel that fit on one SM (for the split planner).
 int mma_ctas_per_sm_bf16(int group);
 int mma_ctas_per_sm_e4m3(int group);

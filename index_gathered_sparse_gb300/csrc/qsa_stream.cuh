@@ -6,11 +6,15 @@
 // Work.  A unit is one query row and a group of HPU adjacent kv heads (4 when
 // num_kv_heads allows): the K rows of those heads are HPU*256 B (BF16) or
 // HPU*128 B (FP8) contiguous in a cache slot, so one translated position
-// feeds HPU heads with one contiguous read.  Every unit owns VT = W / TILE
-// "virtual" key tiles; the launch has one CTA per SM, and CTA c processes the
-// contiguous range [c*T/G, (c+1)*T/G) of all T virtual tiles (stream-K), so
-// the load is balanced to a tile and at most the first and the last unit of a
-// range are shared with other CTAs.  Tiles past a unit's count are skipped.
+// feeds HPU heads with one contiguous read.  A unit has as many key tiles as
+// its row's count fills (one, empty, when the count is 0); the launch has one
+// CTA per SM, and CTA c processes the contiguous range [c*R/G, (c+1)*R/G) of
+// all R tiles (stream-K; G = min(CTAs, R)), found by a block scan of the counts at the start,
+// so the load is balanced to a tile and at most the first and the last unit
+// of a range are shared with other CTAs.  The rows are numbered in an
+// interleaved order that keeps all CTAs on neighbouring rows.  When there
+// are no more units than CTAs, the split skips the scan and counts W / TILE
+// tiles for every unit instead (tiles past a count are skipped).
 //
 // Roles.  The first PW warps produce (eight with one 8-head N tile, else
 // four), the last four consume, linked per stage by a "full" and an "empty"
@@ -61,7 +65,7 @@ struct StreamCfg {
   // Warps that share a head merge through shared memory; a warp that owns its
   // head writes straight from registers and needs no epilogue buffer.
   static constexpr int EPI_FLOATS = WPH > 1 ? 4 * GP * D + 2 * 4 * GP : 0;
-  static constexpr int FIXED = EPI_FLOATS * 4 + 3 * RT * TILE * 4 + MR * 16 + MAXOFF * 4;
+  static constexpr int FIXED = EPI_FLOATS * 4 + 3 * RT * TILE * 4 + MR * 32 + MAXOFF * 4;
   static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
   static constexpr int STAGES_CAP = TILE <= 32 ? 8 : 5;
   static constexpr int STAGES = STAGES_FIT < STAGES_CAP ? STAGES_FIT : STAGES_CAP;
@@ -155,7 +159,166 @@ struct TileCursor {
   bool live;
 };
 
-template <int KIND, int NT, int HPU>
+// Order of the rows in the tile numbering: the transpose of a row-major
+// matrix with `cols` columns, so that a CTA's contiguous range takes rows c,
+// c + cols, c + 2*cols, ... and all CTAs move through neighbouring rows
+// together.  Rows of one sequence read overlapping cache positions, which
+// then stay in L2 between them.  Columns 0..rem-1 hold ni rows, the rest
+// ni - 1.  row(k) is the row index (before the reversal below) at position k.
+struct RowOrder {
+  int cols, ni, rem;
+  __device__ __forceinline__ RowOrder(int total_q, int ctas) {
+    cols = max(1, min(ctas, total_q));
+    ni = (total_q + cols - 1) / cols;
+    rem = total_q - (ni - 1) * cols;
+  }
+  __device__ __forceinline__ int row(int k) const {
+    const int big = rem * ni;
+    int c, i;
+    if (k < big) {
+      c = k / ni;
+      i = k - c * ni;
+    } else {
+      const int k2 = k - big;
+      c = rem + k2 / (ni - 1);
+      i = k2 - (c - rem) * (ni - 1);
+    }
+    return i * cols + c;
+  }
+};
+
+// Query row of unit u: row total_q - 1 - ord.row(u / NG) of the order in use.
+static __device__ __noinline__ int unit_row(const Params& p, const StreamPlan& sp, int u) {
+  const RowOrder ro(p.total_q, sp.G);
+  return p.total_q - 1 - ro.row(u / sp.NG);
+}
+
+// This CTA's share of the key tiles: R tiles in all, its range [t0, t1), the
+// units holding t0 and t1 - 1 and the tile numbers where those units start
+// and end.
+struct SplitRange {
+  int64_t R, t0, t1;
+  int G;  // CTAs with work: min(launched CTAs, R), so that no range is empty
+  int u_first, u_last;
+  int64_t P_first, P_first_end, P_last, P_last_end;
+};
+
+// Block-wide (every thread of the CTA, before any role split): position q of
+// the row order (row total_q - 1 - rorder.row(q)) has NG units of RT = max(1, ceil(n / TILE))
+// tiles each, n = clamp(counts, 0, W); each thread sums a chunk of rows, a
+// block scan places the chunks, and the threads whose chunks hold t0 and
+// t1 - 1 locate them.  The counts are first read coalesced into `s_tiles`
+// (room for `cap` rows; longer batches read them in place).  `s_scan` holds
+// 16 int64.
+template <int TILE, int NTH>
+__device__ __forceinline__ SplitRange split_range(const Params& p, const StreamPlan& sp, const RowOrder& rorder,
+                                                  long long* s_scan, int32_t* s_tiles, int cap) {
+  constexpr int NW = NTH / 32;
+  static_assert(NW <= 16, "scan scratch");
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int total_q = p.total_q, NG = sp.NG;
+  auto tiles = [&](int c) { const int n = min(max(c, 0), p.W); return n > 0 ? (n + TILE - 1) / TILE : 1; };
+  const bool cached = total_q <= cap;
+  if (cached) {
+    for (int base = 0; base < total_q; base += 8 * NTH) {
+      int v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = base + i * NTH + tid;
+        v[i] = q < total_q ? __ldg(p.counts + (total_q - 1 - rorder.row(q))) : 0;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int q = base + i * NTH + tid;
+        if (q < total_q) s_tiles[q] = tiles(v[i]);
+      }
+    }
+    __syncthreads();
+  }
+  const int ch = (total_q + NTH - 1) / NTH;
+  const int q0 = min(tid * ch, total_q), q1 = min(q0 + ch, total_q);
+  auto tiles_of = [&](int q) -> int64_t {
+    return cached ? s_tiles[q] : tiles(__ldg(p.counts + (total_q - 1 - rorder.row(q))));
+  };
+  int64_t mine = 0;
+  for (int q = q0; q < q1; ++q) mine += tiles_of(q);
+  int64_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) s_scan[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int64_t w = lane < NW ? s_scan[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int64_t v = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += v;
+    }
+    __syncwarp();
+    if (lane < NW) s_scan[lane] = w;
+  }
+  __syncthreads();
+  const int64_t before = (warp ? s_scan[warp - 1] : 0) + incl - mine;  // tiles of the rows before this chunk
+  SplitRange rg;
+  rg.R = (int64_t)NG * s_scan[NW - 1];
+  rg.G = (int)min((int64_t)sp.G, rg.R);
+  rg.t0 = blockIdx.x < rg.G ? (int64_t)blockIdx.x * rg.R / rg.G : 0;
+  rg.t1 = blockIdx.x < rg.G ? ((int64_t)blockIdx.x + 1) * rg.R / rg.G : 0;
+  __syncthreads();  // s_scan now receives the result
+  if (rg.t0 < rg.t1) {
+    int64_t s = (int64_t)NG * before;
+    const int64_t e = s + (int64_t)NG * mine;
+    const int64_t a = rg.t0, b = rg.t1 - 1;
+    if ((a >= s && a < e) || (b >= s && b < e)) {
+      for (int q = q0; q < q1; ++q) {
+        const int64_t rt = tiles_of(q), w = (int64_t)NG * rt;
+        if (a >= s && a < s + w) {
+          const int64_t hg = (a - s) / rt;
+          s_scan[0] = (int64_t)q * NG + hg;
+          s_scan[1] = s + hg * rt;
+          s_scan[2] = s + (hg + 1) * rt;
+        }
+        if (b >= s && b < s + w) {
+          const int64_t hg = (b - s) / rt;
+          s_scan[3] = (int64_t)q * NG + hg;
+          s_scan[4] = s + hg * rt;
+          s_scan[5] = s + (hg + 1) * rt;
+        }
+        s += w;
+      }
+    }
+  }
+  __syncthreads();
+  rg.u_first = (int)s_scan[0];
+  rg.P_first = s_scan[1];
+  rg.P_first_end = s_scan[2];
+  rg.u_last = (int)s_scan[3];
+  rg.P_last = s_scan[4];
+  rg.P_last_end = s_scan[5];
+  return rg;
+}
+
+// The split without a scan: every unit counts VT tiles (those past its count
+// are skipped), R = U * VT, CTA c takes [c*R/G, (c+1)*R/G).
+__device__ __forceinline__ SplitRange even_range(const StreamPlan& sp) {
+  SplitRange rg;
+  rg.R = sp.T;
+  rg.G = (int)min((int64_t)sp.G, sp.T);
+  rg.t0 = blockIdx.x < rg.G ? (int64_t)blockIdx.x * rg.R / rg.G : 0;
+  rg.t1 = blockIdx.x < rg.G ? ((int64_t)blockIdx.x + 1) * rg.R / rg.G : 0;
+  rg.u_first = (int)(rg.t0 / sp.VT);
+  rg.u_last = rg.t1 > rg.t0 ? (int)((rg.t1 - 1) / sp.VT) : rg.u_first;
+  rg.P_first = (int64_t)rg.u_first * sp.VT;
+  rg.P_first_end = rg.P_first + sp.VT;
+  rg.P_last = (int64_t)rg.u_last * sp.VT;
+  rg.P_last_end = rg.P_last + sp.VT;
+  return rg;
+}
+
+template <int KIND, int NT, int HPU, bool SCAN>
 __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_kernel(const Params p, const StreamPlan sp) {
   using C = StreamCfg<KIND, NT, HPU>;
   constexpr int H = C::H, S = C::STAGES, TILE = C::TILE, RT = C::RT, MR = C::MR, GP = C::GP;
@@ -166,9 +329,12 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   int32_t* s_pos = reinterpret_cast<int32_t*>(epi_buf + C::EPI_FLOATS);  // [RT][TILE]
   uint32_t* s_page = reinterpret_cast<uint32_t*>(s_pos + RT * TILE); // [RT][TILE]
   uint32_t* s_off = s_page + RT * TILE;                               // [RT][TILE]
-  int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);    // [MR][4]: count, clen, b, rows_b
-  uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 4);  // [MAXOFF]
+  // unit meta [MR][MW]: count, clen, b, rows_b (and, with the scan, the row)
+  constexpr int MW = SCAN ? 8 : 4;
+  int32_t* s_meta = reinterpret_cast<int32_t*>(s_off + RT * TILE);
+  uint32_t* s_rowoff = reinterpret_cast<uint32_t*>(s_meta + MR * 8);  // [MAXOFF]
   __shared__ int s_merge[2];
+  __shared__ long long s_scan[16];  // the work split's scan and its result
   // stage landed: one expect-tx arrival per producer warp (bulk copies), or one
   // cp.async arrival per producer thread plus one release arrival
   __shared__ __align__(8) uint64_t s_full[S];
@@ -178,11 +344,31 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   constexpr int PT = C::PT;
   const int rw = warp < C::PW ? warp : warp - C::PW;  // warp within its role
   const int VT = sp.VT;
-  const int64_t t0 = (int64_t)blockIdx.x * sp.T / sp.G, t1 = ((int64_t)blockIdx.x + 1) * sp.T / sp.G;
-  if (t0 >= t1) return;  // the planner keeps G <= T, so every range holds a tile
-  const int u_first = (int)(t0 / VT), u_last = (int)((t1 - 1) / VT);
-  const int jlo_first = (int)(t0 - (int64_t)u_first * VT);  // first tile of the first unit in range
-  const int jhi_last = (int)(t1 - (int64_t)u_last * VT);    // end tile of the last unit in range
+  // Work split over the tiles that hold keys.  Unit u (row r = total_q-1-u/NG)
+  // has RT(r) = max(1, ceil(clamp(counts[r], 0, W) / TILE)) tiles; tiles are
+  // numbered unit after unit (P_u = tiles before unit u, R = all of them) and
+  // CTA c takes [c*R/G, (c+1)*R/G).  Every CTA scans the counts itself.
+  if (warp < C::PW && p.batch + 1 <= C::MAXOFF)  // lands during the scan
+    for (int k = tid; k <= p.batch; k += C::PT) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
+  SplitRange rg;
+  if constexpr (SCAN) {
+    const RowOrder ro(p.total_q, sp.G);
+    rg = split_range<TILE, C::THREADS>(p, sp, ro, s_scan, reinterpret_cast<int32_t*>(smem), S * C::STAGE_BYTES / 4);
+    fence_proxy_async_smem();  // the scan's writes to the stage ring before any copy into it
+  } else {
+    rg = even_range(sp);
+  }
+  if (rg.t0 >= rg.t1) {
+    cp_async_wait_all();
+    return;
+  }
+  const int u_first = rg.u_first, u_last = rg.u_last;
+  const int jlo_first = (int)(rg.t0 - rg.P_first);  // first tile of the first unit in range
+  const int jhi_last = (int)(rg.t1 - rg.P_last);    // end tile of the last unit in range
+  // the rest of the scanned split is needed only at shared units' ends: keep
+  // it in shared memory (published by the barrier after the mbarrier set-up)
+  __shared__ SplitRange s_rg;
+  if (SCAN && tid == 0) s_rg = rg;
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
       mbar_init(smem_addr(&s_full[k]), C::FULL_ARRIVALS);
@@ -192,7 +378,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   }
   __syncthreads();  // the last block-wide barrier: the roles part here
 
-  auto mslot = [&](int u) { return ((u - u_first) & (MR - 1)) * 4; };
+  auto mslot = [&](int u) { return ((u - u_first) & (MR - 1)) * MW; };
   // tile j of unit u: jl = last tile inside the range that holds keys (or the
   // first tile in range when none does: that unit still gets one empty tile)
   auto unit_jl = [&](int u, int n) {
@@ -210,6 +396,13 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     // producers
     // =====================================================================
     uint32_t bad = 0;
+    // query row of unit u (computed once per unit by thread 0, which
+    // publishes it in the unit meta)
+    const RowOrder rorder(p.total_q, SCAN ? sp.G : p.total_q);  // the identity without the scan
+    auto row_of = [&](int u) {
+      if constexpr (SCAN) return p.total_q - 1 - rorder.row(u / sp.NG);
+      else return p.total_q - 1 - u / sp.NG;
+    };
     auto find_seq = [&](int r) -> int {  // sequence of row r, -1 when no sequence owns it
       const bool in_smem = p.batch + 1 <= C::MAXOFF;
       auto off = [&](int k) { return in_smem ? s_rowoff[k] : __ldg(p.row_offsets + k); };
@@ -225,10 +418,12 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     // unit meta in two parts: the row's count (needs nothing), then its
     // sequence, that sequence's rows and cached length (needs the offsets)
     auto issue_meta_count = [&](int u) {  // producer thread 0 only
-      cp_async4(smem_addr(&s_meta[mslot(u) + 0]), p.counts + (p.total_q - 1 - u / sp.NG));
+      const int r = row_of(u), m = mslot(u);
+      if constexpr (SCAN) s_meta[m + 4] = r;  // the unit's query row, for the other producers and the consumers
+      cp_async4(smem_addr(&s_meta[m + 0]), p.counts + r);
     };
     auto issue_meta_seq = [&](int u) {  // producer thread 0 only
-      const int r = p.total_q - 1 - u / sp.NG, m = mslot(u);
+      const int m = mslot(u), r = SCAN ? s_meta[m + 4] : row_of(u);
       const int b = find_seq(r);
       s_meta[m + 2] = b;
       if (b >= 0) {
@@ -269,7 +464,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       ensure_meta(u);
       c.u = u;
       const int q = u / sp.NG;
-      c.r = p.total_q - 1 - q;
+      c.r = SCAN ? s_meta[mslot(u) + 4] : p.total_q - 1 - q;
       c.hg = u - q * sp.NG;
       c.n = unit_n(u);
       c.jl = unit_jl(u, c.n);
@@ -393,9 +588,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     // together with the first index hops (which need only counts), then page
     // entries, then K/V
     const int u_pro = min(u_first + H + 1, u_last);
-    if (p.batch + 1 <= C::MAXOFF)
-      for (int k = tid; k <= p.batch; k += PT) cp_async4(smem_addr(&s_rowoff[k]), p.row_offsets + k);
-    if (tid == 0)
+    if (tid == 0)  // (the row offsets were issued before the split)
       for (int v = u_first; v <= u_pro; ++v) issue_meta_count(v);
     cp_async_wait_all();
     role_sync(1, PT);
@@ -466,9 +659,25 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   // consumers
   // =========================================================================
   const int hh = rw / C::WPH, kp = rw % C::WPH;
-  auto cta_of = [&](int64_t x) { return (int)(((x + 1) * sp.G - 1) / sp.T); };
-  auto first_cta = [&](int u) { return cta_of((int64_t)u * VT); };
-  auto contributors = [&](int u) { return cta_of((int64_t)(u + 1) * VT - 1) - first_cta(u) + 1; };
+  auto cta_of = [&](int64_t x) {  // owner of tile x
+    if constexpr (SCAN) return (int)(((x + 1) * s_rg.G - 1) / s_rg.R);
+    else return (int)(((x + 1) * sp.G - 1) / sp.T);
+  };
+  // tiles before unit u and before u + 1, for the first and last unit in range
+  // (the only ones another CTA can share)
+  auto unit_lo = [&](int u) -> int64_t {
+    if constexpr (SCAN) return u == u_first ? s_rg.P_first : s_rg.P_last;
+    else return (int64_t)u * VT;
+  };
+  auto unit_hi = [&](int u) -> int64_t {
+    if constexpr (SCAN) return u == u_last ? s_rg.P_last_end : s_rg.P_first_end;
+    else return (int64_t)(u + 1) * VT;
+  };
+  auto first_cta = [&](int u) { return cta_of(unit_lo(u)); };
+  auto contributors = [&](int u) {
+    if (SCAN && u != u_first && u != u_last) return 1;
+    return cta_of(unit_hi(u) - 1) - first_cta(u) + 1;
+  };
   // A shared unit's partial records: two per CTA, slot 0 for the CTA's first
   // unit and slot 1 for its last.  Every contributor after a unit's first
   // starts its range inside that unit, so only the first one can hold the
@@ -476,7 +685,10 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   auto own_record = [&](int u) { return p.ws_partial + ((int64_t)2 * blockIdx.x + (u == u_first ? 0 : 1)) * sp.rec_floats; };
   auto record_of = [&](int c0, int c, int u) {  // contributor c0 + c of unit u
     int slot = 0;
-    if (c == 0) slot = (int64_t)c0 * sp.T / sp.G == (int64_t)u * VT ? 0 : 1;
+    if (c == 0) {
+      const int64_t start = SCAN ? (int64_t)c0 * s_rg.R / s_rg.G : (int64_t)c0 * sp.T / sp.G;
+      slot = start == unit_lo(u) ? 0 : 1;
+    }
     return p.ws_partial + ((int64_t)2 * (c0 + c) + slot) * sp.rec_floats;
   };
   const int ctid = tid - PT;
@@ -485,9 +697,8 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   float* epi = C::EPI_FLOATS ? epi_buf : reinterpret_cast<float*>(smem);
 
   uint32_t qf[NT][C::KSTEPS][2], qn[NT][C::KSTEPS][2];
-  auto load_q = [&](int u, uint32_t (&dst)[NT][C::KSTEPS][2]) {
-    const int q = u / sp.NG;
-    const int r = p.total_q - 1 - q, h = (u - q * sp.NG) * HPU + hh;
+  auto load_q = [&](int u, int r, uint32_t (&dst)[NT][C::KSTEPS][2]) {
+    const int h = (u - (u / sp.NG) * sp.NG) * HPU + hh;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int head = nt * 8 + gid;
@@ -670,7 +881,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   auto finish = [&](int u, bool row_ok) {
     const int G = p.group, D = C::D;
     const int q = u / sp.NG;
-    const int r = p.total_q - 1 - q, hg = u - q * sp.NG;
+    const int r = SCAN ? s_meta[mslot(u) + 4] : p.total_q - 1 - q, hg = u - q * sp.NG;
     const bool own = contributors(u) == 1;
     float* rec = own ? nullptr : own_record(u);
     const int64_t stride = partial_stride(G, D);
@@ -779,8 +990,9 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   };
 
   // main loop: wait for a tile, consume it (releasing its stage), finish units
-  load_q(u_first, qf);
-  if (u_first < u_last) load_q(u_first + 1, qn);
+  auto first_rows = [&](int u) { return SCAN ? unit_row(p, sp, u) : p.total_q - 1 - u / sp.NG; };
+  load_q(u_first, first_rows(u_first), qf);
+  if (u_first < u_last) load_q(u_first + 1, first_rows(u_first + 1), qn);
   reset_state();
   int u = u_first, j = jlo_first, n = 0, jl = 0, ord = 0;
   bool entered = false, row_ok = false, aborted = false;
@@ -814,7 +1026,8 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
         qf[nt][ks][0] = qn[nt][ks][0];
         qf[nt][ks][1] = qn[nt][ks][1];
       }
-    if (u + 1 <= u_last) load_q(u + 1, qn);
+    // unit u + 1's meta (its row) arrived with the first tile of unit u - 1
+    if (u + 1 <= u_last) load_q(u + 1, SCAN ? s_meta[mslot(u + 1) + 4] : p.total_q - 1 - (u + 1) / sp.NG, qn);
   }
   if (aborted) {
     if (ctid == 0) atomicOr(p.status, QSA_STATUS_TIMEOUT);
@@ -836,7 +1049,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     __threadfence();
     const int G = p.group, D = C::D, K = contributors(um), c0 = first_cta(um);
     const int q = um / sp.NG;
-    const int r = p.total_q - 1 - q, hg = um - q * sp.NG;
+    const int r = SCAN ? unit_row(p, sp, um) : p.total_q - 1 - q, hg = um - q * sp.NG;
     const int64_t stride = partial_stride(G, D);
     const float* rec0 = record_of(c0, 0, um);
     const float* rec1 = record_of(c0, 1, um);  // contributors 1.. are 2 * rec_floats apart
@@ -886,7 +1099,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   }
 }
 
-template <int KIND, int NT, int HPU>
+template <int KIND, int NT, int HPU, bool SCAN>
 cudaError_t launch_stream_t(const Params& p, const StreamPlan& sp, cudaStream_t s) {
   using C = StreamCfg<KIND, NT, HPU>;
   static int configured_mask = 0;
@@ -894,22 +1107,24 @@ cudaError_t launch_stream_t(const Params& p, const StreamPlan& sp, cudaStream_t 
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
     const cudaError_t e =
-        cudaFuncSetAttribute(stream_kernel<KIND, NT, HPU>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaFuncSetAttribute(stream_kernel<KIND, NT, HPU, SCAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured_mask |= 1 << (dev & 31);
   }
   if (sp.G == 0) return cudaSuccess;
-  stream_kernel<KIND, NT, HPU><<<sp.G, C::THREADS, C::SMEM, s>>>(p, sp);
+  stream_kernel<KIND, NT, HPU, SCAN><<<sp.G, C::THREADS, C::SMEM, s>>>(p, sp);
   return cudaGetLastError();
 }
 
-template <int KIND>
+// Instantiations for one element type and one split (each in its own
+// translation unit, so that they compile in parallel).
+template <int KIND, bool SCAN>
 cudaError_t launch_stream_kind(const Params& p, const StreamPlan& sp, cudaStream_t s) {
   const bool nt2 = p.group > 8;
   switch (sp.HPU) {
-    case 4: return nt2 ? launch_stream_t<KIND, 2, 4>(p, sp, s) : launch_stream_t<KIND, 1, 4>(p, sp, s);
-    case 2: return nt2 ? launch_stream_t<KIND, 2, 2>(p, sp, s) : launch_stream_t<KIND, 1, 2>(p, sp, s);
-    default: return nt2 ? launch_stream_t<KIND, 2, 1>(p, sp, s) : launch_stream_t<KIND, 1, 1>(p, sp, s);
+    case 4: return nt2 ? launch_stream_t<KIND, 2, 4, SCAN>(p, sp, s) : launch_stream_t<KIND, 1, 4, SCAN>(p, sp, s);
+    case 2: return nt2 ? launch_stream_t<KIND, 2, 2, SCAN>(p, sp, s) : launch_stream_t<KIND, 1, 2, SCAN>(p, sp, s);
+    default: return nt2 ? launch_stream_t<KIND, 2, 1, SCAN>(p, sp, s) : launch_stream_t<KIND, 1, 1, SCAN>(p, sp, s);
   }
 }
 

@@ -1,0 +1,11 @@
+// FP8 e4m3 instantiations of the persistent stream-K kernel with the scanned
+// split over the tiles that hold keys.
+#include "qsa_stream.cuh"
+
+namespace qsa {
+
+cudaError_t launch_stream_e4m3_scan(const Params& p, const StreamPlan& sp, cudaStream_t s) {
+  return launch_stream_kind<kE4M3, true>(p, sp, s);
+}
+
+}  // namespace qsa
