@@ -119,8 +119,11 @@ typedef enum qsa_status {
  *   stream            cudaStream_t to enqueue on
  *
  * Kernel coverage: output F32 or BF16; head_dim 64 or 128.  BF16 and F8E4M3
- * with head_dim 128 run on the persistent tensor-core kernel (group 1..16);
- * the rest on the CUDA-core kernel (group 1..8 or 16).  Device pointers must be 16-byte aligned, and
+ * with head_dim 128 run on the persistent tensor-core kernel (group 1..16),
+ * or, when its units (total_q * num_kv_heads / H, H = 4, 2 or 1, the largest
+ * that divides num_kv_heads) are under a quarter of the SM count, on the
+ * per-(row, kv head) tensor-core kernel with split-K; the rest on the
+ * CUDA-core kernel (group 1..8 or 16).  Device pointers must be 16-byte aligned, and
  * page_stride * element size a multiple of 16 bytes.  kv_blocks may span up
  * to 64 GiB.
  *

@@ -74,8 +74,23 @@ struct Resolved {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Picks the kernel for a resolved call: the tensor-core kernel for BF16 and
-// FP8 with head_dim 128, the CUDA-core kernel otherwise (or as forced).
+// True when the persistent kernel would have fewer than a quarter as many
+// units (row x group of up to four kv heads) as the device has SMs: each unit
+// then spreads over many CTAs whose short ranges cannot hide the dependent
+// prologue, and the per-(row, kv head) kernel with split-K, several CTAs per
+// SM, is faster.
+bool few_stream_units(const Resolved& R) {
+  const int64_t hpu = R.nkv % 4 == 0 ? 4 : R.nkv % 2 == 0 ? 2 : 1;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return false;
+  return R.total_q * (R.nkv / hpu) * 4 < sms;
+}
+
+// Picks the kernel for a resolved call: for BF16 and FP8 with head_dim 128
+// the persistent tensor-core kernel, or the per-(row, kv head) one when the
+// persistent kernel would get few units; the CUDA-core kernel otherwise (or
+// as forced).
 qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
   const bool mma_ok = (R.elem == qsa::kBF16 || R.elem == qsa::kE4M3) && R.D == 128;
   const bool simt_ok = group <= 8 || group == 16;
@@ -88,6 +103,7 @@ qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
     R.kernel = 1;
   } else if (want == 0) {
     R.kernel = mma_ok ? 3 : 1;
+    if (R.kernel == 3 && few_stream_units(R)) R.kernel = 2;
     if (R.kernel == 1 && !simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
   } else {
     return fail(QSA_ERR_ARG, "options.kernel must be 0, 1, 2 or 3");
