@@ -71,15 +71,12 @@ struct StreamCfg {
   static constexpr int STAGES = STAGES_FIT < STAGES_CAP ? STAGES_FIT : STAGES_CAP;
   static constexpr int H = STAGES - 1;
   static constexpr int SMEM = STAGES * STAGE_BYTES + FIXED;
-  // Consumers copy a tile's K/V fragments to registers and release the stage
-  // before computing, when one 8-head N tile leaves them the registers.
   // Producer warps: eight when the consumers fit the 168 registers a thread of
   // a 384-thread CTA gets (one 8-head N tile), else four; more producers keep
   // more copies in flight while some of them translate.
   static constexpr int PW = NT == 1 ? 8 : 4;
   static constexpr int PT = PW * 32;
   static constexpr int THREADS = PT + 128;
-  static constexpr bool EARLY = NT == 1 && PW == 4;
   // K/V copies: one bulk copy per key chunk when chunks are 512 B or more (a
   // warp pays a fixed issue time per bulk copy), else 16-byte cp.async, whose
   // outstanding copies are limited per thread.
@@ -726,151 +723,145 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   };
   const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_col = ((lane >> 4) & 1) * 16;
   const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8, t_col = ((lane >> 3) & 1) * 16;
-  constexpr int VLD = KIND == kBF16 ? 8 : 4;  // transposing ldmatrix.x4 per 16-key slice of V
 
-  // One 16-key slice of this warp: its K and V fragments and key masks.
-  struct Slice {
-    uint32_t k[C::KSTEPS][4];
-    uint32_t v[C::EARLY ? VLD : 1][4];  // without EARLY, V is read from the stage during PV
-    uint32_t vbase;
-    bool vA, vB, any;
-  };
-  auto load_slice = [&](Slice& f, int kt, int ord, int sl) {
+  // A tile of this warp: its MSL 16-key slices.  The scores of every slice
+  // come first (independent MMA chains), then one softmax update over all of
+  // the warp's keys in the tile (one max reduction and one rescale of O per
+  // tile, not per slice), then P.V for every slice; the stage is released
+  // after the last V read.
+  constexpr int MSL = C::MSL;
+  constexpr bool TWO_CHAINS = MSL == 1;  // a lone slice splits its K steps over two accumulators
+  auto consume_tile = [&](int kt, int ord) {
+    const uint32_t empty = smem_addr(&s_empty[ord % S]);
     const int slot = (ord & (RT - 1)) * TILE;
     const unsigned char* sb = smem + (ord % S) * C::STAGE_BYTES;
-    const int k0 = kp * C::KPW + sl * 16;
-    const int kA = k0 + gid, kB = kA + 8;
-    f.vA = kA < kt && s_off[slot + kA] != kInvalidOff;
-    f.vB = kB < kt && s_off[slot + kB] != kInvalidOff;
-    f.any = __any_sync(0xffffffffu, f.vA || f.vB);
-    if (!f.any) return;
-    const uint32_t kbase = smem_addr(sb) + k0 * C::SROW + hh * C::ROWB;
-    const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + k0 * C::SROW + hh * C::ROWB;
+    bool vA[MSL], vB[MSL], any[MSL];
+    float sc[MSL][NT][4];
 #pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) ldsm_x4(kbase + a_row * C::SROW + ks * 32 + a_col, f.k[ks]);
-    f.vbase = vbase + t_row * C::SROW + t_col;
-    if constexpr (C::EARLY) {
+    for (int sl = 0; sl < MSL; ++sl) {
+      const int k0 = kp * C::KPW + sl * 16;
+      const int kA = k0 + gid, kB = kA + 8;
+      vA[sl] = kA < kt && s_off[slot + kA] != kInvalidOff;
+      vB[sl] = kB < kt && s_off[slot + kB] != kInvalidOff;
+      any[sl] = __any_sync(0xffffffffu, vA[sl] || vB[sl]);
+      float s2[NT][4];
 #pragma unroll
-      for (int mt = 0; mt < VLD; ++mt) ldsm_x4_t(f.vbase + mt * 32, f.v[mt]);
-    }
-  };
-  auto v_frag = [&](const Slice& f, int mt, uint32_t (&a)[4]) {
-    if constexpr (C::EARLY) {
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) a[k] = f.v[C::EARLY ? mt : 0][k];
-    } else {
-      ldsm_x4_t(f.vbase + mt * 32, a);
-    }
-  };
-  auto compute_slice = [&](const Slice& f) {
-    if (!f.any) return;
-    float s[NT][4], s2[NT][4];
+        for (int c = 0; c < 4; ++c) sc[sl][nt][c] = s2[nt][c] = 0.f;
+      if (any[sl]) {
+        const uint32_t kbase = smem_addr(sb) + k0 * C::SROW + hh * C::ROWB + a_row * C::SROW + a_col;
+        uint32_t kf[C::KSTEPS][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-      s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = s2[nt][0] = s2[nt][1] = s2[nt][2] = s2[nt][3] = 0.f;
+        for (int ks = 0; ks < C::KSTEPS; ++ks) ldsm_x4(kbase + ks * 32, kf[ks]);
 #pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) {  // two accumulator chains halve the dependent-MMA latency
+        for (int ks = 0; ks < C::KSTEPS; ++ks)
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        if constexpr (KIND == kBF16) {
-          if (ks & 1) mma_bf16(s2[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
-          else mma_bf16(s[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
-        } else {
-          if (ks & 1) mma_e4m3(s2[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
-          else mma_e4m3(s[nt], f.k[ks], qf[nt][ks][0], qf[nt][ks][1]);
+          for (int nt = 0; nt < NT; ++nt) {
+            float (&acc)[4] = (TWO_CHAINS && (ks & 1)) ? s2[nt] : sc[sl][nt];
+            if constexpr (KIND == kBF16) mma_bf16(acc, kf[ks], qf[nt][ks][0], qf[nt][ks][1]);
+            else mma_e4m3(acc, kf[ks], qf[nt][ks][0], qf[nt][ks][1]);
+          }
+        if constexpr (TWO_CHAINS) {
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) sc[sl][nt][c] += s2[nt][c];
         }
       }
     }
-    uint32_t pb[NT][2];
+    bool any_tile = false;
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      float pv[4];
+    for (int sl = 0; sl < MSL; ++sl) any_tile |= any[sl];
+    uint32_t pb[MSL][NT][2];
+    if (any_tile) {
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        const float x0 = f.vA ? (s[nt][c] + s2[nt][c]) * p.scale_log2 : -CUDART_INF_F;
-        const float x1 = f.vB ? (s[nt][2 + c] + s2[nt][2 + c]) * p.scale_log2 : -CUDART_INF_F;
-        float mx = fmaxf(x0, x1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mnew = fmaxf(m_run[nt][c], mx);
-        const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
-        const float alpha = exp2f(m_run[nt][c] - muse);
-        const float p0 = exp2f(x0 - muse), p1 = exp2f(x1 - muse);
-        l_run[nt][c] = l_run[nt][c] * alpha + p0 + p1;
-        m_run[nt][c] = mnew;
-        pv[c] = p0;
-        pv[2 + c] = p1;
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      for (int nt = 0; nt < NT; ++nt) {
+        float pv[MSL][4];
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          float mx = -CUDART_INF_F;
+#pragma unroll
+          for (int sl = 0; sl < MSL; ++sl) {
+            sc[sl][nt][c] = vA[sl] ? sc[sl][nt][c] * p.scale_log2 : -CUDART_INF_F;
+            sc[sl][nt][2 + c] = vB[sl] ? sc[sl][nt][2 + c] * p.scale_log2 : -CUDART_INF_F;
+            mx = fmaxf(mx, fmaxf(sc[sl][nt][c], sc[sl][nt][2 + c]));
+          }
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mnew = fmaxf(m_run[nt][c], mx);
+          const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
+          const float alpha = exp2f(m_run[nt][c] - muse);
+          float lsum = 0.f;
+#pragma unroll
+          for (int sl = 0; sl < MSL; ++sl) {
+            const float p0 = exp2f(sc[sl][nt][c] - muse), p1 = exp2f(sc[sl][nt][2 + c] - muse);
+            pv[sl][c] = p0;
+            pv[sl][2 + c] = p1;
+            lsum += p0 + p1;
+          }
+          l_run[nt][c] = l_run[nt][c] * alpha + lsum;
+          m_run[nt][c] = mnew;
+          if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              o[mt][nt][c] *= alpha;
+              o[mt][nt][2 + c] *= alpha;
+            }
+          }
+        }
+#pragma unroll
+        for (int sl = 0; sl < MSL; ++sl) {
+          const uint32_t top = KIND == kBF16 ? pack_bf16(pv[sl][0], pv[sl][1]) : pack_f16(pv[sl][0], pv[sl][1]);
+          const uint32_t bot = KIND == kBF16 ? pack_bf16(pv[sl][2], pv[sl][3]) : pack_f16(pv[sl][2], pv[sl][3]);
+          pb[sl][nt][0] = movmatrix_t(top);
+          pb[sl][nt][1] = movmatrix_t(bot);
+        }
+      }
+#pragma unroll
+      for (int sl = 0; sl < MSL; ++sl) {
+        if (!any[sl]) continue;
+        const int k0 = kp * C::KPW + sl * 16;
+        const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + k0 * C::SROW + hh * C::ROWB + t_row * C::SROW + t_col;
+        if constexpr (KIND == kBF16) {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
-            o[mt][nt][c] *= alpha;
-            o[mt][nt][2 + c] *= alpha;
+            uint32_t a[4];
+            ldsm_x4_t(vbase + mt * 32, a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a, pb[sl][nt][0], pb[sl][nt][1]);
+          }
+        } else {
+#pragma unroll
+          for (int pr = 0; pr < 4; ++pr) {
+            // e4m3 rows are read as byte pairs: the transposing ldmatrix hands this
+            // thread (key 2tig, 2tig+1) x (d 2gid, 2gid+1) of each 16-byte column
+            // block; output rows of an M tile are d = 16mt + 2gid and 16mt + 2gid + 1
+            uint32_t r4[4];
+            ldsm_x4_t(vbase + pr * 32, r4);
+            uint32_t ae[4], ao[4];
+            const uint32_t q0 = __byte_perm(r4[0], 0, 0x3120), q1 = __byte_perm(r4[1], 0, 0x3120);
+            const uint32_t q2 = __byte_perm(r4[2], 0, 0x3120), q3 = __byte_perm(r4[3], 0, 0x3120);
+            ae[0] = e4m3x2_to_f16x2(q0 & 0xFFFFu);
+            ae[1] = e4m3x2_to_f16x2(q0 >> 16);
+            ae[2] = e4m3x2_to_f16x2(q2 & 0xFFFFu);
+            ae[3] = e4m3x2_to_f16x2(q2 >> 16);
+            ao[0] = e4m3x2_to_f16x2(q1 & 0xFFFFu);
+            ao[1] = e4m3x2_to_f16x2(q1 >> 16);
+            ao[2] = e4m3x2_to_f16x2(q3 & 0xFFFFu);
+            ao[3] = e4m3x2_to_f16x2(q3 >> 16);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              mma_f16(o[2 * pr][nt], ae, pb[sl][nt][0], pb[sl][nt][1]);
+              mma_f16(o[2 * pr + 1][nt], ao, pb[sl][nt][0], pb[sl][nt][1]);
+            }
           }
         }
       }
-      const uint32_t top = KIND == kBF16 ? pack_bf16(pv[0], pv[1]) : pack_f16(pv[0], pv[1]);
-      const uint32_t bot = KIND == kBF16 ? pack_bf16(pv[2], pv[3]) : pack_f16(pv[2], pv[3]);
-      pb[nt][0] = movmatrix_t(top);
-      pb[nt][1] = movmatrix_t(bot);
     }
-    if constexpr (KIND == kBF16) {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        uint32_t a[4];
-        v_frag(f, mt, a);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a, pb[nt][0], pb[nt][1]);
-      }
-    } else {
-#pragma unroll
-      for (int pr = 0; pr < 4; ++pr) {
-        // e4m3 rows are read as byte pairs: the transposing ldmatrix hands this
-        // thread (key 2tig, 2tig+1) x (d 2gid, 2gid+1) of each 16-byte column
-        // block; output rows of an M tile are d = 16mt + 2gid and 16mt + 2gid + 1
-        uint32_t r4[4];
-        v_frag(f, pr, r4);
-        uint32_t ae[4], ao[4];
-        const uint32_t q0 = __byte_perm(r4[0], 0, 0x3120), q1 = __byte_perm(r4[1], 0, 0x3120);
-        const uint32_t q2 = __byte_perm(r4[2], 0, 0x3120), q3 = __byte_perm(r4[3], 0, 0x3120);
-        ae[0] = e4m3x2_to_f16x2(q0 & 0xFFFFu);
-        ae[1] = e4m3x2_to_f16x2(q0 >> 16);
-        ae[2] = e4m3x2_to_f16x2(q2 & 0xFFFFu);
-        ae[3] = e4m3x2_to_f16x2(q2 >> 16);
-        ao[0] = e4m3x2_to_f16x2(q1 & 0xFFFFu);
-        ao[1] = e4m3x2_to_f16x2(q1 >> 16);
-        ao[2] = e4m3x2_to_f16x2(q3 & 0xFFFFu);
-        ao[3] = e4m3x2_to_f16x2(q3 >> 16);
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          mma_f16(o[2 * pr][nt], ae, pb[nt][0], pb[nt][1]);
-          mma_f16(o[2 * pr + 1][nt], ao, pb[nt][0], pb[nt][1]);
-        }
-      }
-    }
-  };
-  // A tile: with EARLY, every slice's fragments come to registers and the
-  // stage is released before any math; otherwise slice by slice, then release.
-  auto consume_tile = [&](int kt, int ord) {
-    const uint32_t empty = smem_addr(&s_empty[ord % S]);
-    if constexpr (C::EARLY) {
-      Slice f[C::MSL];
-#pragma unroll
-      for (int sl = 0; sl < C::MSL; ++sl) load_slice(f[sl], kt, ord, sl);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty);
-#pragma unroll
-      for (int sl = 0; sl < C::MSL; ++sl) compute_slice(f[sl]);
-    } else {
-#pragma unroll
-      for (int sl = 0; sl < C::MSL; ++sl) {
-        Slice f;
-        load_slice(f, kt, ord, sl);
-        compute_slice(f);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty);
-    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty);
   };
 
   // End of unit u: output (unit owned by this CTA) or this CTA's partial
