@@ -16,9 +16,10 @@
 // are no more units than CTAs, the split skips the scan and counts W / TILE
 // tiles for every unit instead (tiles past a count are skipped).
 //
-// Roles.  The first PW warps produce (eight with one 8-head N tile, else
-// four), the last four consume, linked per stage by a "full" and an "empty"
-// mbarrier.  Producers fetch everything a tile needs in hops
+// Roles.  The first PW warps produce (four, or eight for units of one or two
+// heads with one 8-head N tile), the last NC consume (eight, two per kv head,
+// for units of four heads with one N tile, else four), linked per stage by a
+// "full" and an "empty" mbarrier.  Producers fetch everything a tile needs in hops
 // spaced H = STAGES - 1 producer iterations apart, so each hop has landed when
 // the next one reads it and nothing waits on a dependent load in steady state:
 //     unit meta (counts, cache_lengths)   ~ H + 1 units ahead of the index hop
@@ -27,7 +28,7 @@
 //     offsets  (computed from both)        H + 1 tiles ahead
 // and the K/V rows by 16-byte cp.async (zero-filled for slots without a valid
 // key), each producer thread arriving on the stage's full barrier when its
-// copies land.  Consumers own heads (WPH = 4 / HPU warps per head split a
+// copies land.  Consumers own heads (WPH = NC / HPU warps per head split a
 // tile's keys) and run the keys-on-M / heads-on-N mma.sync scheme: S^T = K Q^T,
 // online softmax in base 2, P^T by movmatrix, O^T += V^T P^T; they release each
 // stage on its empty barrier.  A unit's end merges the consumer warps in
@@ -47,7 +48,15 @@ struct StreamCfg {
   static constexpr int ROWB = D * ELEM;             // one head's K (or V) row
   static constexpr int KEYB = HPU * ROWB;           // a unit's K (or V) bytes per key, contiguous
   static constexpr int SROW = KEYB + 16;            // padded shared-memory row (conflict-free ldmatrix)
-  static constexpr int WPH = 4 / HPU;               // warps per head
+  // Consumer warps: eight (two per kv head, splitting each tile's keys) for
+  // units of four heads with one 8-head N tile, so that two dependent
+  // MMA/softmax chains share each SM sub-partition; else four.
+  static constexpr int NC = (NT == 1 && HPU == 4) ? 8 : 4;
+  static constexpr int CT = NC * 32;                // consumer threads
+  static constexpr int WPH = NC / HPU;              // warps per head
+  // two warps per head merge their softmax states pairwise through shared
+  // memory (half of head_dim at a time) into the first warp's registers
+  static constexpr bool PAIR = NC == 8;
   // keys per stage: 64 KB of K+V when each warp owns a head (no epilogue
   // buffer competes for shared memory), else 32 KB
   static constexpr int TILE = stream_tile(ELEM, HPU);
@@ -64,7 +73,7 @@ struct StreamCfg {
   static constexpr int MAXOFF = 1024;               // input_row_offsets entries kept in shared memory
   // Warps that share a head merge through shared memory; a warp that owns its
   // head writes straight from registers and needs no epilogue buffer.
-  static constexpr int EPI_FLOATS = WPH > 1 ? 4 * GP * D + 2 * 4 * GP : 0;
+  static constexpr int EPI_FLOATS = PAIR ? 4 * GP * (D / 2) + 2 * 4 * GP : WPH > 1 ? 4 * GP * D + 2 * 4 * GP : 0;
   static constexpr int FIXED = EPI_FLOATS * 4 + 3 * RT * TILE * 4 + MR * 32 + MAXOFF * 4;
   static constexpr int STAGES_FIT = (232448 - FIXED) / STAGE_BYTES;
   static constexpr int STAGES_CAP = TILE <= 32 ? 8 : 5;
@@ -74,9 +83,9 @@ struct StreamCfg {
   // Producer warps: eight when the consumers fit the 168 registers a thread of
   // a 384-thread CTA gets (one 8-head N tile), else four; more producers keep
   // more copies in flight while some of them translate.
-  static constexpr int PW = NT == 1 ? 8 : 4;
+  static constexpr int PW = NT == 1 && NC == 4 ? 8 : 4;
   static constexpr int PT = PW * 32;
-  static constexpr int THREADS = PT + 128;
+  static constexpr int THREADS = PT + CT;
   // K/V copies: one bulk copy per key chunk when chunks are 512 B or more (a
   // warp pays a fixed issue time per bulk copy), else 16-byte cp.async, whose
   // outstanding copies are limited per thread.
@@ -369,7 +378,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   if (tid == 0) {
     for (int k = 0; k < S; ++k) {
       mbar_init(smem_addr(&s_full[k]), C::FULL_ARRIVALS);
-      mbar_init(smem_addr(&s_empty[k]), 4);
+      mbar_init(smem_addr(&s_empty[k]), C::NC);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
@@ -887,10 +896,71 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         lsum[nt][c] = l;
       }
-    if constexpr (C::WPH == 1) {
+    if constexpr (C::PAIR) {
+      // the second warp of each head hands its (m, l, O) to the first, half
+      // of head_dim per round; the first rescales both to the common max
+      float* bo = epi;                     // [4][GP][D/2]
+      float* bm = epi + 4 * GP * (D / 2);  // [4][GP]
+      float* bl = bm + 4 * GP;             // [4][GP]
+      float a0[NT][2], a1[NT][2];
+      if (kp == 1 && gid == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            bm[hh * GP + nt * 8 + 2 * tig + c] = m_run[nt][c];
+            bl[hh * GP + nt * 8 + 2 * tig + c] = lsum[nt][c];
+          }
+      }
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        if (kp == 1) {
+#pragma unroll
+          for (int mt = half * 4; mt < half * 4 + 4; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int head = nt * 8 + 2 * tig + (c4 & 1);
+                const int d = (KIND == kBF16 ? mt * 16 + gid + (c4 >> 1) * 8 : mt * 16 + 2 * gid + (c4 >> 1)) - half * (D / 2);
+                bo[(hh * GP + head) * (D / 2) + d] = o[mt][nt][c4];
+              }
+        }
+        role_sync(2, C::CT);
+        if (kp == 0) {
+          if (half == 0) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int c = 0; c < 2; ++c) {
+                const int head = nt * 8 + 2 * tig + c;
+                const float m1 = bm[hh * GP + head], l1 = bl[hh * GP + head];
+                const float M = fmaxf(m_run[nt][c], m1);
+                a0[nt][c] = M == -CUDART_INF_F ? 0.f : exp2f(m_run[nt][c] - M);
+                a1[nt][c] = M == -CUDART_INF_F ? 0.f : exp2f(m1 - M);
+                lsum[nt][c] = lsum[nt][c] * a0[nt][c] + l1 * a1[nt][c];
+                m_run[nt][c] = M;
+              }
+          }
+#pragma unroll
+          for (int mt = half * 4; mt < half * 4 + 4; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+              for (int c4 = 0; c4 < 4; ++c4) {
+                const int head = nt * 8 + 2 * tig + (c4 & 1);
+                const int d = (KIND == kBF16 ? mt * 16 + gid + (c4 >> 1) * 8 : mt * 16 + 2 * gid + (c4 >> 1)) - half * (D / 2);
+                o[mt][nt][c4] = o[mt][nt][c4] * a0[nt][c4 & 1] + bo[(hh * GP + head) * (D / 2) + d] * a1[nt][c4 & 1];
+              }
+        }
+        role_sync(2, C::CT);
+      }
+    }
+    if constexpr (C::WPH == 1 || C::PAIR) {
       const int h = hg * HPU + hh;
       const int64_t out0 = ((int64_t)r * p.nq + (int64_t)h * G) * D;
       float* part = own ? nullptr : rec + hh * stride;
+      if (!C::PAIR || kp == 0)
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -935,9 +1005,9 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
             const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
             sm_o[(rw * GP + head) * C::D + d] = o[mt][nt][c];
           }
-      role_sync(2, 128);
+      role_sync(2, C::CT);
       const int64_t out0 = ((int64_t)r * p.nq + (int64_t)hg * HPU * G) * D;
-      for (int idx = ctid; idx < HPU * G * D; idx += 128) {
+      for (int idx = ctid; idx < HPU * G * D; idx += C::CT) {
         const int h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D, d = rem - i * D;
         float M = -CUDART_INF_F;
 #pragma unroll
@@ -963,14 +1033,14 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
           }
         }
       }
-      role_sync(2, 128);  // the epilogue buffer is free again
+      role_sync(2, C::CT);  // the epilogue buffer is free again
     }
     if (!own) {
       // publish the partial; arrive on the unit's ticket now when it is this
       // CTA's first unit (the CTA before finishes it late, so it is rarely
       // the last arrival) and keep the answer for the end of the range
       __threadfence();
-      role_sync(2, 128);
+      role_sync(2, C::CT);
       if (u == u_first && u != u_last) {
         if (ctid == 0) first_ticket = atomicAdd(p.ws_ticket + u, 1u);
       } else {
@@ -989,7 +1059,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   bool entered = false, row_ok = false, aborted = false;
   while (true) {
     const bool ok = mbar_wait(smem_addr(&s_full[ord % S]), (uint32_t)((ord / S) & 1));
-    if (role_any(2, 128, !ok)) {  // a give-up by any consumer is every consumer's decision
+    if (role_any(2, C::CT, !ok)) {  // a give-up by any consumer is every consumer's decision
       aborted = true;
       break;
     }
@@ -1033,7 +1103,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     if (pend_last >= 0 && atomicAdd(p.ws_ticket + pend_last, 1u) == (uint32_t)(contributors(pend_last) - 1))
       s_merge[1] = pend_last;
   }
-  role_sync(2, 128);
+  role_sync(2, C::CT);
   for (int k = 0; k < 2; ++k) {
     const int um = s_merge[k];
     if (um < 0) continue;
@@ -1046,7 +1116,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     const float* rec1 = record_of(c0, 1, um);  // contributors 1.. are 2 * rec_floats apart
     auto rec_c = [&](int c) { return c == 0 ? rec0 : rec1 + (int64_t)2 * (c - 1) * sp.rec_floats; };
     // online merge over the contributors, four records' loads in flight at a time
-    for (int q4 = ctid; q4 < HPU * G * D / 4; q4 += 128) {
+    for (int q4 = ctid; q4 < HPU * G * D / 4; q4 += C::CT) {
       const int idx = q4 * 4, h2 = idx / (G * D), rem = idx - h2 * G * D, i = rem / D;
       float M = -CUDART_INF_F, L = 0.f;
       float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
