@@ -551,28 +551,32 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
       const uint32_t bar = smem_addr(&s_full[st]);
       if constexpr (C::BULK) {
-        // producer warp w moves keys w, w + PW, ...: one bulk copy per K and per
-        // V chunk; its lane 0 then arrives with the bytes to expect (and so
-        // also publishes the tile's offsets and the unit meta, written before
-        // the last producer barrier)
+        // producer warp w moves keys w, w + PW, ...: lane j copies key j's K
+        // row and lane KPWARP + j its V row (one bulk copy each); lane 0 then
+        // arrives with the bytes to expect (and so also publishes the tile's
+        // offsets and the unit meta, written before the last producer barrier)
         constexpr int KPWARP = (TILE + C::PW - 1) / C::PW;
+        static_assert((KPWARP & (KPWARP - 1)) == 0 && 2 * KPWARP <= 32, "one copy per lane");
         unsigned char* sb = smem + st * C::STAGE_BYTES;
-        const int key = rw + C::PW * lane;
-        const bool mine = lane < KPWARP && key < TILE;
+        const int j = lane & (KPWARP - 1), half = lane / KPWARP;
+        const int key = rw + C::PW * j;
+        const bool mine = lane < 2 * KPWARP && key < TILE;
         const bool v = mine && key < kt && s_off[slot + key] != kInvalidOff;
         const uint32_t nv = __popc(__ballot_sync(0xffffffffu, v));
-        if (mine && !v) {
+        if (mine && !v && half == 1) {
+          // a slot without a valid key: zero V (its score is masked, but 0 * NaN
+          // would not vanish); this lane also fills the row when it is valid,
+          // so its own proxy fence orders these writes before that copy
           uint4* row = reinterpret_cast<uint4*>(sb + C::KV_BYTES + key * C::SROW);
           for (int q = 0; q < C::KEYB / 16; ++q) row[q] = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();  // generic writes to the ring before later async copies into it
         __syncwarp();
-        if (lane == 0) mbar_arrive_expect_tx(bar, nv * 2u * (uint32_t)C::KEYB);
+        if (lane == 0) mbar_arrive_expect_tx(bar, nv * (uint32_t)C::KEYB);
         __syncwarp();
         if (v) {
-          const unsigned char* src = p.kv + (int64_t)s_off[slot + key] * 16;
-          bulk_g2s(smem_addr(sb + key * C::SROW), src, C::KEYB, bar);
-          bulk_g2s(smem_addr(sb + C::KV_BYTES + key * C::SROW), src + p.v_minus_k_bytes, C::KEYB, bar);
+          const unsigned char* src = p.kv + (int64_t)s_off[slot + key] * 16 + (half ? p.v_minus_k_bytes : 0);
+          bulk_g2s(smem_addr(sb + half * C::KV_BYTES + key * C::SROW), src, C::KEYB, bar);
         }
       } else {
         const uint32_t sbase = smem_addr(smem + st * C::STAGE_BYTES) + my_dst;
