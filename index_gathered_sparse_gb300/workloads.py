@@ -511,3 +511,147 @@ def to_torch(x: QSAInputs, device, out_dtype: Optional[str] = None) -> dict:
         scale=x.scale,
         group=x.group,
     )
+
+
+# ----------------------------------------------------------------------------
+# block-granular (MSA-style) selection: d_indices [num_kv_heads, total_q, topk]
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class MSAInputs(QSAInputs):
+    """A block-sparse call: the same paged cache, queries and page table, with
+    ``d_indices[h, r, :]`` naming whole logical blocks (pages) of row r's
+    sequence per kv head (``-1`` = unused).  ``token_indices``/``counts`` are
+    empty: block ids replace them."""
+
+    d_indices: Optional[np.ndarray] = None
+
+    @property
+    def topk(self) -> int:
+        return int(self.d_indices.shape[2])
+
+    def query_positions(self) -> np.ndarray:
+        """Each row's position: cache_lengths[b] + (r - input_row_offsets[b])."""
+        seq = self.row_sequence()
+        off = self.input_row_offsets.astype(np.int64)
+        return self.cache_lengths.astype(np.int64)[seq] + np.arange(self.total_q) - off[seq]
+
+    def attended_keys(self) -> np.ndarray:
+        """Keys attended per (kv head, row): positions <= the row's position
+        inside its listed blocks (duplicates count twice)."""
+        P = int(self.kv_shape[3])
+        pos = self.query_positions()[None, :, None]
+        blk = self.d_indices.astype(np.int64)
+        return np.where(blk >= 0, np.clip(pos - blk * P + 1, 0, P), 0).sum(axis=2)
+
+    def algorithmic_bytes(self) -> int:
+        ekv = ELEM_BYTES[self.dtype]
+        eo = ELEM_BYTES[self.out_dtype]
+        n = int(self.attended_keys().sum())  # summed over kv heads already
+        D = self.head_dim
+        return (n * 2 * D * ekv + self.total_q * self.num_q_heads * D * (ekv + eo)
+                + self.d_indices.size * 4)
+
+
+@dataclasses.dataclass
+class MSASpec:
+    """Block-sparse workload recipe: per (kv head, row), the block holding the
+    row's position plus ``topk - 1`` distinct uniform picks among the earlier
+    blocks, in random order; ``-1`` fills the rest when fewer exist."""
+
+    name: str
+    seed: int
+    rows: Sequence[int]
+    cache_lengths: Sequence[int]
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    page_size: int
+    num_layers: int
+    layer_idx: int
+    dtype: str
+    out_dtype: str
+    topk: int
+    page_pad: Optional[int] = None
+
+    def build(self, keep_logical: bool = False) -> MSAInputs:
+        rng = np.random.default_rng(self.seed)
+        B = len(self.rows)
+        rows = np.asarray(self.rows, dtype=np.int64)
+        cache = np.asarray(self.cache_lengths, dtype=np.int64)
+        nq, nkv, D, P = self.num_q_heads, self.num_kv_heads, self.head_dim, self.page_size
+        kv_len = cache + rows
+        perm = rng.permutation(int((-(-kv_len // P)).sum()))
+        total_q = int(rows.sum())
+        q = encode(rng.standard_normal((total_q, nq, D), dtype=np.float32), self.dtype)
+        lk, lv = [], []
+        for b in range(B):
+            n = int(kv_len[b])
+            lk.append(encode(rng.standard_normal((n, nkv, D), dtype=np.float32), self.dtype))
+            lv.append(encode(rng.standard_normal((n, nkv, D), dtype=np.float32), self.dtype))
+        d_idx = np.full((nkv, total_q, self.topk), -1, dtype=np.int32)
+        r = 0
+        for b in range(B):
+            for t in range(int(rows[b])):
+                last = (int(cache[b]) + t) // P
+                for h in range(nkv):
+                    k = min(self.topk, last + 1)
+                    others = rng.choice(last, size=k - 1, replace=False) if k > 1 else np.zeros(0, np.int64)
+                    blocks = np.concatenate([others.astype(np.int64), [last]])
+                    d_idx[h, r, :k] = blocks[rng.permutation(k)]
+                r += 1
+        base = assemble(self.name, self.dtype, self.out_dtype, q, lk, lv, rows, cache, P, self.num_layers,
+                        self.layer_idx, np.zeros((total_q, 0), np.int32), np.zeros(total_q, np.int32),
+                        1.0 / math.sqrt(D), page_perm=perm, page_pad=self.page_pad, keep_logical=keep_logical)
+        return MSAInputs(**{f.name: getattr(base, f.name) for f in dataclasses.fields(QSAInputs)}, d_indices=d_idx)
+
+
+def msa_bf16_decode(seed: int = 6, batch: int = 64, cache_range=(1024, 8192), topk: int = 32,
+                    name: str = "msa_bf16_decode") -> MSASpec:
+    """Block-sparse bf16 decode: 64 x 1 row, cache U[1024, 8192], 32 q heads on
+    8 kv heads, head_dim 128, page (block) 64, 1 layer, topk 32 blocks per
+    (kv head, row) = up to 2048 keys."""
+    rng = np.random.default_rng(seed + 1000)
+    cache = rng.integers(cache_range[0], cache_range[1] + 1, size=batch)
+    return MSASpec(name=name, seed=seed, rows=[1] * batch, cache_lengths=cache.tolist(), num_q_heads=32,
+                   num_kv_heads=8, head_dim=128, page_size=64, num_layers=1, layer_idx=0, dtype="bf16",
+                   out_dtype="bf16", topk=topk)
+
+
+def msa_bf16_prefill(seed: int = 7, rows=(128, 256, 64, 512), cache=(0, 4096, 16384, 8192), topk: int = 32,
+                     name: str = "msa_bf16_prefill") -> MSASpec:
+    """Block-sparse bf16 chunked prefill: rows [128,256,64,512] on cache
+    [0,4096,16384,8192], 64 q heads on 8 kv heads, head_dim 128, block 64,
+    topk 32 (causal inside the block holding each row's position)."""
+    return MSASpec(name=name, seed=seed, rows=list(rows), cache_lengths=list(cache), num_q_heads=64,
+                   num_kv_heads=8, head_dim=128, page_size=64, num_layers=1, layer_idx=0, dtype="bf16",
+                   out_dtype="bf16", topk=topk)
+
+
+def msa_fp8_decode(seed: int = 8, batch: int = 96, cache_range=(512, 16384), topk: int = 16,
+                   name: str = "msa_fp8_decode") -> MSASpec:
+    """Block-sparse scale-free FP8 e4m3 decode: 96 x 1 row, cache U[512,16384],
+    32 q heads on 4 kv heads, head_dim 128, block 128, 2 layers (layer 1),
+    padded pages, bf16 output, topk 16 blocks."""
+    rng = np.random.default_rng(seed + 1000)
+    cache = rng.integers(cache_range[0], cache_range[1] + 1, size=batch)
+    return MSASpec(name=name, seed=seed, rows=[1] * batch, cache_lengths=cache.tolist(), num_q_heads=32,
+                   num_kv_heads=4, head_dim=128, page_size=128, num_layers=2, layer_idx=1, dtype="e4m3",
+                   out_dtype="bf16", topk=topk, page_pad=4096)
+
+
+MSA_WORKLOADS = {
+    "msa_bf16_decode": msa_bf16_decode,
+    "msa_bf16_prefill": msa_bf16_prefill,
+    "msa_fp8_decode": msa_fp8_decode,
+}
+
+
+def msa_small_variants() -> dict:
+    """Block-sparse workloads at oracle-friendly sizes (several blocks, a
+    partial last block, -1 padding where a row has fewer blocks than topk)."""
+    return {
+        "msa_bf16_decode_small": msa_bf16_decode(seed=16, batch=5, cache_range=(70, 900), topk=6),
+        "msa_bf16_prefill_small": msa_bf16_prefill(seed=17, rows=(20, 7, 33), cache=(0, 130, 300), topk=5),
+        "msa_fp8_decode_small": msa_fp8_decode(seed=18, batch=4, cache_range=(100, 1200), topk=4),
+    }

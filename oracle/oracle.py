@@ -62,6 +62,16 @@ def load():
             i64, p, i64,
             p, ctypes.c_double, i64, ctypes.POINTER(i64),
         ]
+        lib.qsa_oracle_msa_attention.restype = ctypes.c_int
+        lib.qsa_oracle_msa_attention.argtypes = [
+            p, p, i64,
+            p, ctypes.c_int, i64, i64, i64,
+            p, i64,
+            p, i64, i64,
+            i64, i64, i64,
+            p, p, i64,
+            i64, p, i64, ctypes.c_double, i64, ctypes.POINTER(i64),
+        ]
         lib.qsa_oracle_decode.restype = None
         lib.qsa_oracle_decode.argtypes = [p, p, ctypes.c_int, i64]
         _lib = lib
@@ -106,6 +116,37 @@ def sparse_attention(x, rows=None) -> np.ndarray:
         _ptr(cl), _ptr(tab), tab.shape[1],
         int(x.layer_idx), _ptr(idx), idx.shape[1],
         _ptr(cnt), float(x.scale), int(x.group), ctypes.byref(bad),
+    )
+    if code != 0:
+        raise OracleError(code, bad.value)
+    return out
+
+
+def msa_attention(x, rows=None) -> np.ndarray:
+    """float64 block-sparse (MSA-style) attention output for the query rows
+    ``rows`` (all if None): ``x`` also carries ``d_indices`` [nkv, total_q, topk]."""
+    lib = load()
+    total_q, nq, D = x.q.shape
+    rows = np.arange(total_q, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, nq, D), dtype=np.float64)
+    num_pages, two, L, P, nkv, Dk = x.kv_shape
+    assert Dk == D and two == 2
+    q = np.ascontiguousarray(x.q)
+    kv = np.ascontiguousarray(x.kv_flat)
+    off = np.ascontiguousarray(x.input_row_offsets, dtype=np.uint32)
+    cl = np.ascontiguousarray(x.cache_lengths, dtype=np.uint32)
+    tab = np.ascontiguousarray(x.kv_lookup_table, dtype=np.uint32)
+    di = np.ascontiguousarray(x.d_indices, dtype=np.int32)
+    assert di.shape[:2] == (nkv, total_q)
+    bad = ctypes.c_int64(-1)
+    code = lib.qsa_oracle_msa_attention(
+        _ptr(out), _ptr(rows), rows.size,
+        _ptr(q), ORACLE_DTYPES[x.dtype], total_q, nq, D,
+        _ptr(off), cl.size,
+        _ptr(kv), num_pages, int(x.page_stride),
+        L, P, nkv,
+        _ptr(cl), _ptr(tab), tab.shape[1],
+        int(x.layer_idx), _ptr(di), di.shape[2], float(x.scale), int(x.group), ctypes.byref(bad),
     )
     if code != 0:
         raise OracleError(code, bad.value)

@@ -212,3 +212,116 @@ void qsa_oracle_decode(double* out, const void* src, int dtype, int64_t n) {
   int64_t i;
   for (i = 0; i < n; ++i) out[i] = decode(dtype, src, i);
 }
+
+/*
+ * Block-sparse (MSA-style) variant: Struct_msa_attention_ragged_paged,
+ * "Gathers topk KV blocks per (kv head, query token) using the block ids in
+ * d_indices" ([n_kv_heads, num_rows, topk] int32), decode with no mask,
+ * prefill and speculative decode causal per token.
+ *
+ * Readings taken where the page is silent: a block is one page of the row's
+ * own sequence, block id beta names logical page beta (positions beta*P ..
+ * beta*P + P - 1, physical page kv_lookup_table[b, beta]); a negative id is
+ * an unused slot; a position attends when it is <= the row's position
+ * pos = cache_lengths[b] + (r - input_row_offsets[b]) (for one new token per
+ * sequence this is exactly "every cached key", so decode needs no mask); a
+ * repeated id is attended twice; a row with nothing attended is zero.  An id
+ * whose first position is <= pos but that has no page-table entry or names a
+ * page outside kv_blocks is a precondition violation.
+ */
+int qsa_oracle_msa_attention(
+    double* out, const int64_t* rows, int64_t n_rows,
+    const void* q, int dtype, int64_t total_q, int64_t num_q_heads, int64_t head_dim,
+    const uint32_t* input_row_offsets, int64_t batch,
+    const void* kv_blocks, int64_t num_pages, int64_t page_stride,
+    int64_t num_layers, int64_t page_size, int64_t num_kv_heads,
+    const uint32_t* cache_lengths, const uint32_t* kv_lookup_table, int64_t max_pages,
+    int64_t layer_idx, const int32_t* d_indices, int64_t topk, double scale, int64_t group,
+    int64_t* bad_row) {
+  int64_t packed_page, pitch, ri, cap;
+  double* s;
+  int64_t* koff;
+
+  *bad_row = -1;
+  if (group <= 0 || num_kv_heads <= 0 || num_q_heads != group * num_kv_heads) return ORACLE_BAD_ARGUMENT;
+  if (layer_idx < 0 || layer_idx >= num_layers || dtype < 0 || dtype > 2 || topk < 0) return ORACLE_BAD_ARGUMENT;
+  packed_page = 2 * num_layers * page_size * num_kv_heads * head_dim;
+  if (page_stride != -1 && page_stride < packed_page) return ORACLE_BAD_ARGUMENT;
+  pitch = (page_stride == -1) ? packed_page : page_stride;
+
+  cap = topk * page_size > 0 ? topk * page_size : 1;
+  s = (double*)malloc(sizeof(double) * (size_t)cap);
+  koff = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);
+  if (!s || !koff) {
+    free(s);
+    free(koff);
+    return ORACLE_NO_MEMORY;
+  }
+
+  for (ri = 0; ri < n_rows; ++ri) {
+    int64_t r = rows[ri];
+    int64_t b = -1, k, pos, h, i, d;
+
+    if (r < 0 || r >= total_q) goto msa_bad_row;
+    for (k = 0; k < batch; ++k)
+      if ((int64_t)input_row_offsets[k] <= r && r < (int64_t)input_row_offsets[k + 1]) {
+        b = k;
+        break;
+      }
+    if (b < 0) goto msa_bad_row;
+    pos = (int64_t)cache_lengths[b] + (r - (int64_t)input_row_offsets[b]);
+
+    for (h = 0; h < num_kv_heads; ++h) {
+      /* the attended keys of (row, kv head): K-row element offsets, in list order */
+      int64_t n = 0, j, e;
+      for (e = 0; e < topk; ++e) {
+        int64_t beta = d_indices[(h * total_q + r) * topk + e], sl;
+        if (beta < 0) continue; /* unused slot */
+        for (sl = 0; sl < page_size; ++sl) {
+          int64_t p = beta * page_size + sl, page;
+          if (p > pos) break; /* causal: later positions of the block are not attended */
+          if (beta >= max_pages) goto msa_bad_page;
+          page = (int64_t)kv_lookup_table[b * max_pages + beta];
+          if (page >= num_pages) goto msa_bad_page;
+          koff[n++] = page * pitch + ((0 * num_layers + layer_idx) * page_size + sl) * num_kv_heads * head_dim +
+                      h * head_dim;
+        }
+      }
+      for (i = 0; i < group; ++i) {
+        int64_t head = h * group + i;
+        int64_t q_off = (r * num_q_heads + head) * head_dim;
+        double* o = out + (ri * num_q_heads + head) * head_dim;
+        double m = -INFINITY, z = 0.0;
+        for (d = 0; d < head_dim; ++d) o[d] = 0.0;
+        if (n == 0) continue;
+        for (j = 0; j < n; ++j) {
+          double dot = 0.0;
+          for (d = 0; d < head_dim; ++d) dot += decode(dtype, q, q_off + d) * decode(dtype, kv_blocks, koff[j] + d);
+          s[j] = scale * dot;
+          if (s[j] > m || isnan(s[j])) m = s[j];
+        }
+        for (j = 0; j < n; ++j) z += exp(s[j] - m);
+        for (j = 0; j < n; ++j) {
+          /* V sits num_layers * page_size * num_kv_heads * head_dim after K */
+          int64_t v_off = koff[j] + num_layers * page_size * num_kv_heads * head_dim;
+          double a = exp(s[j] - m) / z;
+          for (d = 0; d < head_dim; ++d) o[d] += a * decode(dtype, kv_blocks, v_off + d);
+        }
+      }
+    }
+    continue;
+  msa_bad_page:
+    *bad_row = r;
+    free(s);
+    free(koff);
+    return ORACLE_BAD_PAGE;
+  msa_bad_row:
+    *bad_row = r;
+    free(s);
+    free(koff);
+    return ORACLE_BAD_ROW;
+  }
+  free(s);
+  free(koff);
+  return ORACLE_OK;
+}
