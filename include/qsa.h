@@ -164,6 +164,42 @@ QSA_API qsa_status qsa_sparse_attention_ragged_paged_ex(
     qsa_tensor token_indices, qsa_tensor counts, float scale, int32_t group, void* stream,
     const qsa_options* options);
 
+/*
+ * qsa_msa_attention_ragged_paged - block-sparse attention: the selection is a
+ * list of whole blocks per (kv head, query row) instead of token positions
+ * (MAX page "Struct_msa_attention_ragged_paged": "Gathers topk KV blocks per
+ * (kv head, query token) using the block ids in d_indices"; its Args list).
+ *
+ *   d_indices  [num_kv_heads, total_q, topk] I32, block ids per (kv head, row)
+ *
+ * Every other argument is as for qsa_sparse_attention_ragged_paged (no
+ * token_indices or counts).  For row r of sequence b, kv head h and each of
+ * its query heads, the attended keys are the slots s of each listed block
+ * beta = d_indices[h, r, e] (positions beta*page_size + s, page
+ * kv_lookup_table[b, beta]) whose position is <= the row's own position
+ * cache_lengths[b] + (r - input_row_offsets[b]).  Readings where the page is
+ * silent: a block is one page of the row's own sequence; beta < 0 marks an
+ * unused slot; the position rule is the page's per-token causal masking for
+ * prefill and speculative decode and, for one new token per sequence, exactly
+ * "every cached key" (its decode path has no mask); a repeated block counts
+ * twice; nothing attended gives a zero row; a listed block with no page
+ * (beta >= max_pages, or a table entry >= num_pages) is skipped and sets
+ * QSA_STATUS_BAD_PAGE.
+ *
+ * Runs on the per-(row, kv head) tensor-core kernel with split-K: BF16 or
+ * F8E4M3 with head_dim 128, group <= 16, output F32 or BF16 (the page's op
+ * always writes BF16).  `options` may set splits (kernel must be 0 or 2).
+ * Differences from the page's signature: cache_row_offsets,
+ * total_context_length and msa_scalar_args are not taken (the first two follow
+ * from cache_lengths, the scalars are host-known), and max_prompt_length /
+ * max_cache_length are host hints as above.
+ */
+QSA_API qsa_status qsa_msa_attention_ragged_paged(
+    qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks,
+    int64_t page_stride, qsa_tensor cache_lengths, qsa_tensor kv_lookup_table,
+    uint32_t max_prompt_length, uint32_t max_cache_length, uint32_t layer_idx,
+    qsa_tensor d_indices, float scale, int32_t group, void* stream, const qsa_options* options);
+
 /* Describes the launch a call with these extents would make, without
  * launching: kernel (1 CUDA-core, 2 tensor-core), CTAs per (row, kv head)
  * along the selection, total CTAs and split-K workspace bytes.  dtype is the

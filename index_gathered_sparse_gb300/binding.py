@@ -68,6 +68,9 @@ def load_library():
     lib.qsa_sparse_attention_ragged_paged.restype = ctypes.c_int
     lib.qsa_sparse_attention_ragged_paged_ex.argtypes = common + [ctypes.POINTER(qsa_options)]
     lib.qsa_sparse_attention_ragged_paged_ex.restype = ctypes.c_int
+    lib.qsa_msa_attention_ragged_paged.argtypes = [T, T, T, T, i64, T, T, u32, u32, u32, T, ctypes.c_float, i32, P,
+                                                   ctypes.POINTER(qsa_options)]
+    lib.qsa_msa_attention_ragged_paged.restype = ctypes.c_int
     lib.qsa_plan.argtypes = [i32, i64, i64, i64, i64, i32, ctypes.POINTER(qsa_options), ctypes.POINTER(i32),
                              ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_size_t)]
     lib.qsa_plan.restype = ctypes.c_int
@@ -172,6 +175,26 @@ def qsa_sparse_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, p
         _check(lib.qsa_sparse_attention_ragged_paged_ex(*args, ctypes.byref(opt)))
     else:
         _check(lib.qsa_sparse_attention_ragged_paged(*args))
+
+
+def qsa_msa_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
+                                   kv_lookup_table, max_prompt_length, max_cache_length, layer_idx, d_indices,
+                                   scale, group, stream=None, *, kernel: int = 0, splits: int = 0) -> None:
+    """Block-sparse attention on the GPU: ``d_indices`` [num_kv_heads, total_q,
+    topk] int32 lists whole blocks (pages) per (kv head, row); see qsa.h."""
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    if d_indices.dtype != torch.int32:
+        raise TypeError("d_indices must be int32")
+    opt = qsa_options(kernel=kernel, splits=splits, ctas=0)
+    _check(lib.qsa_msa_attention_ragged_paged(
+        _contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets), _kv_desc(kv_blocks, int(page_stride)),
+        int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length),
+        int(max_cache_length), int(layer_idx), _contig(d_indices, "d_indices"), float(scale), int(group),
+        ctypes.c_void_p(stream), ctypes.byref(opt)))
 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,

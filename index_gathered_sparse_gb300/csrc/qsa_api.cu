@@ -395,30 +395,16 @@ qsa_status ensure_status(DeviceState& st) {
   return QSA_OK;
 }
 
-}  // namespace
-
-extern "C" {
-
-qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
-                                                qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths,
-                                                qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
-                                                uint32_t max_cache_length, uint32_t layer_idx,
-                                                qsa_tensor token_indices, qsa_tensor counts, float scale,
-                                                int32_t group, void* stream, const qsa_options* options) {
-  (void)max_prompt_length;  // launch-sizing hints only: the plan uses host-known extents
-  (void)max_cache_length;
-  Resolved R;
-  qsa_status s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table,
-                            layer_idx, token_indices, counts, group, options, R);
-  if (s != QSA_OK) return s;
-  if (R.total_q == 0) return QSA_OK;
-
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  s = plan_launch(R, group, options, dev);
-  if (s != QSA_OK) return s;
-
+// Everything after the plan: status word and workspace of (device, stream),
+// the kernel parameters, and the launch.  `indices`/`counts` carry a token
+// selection, or `blocks`/`topk` a block selection (kernel 2 only).
+qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tensor& q,
+                          const qsa_tensor& input_row_offsets, const qsa_tensor& kv_blocks,
+                          const qsa_tensor& cache_lengths, const qsa_tensor& kv_lookup_table, uint32_t layer_idx,
+                          const int32_t* indices, const int32_t* counts, const int32_t* blocks, int32_t topk,
+                          float scale, int32_t group, void* stream, int dev) {
+  qsa_status s = QSA_OK;
+  cudaError_t e = cudaSuccess;
   Params p;
   std::memset(&p, 0, sizeof(p));
   {
@@ -442,8 +428,10 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
   p.kv = static_cast<const unsigned char*>(kv_blocks.data);
   p.cache_lengths = static_cast<const uint32_t*>(cache_lengths.data);
   p.table = static_cast<const uint32_t*>(kv_lookup_table.data);
-  p.indices = static_cast<const int32_t*>(token_indices.data);
-  p.counts = static_cast<const int32_t*>(counts.data);
+  p.indices = indices;
+  p.counts = counts;
+  p.blocks = blocks;
+  p.topk = topk;
   p.page_pitch_bytes = R.pitch * eb;
   p.k_layer_bytes = (int64_t)layer_idx * R.P * R.nkv * R.D * eb;
   p.v_minus_k_bytes = R.L * R.P * R.nkv * R.D * eb;
@@ -478,6 +466,35 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
   return QSA_OK;
 }
 
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
+                                                qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths,
+                                                qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
+                                                uint32_t max_cache_length, uint32_t layer_idx,
+                                                qsa_tensor token_indices, qsa_tensor counts, float scale,
+                                                int32_t group, void* stream, const qsa_options* options) {
+  (void)max_prompt_length;  // launch-sizing hints only: the plan uses host-known extents
+  (void)max_cache_length;
+  Resolved R;
+  qsa_status s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table,
+                            layer_idx, token_indices, counts, group, options, R);
+  if (s != QSA_OK) return s;
+  if (R.total_q == 0) return QSA_OK;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  s = plan_launch(R, group, options, dev);
+  if (s != QSA_OK) return s;
+
+  return launch_planned(R, output, q, input_row_offsets, kv_blocks, cache_lengths, kv_lookup_table, layer_idx,
+                        static_cast<const int32_t*>(token_indices.data), static_cast<const int32_t*>(counts.data),
+                        nullptr, 0, scale, group, stream, dev);
+}
+
 qsa_status qsa_sparse_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
                                              qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths,
                                              qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
@@ -486,6 +503,55 @@ qsa_status qsa_sparse_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qs
   return qsa_sparse_attention_ragged_paged_ex(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
                                               kv_lookup_table, max_prompt_length, max_cache_length, layer_idx,
                                               token_indices, counts, scale, group, stream, nullptr);
+}
+
+qsa_status qsa_msa_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
+                                          qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths,
+                                          qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
+                                          uint32_t max_cache_length, uint32_t layer_idx, qsa_tensor d_indices,
+                                          float scale, int32_t group, void* stream, const qsa_options* options) {
+  (void)max_prompt_length;
+  (void)max_cache_length;
+  if (d_indices.ndim != 3) return fail(QSA_ERR_SHAPE, "d_indices: rank " + std::to_string(d_indices.ndim) + ", expected 3");
+  if (d_indices.dtype != QSA_I32) return fail(QSA_ERR_DTYPE, "d_indices: element type must be I32");
+  for (int i = 0; i < 3; ++i)
+    if (d_indices.shape[i] < 0) return fail(QSA_ERR_SHAPE, "d_indices: negative extent");
+  if (kv_blocks.ndim == 6 && d_indices.shape[0] != kv_blocks.shape[4])
+    return fail(QSA_ERR_SHAPE, "d_indices: first extent must be num_kv_heads");
+  if (q.ndim == 3 && d_indices.shape[1] != q.shape[0]) return fail(QSA_ERR_SHAPE, "d_indices: second extent must be total_q");
+  if (!d_indices.data && numel(d_indices)) return fail(QSA_ERR_NULL, "d_indices is NULL");
+  qsa_options opt;
+  std::memset(&opt, 0, sizeof(opt));
+  if (options) opt = *options;
+  if (opt.kernel != 0 && opt.kernel != 2)
+    return fail(QSA_ERR_UNSUPPORTED, "block lists run on the per-(row, kv head) tensor-core kernel (options.kernel 2)");
+  opt.kernel = 2;
+  const int64_t topk = d_indices.shape[2];
+  const int64_t P = kv_blocks.ndim == 6 ? kv_blocks.shape[3] : 0;
+  if (topk * P > 0x7FFFFFFF) return fail(QSA_ERR_UNSUPPORTED, "topk * page_size exceeds 2^31 - 1");
+  // the shared checks see the block list as a token list of topk * page_size
+  // keys per row with no counts (stand-ins that are never read)
+  qsa_tensor keys = d_indices, cnt = d_indices;
+  keys.ndim = 2;
+  keys.shape[0] = q.ndim == 3 ? q.shape[0] : 0;
+  keys.shape[1] = topk * P;
+  cnt.ndim = 1;
+  cnt.shape[0] = keys.shape[0];
+  cnt.data = output.data;
+  if (!keys.data) keys.data = output.data;
+  Resolved R;
+  qsa_status s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table,
+                            layer_idx, keys, cnt, group, &opt, R);
+  if (s != QSA_OK) return s;
+  if (R.total_q == 0) return QSA_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  s = plan_launch(R, group, &opt, dev);
+  if (s != QSA_OK) return s;
+  return launch_planned(R, output, q, input_row_offsets, kv_blocks, cache_lengths, kv_lookup_table, layer_idx,
+                        nullptr, nullptr, static_cast<const int32_t*>(d_indices.data), (int32_t)topk, scale, group,
+                        stream, dev);
 }
 
 qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,

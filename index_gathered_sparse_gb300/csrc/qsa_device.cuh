@@ -17,7 +17,7 @@ constexpr uint32_t kInvalidOff = 0xFFFFFFFFu;
 struct RowInfo {
   int b;           // owning sequence
   int64_t kv_len;  // valid positions of that sequence: cache_lengths[b] + rows_b
-  int n;           // valid selection entries: clamp(counts[r], 0, W)
+  int n;           // valid selection entries: clamp(counts[r], 0, W) (W with block lists)
   bool ok;         // r belongs to a sequence
 };
 
@@ -42,7 +42,7 @@ __device__ __forceinline__ RowInfo row_info(const Params& p, int r) {
     if (o0 <= (uint32_t)r && (uint32_t)r < o1) {
       ri.ok = true;
       ri.kv_len = (int64_t)__ldg(p.cache_lengths + c) + (int64_t)(o1 - o0);
-      ri.n = min(max(__ldg(p.counts + r), 0), p.W);
+      ri.n = p.counts ? min(max(__ldg(p.counts + r), 0), p.W) : p.W;  // no counts with block lists
     }
   }
   return ri;

@@ -35,6 +35,13 @@ struct Params {
   int32_t out_bf16;
   int32_t splits;    // CTAs per (row, kv head)
   int32_t band;      // keys per split band (multiple of the key tile)
+  // Block-granular selection (kernel 2 only): when `blocks` is set, key j of
+  // (row r, kv head h) is slot j % P of logical block
+  // blocks[(h * total_q + r) * topk + j / P] (-1: unused), attended when its
+  // position is <= the row's position; W == topk * P and indices/counts are
+  // unused.
+  const int32_t* blocks;  // [nkv, total_q, topk] or nullptr
+  int32_t topk;
 };
 
 // Launch plan of the persistent stream-K kernel (computed on the host).

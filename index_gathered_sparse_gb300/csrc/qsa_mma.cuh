@@ -133,13 +133,18 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   const int r = p.total_q - 1 - cta / p.splits;
 
   const RowInfo ri = row_info(p, r);
+  const bool block_sel = p.blocks != nullptr;
   const int j0 = split * p.band;
-  const int band_n = ri.ok ? max(0, min(ri.n - j0, p.band)) : 0;
+  const int n_row = block_sel ? p.W : ri.n;  // block lists are masked per key instead
+  const int band_n = ri.ok ? max(0, min(n_row - j0, p.band)) : 0;
   uint32_t bad = ri.ok ? 0u : QSA_STATUS_BAD_ROW;
 
   // ---- translate the band's positions into K-row offsets (16-byte units) ----
   {
     const int32_t* idx_row = p.indices + (int64_t)r * p.W + j0;
+    const int32_t* blk_row = p.blocks + ((int64_t)h * p.total_q + r) * p.topk;
+    // the row's own position, for the block lists' causal rule
+    const int64_t pos_q = block_sel && ri.ok ? (int64_t)__ldg(p.cache_lengths + ri.b) + r - (int64_t)__ldg(p.row_offsets + ri.b) : 0;
     const uint32_t* trow = p.table + (int64_t)ri.b * p.max_pages;
     for (int k0 = 0; k0 < band_n; k0 += kMmaThreads * 8) {
       int32_t pos[8];
@@ -148,12 +153,22 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kMmaThreads + tid;
-        pos[u] = k < band_n ? __ldg(idx_row + k) : 0;
+        if (block_sel) {
+          // slot (j0 + k) % P of listed block (j0 + k) / P; -1 when unused or
+          // after the row's position (never attended, not an error)
+          const int j = j0 + k;
+          const int32_t beta = k < band_n ? __ldg(blk_row + j / p.P) : -1;
+          const int64_t q = (int64_t)beta * p.P + (j - (j / p.P) * p.P);
+          pos[u] = beta >= 0 && q <= pos_q ? (int32_t)q : -1;
+        } else {
+          pos[u] = k < band_n ? __ldg(idx_row + k) : 0;
+        }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kMmaThreads + tid;
-        lp[u] = k < band_n ? logical_page(p, ri.kv_len, pos[u], bad) : -1;
+        const bool skip = block_sel && pos[u] < 0;
+        lp[u] = k < band_n && !skip ? logical_page(p, ri.kv_len, pos[u], bad) : -1;
         page[u] = lp[u] >= 0 ? __ldg(trow + lp[u]) : 0u;
       }
 #pragma unroll

@@ -655,3 +655,15 @@ def msa_small_variants() -> dict:
         "msa_bf16_prefill_small": msa_bf16_prefill(seed=17, rows=(20, 7, 33), cache=(0, 130, 300), topk=5),
         "msa_fp8_decode_small": msa_fp8_decode(seed=18, batch=4, cache_range=(100, 1200), topk=4),
     }
+
+
+def to_torch_msa(x: MSAInputs, device, out_dtype: Optional[str] = None) -> dict:
+    """Uploads a block-sparse call: the keyword arguments of
+    ``binding.qsa_msa_attention_ragged_paged``."""
+    import torch
+
+    d = to_torch(x, device, out_dtype)
+    d.pop("token_indices")
+    d.pop("counts")
+    d["d_indices"] = torch.from_numpy(np.ascontiguousarray(x.d_indices, dtype=np.int32)).to(device)
+    return d
