@@ -134,7 +134,7 @@ def replica_spec(name: str, rank: int, world: int):
     """The workload one rank runs: every rank gets its own seeded batch."""
     from index_gathered_sparse_gb300 import workloads as wl
 
-    spec = wl.WORKLOADS[name]()
+    spec = (wl.WORKLOADS.get(name) or wl.MSA_WORKLOADS[name])()
     if world > 1:
         spec.seed += 100 * rank
     return spec
@@ -165,15 +165,25 @@ def sample_rows(total_q: int):
     return order.astype(np.int64)
 
 
-def cpu_oracle_rate(x, seconds: float, rows_per_call: int = 1):
-    """Rows per second of the float64 oracle on this host, one thread."""
+def is_block_sparse(x) -> bool:
+    return getattr(x, "d_indices", None) is not None
+
+
+def oracle_fn(x):
+    """The oracle function for ``x``: token lists or block lists."""
     import oracle
 
+    return oracle.msa_attention if is_block_sparse(x) else oracle.sparse_attention
+
+
+def cpu_oracle_rate(x, seconds: float, rows_per_call: int = 1):
+    """Rows per second of the float64 oracle on this host, one thread."""
+    run = oracle_fn(x)
     rows = sample_rows(x.total_q)
     done, t0 = 0, time.perf_counter()
     while True:
         sel = rows[done % rows.size: done % rows.size + rows_per_call]
-        oracle.sparse_attention(x, sel)
+        run(x, sel)
         done += sel.size
         el = time.perf_counter() - t0
         if el >= seconds:
@@ -189,9 +199,10 @@ def run_reference(args, x, rank, world):
     if rank != 0:
         return
     oracle.build()
+    run = oracle_fn(x)
     rows = sample_rows(x.total_q)
     t0 = time.perf_counter()
-    oracle.sparse_attention(x, rows[:1])
+    run(x, rows[:1])
     per_row = time.perf_counter() - t0
     rows_per_step = max(1, int(round(0.5 / max(per_row, 1e-6))))
     k = 0
@@ -199,7 +210,7 @@ def run_reference(args, x, rank, world):
     def step():
         nonlocal k
         sel = np.take(rows, np.arange(k, k + rows_per_step), mode="wrap")
-        oracle.sparse_attention(x, sel)
+        run(x, sel)
         k += rows_per_step
 
     for _ in range(args.warmup):
@@ -222,13 +233,17 @@ def run_reference(args, x, rank, world):
 
 
 def workload_config(x) -> dict:
-    return {
+    cfg = {
         "workload": x.name, "batch": x.batch, "total_q": x.total_q, "num_q_heads": x.num_q_heads,
         "num_kv_heads": x.num_kv_heads, "group": x.group, "head_dim": x.head_dim, "page_size": x.kv_shape[3],
         "num_layers": x.kv_shape[2], "layer_idx": x.layer_idx, "selection_width": x.selection_width,
         "cache_dtype": x.dtype, "out_dtype": x.out_dtype,
         "l2": "flushed before every timed step (2x L2 buffer written, then a second 2x L2 buffer read)",
     }
+    if is_block_sparse(x):
+        cfg.update({"selection": "blocks (d_indices [num_kv_heads, total_q, topk])", "topk": x.topk,
+                    "selection_width": x.topk * x.kv_shape[3]})
+    return cfg
 
 
 def main():
@@ -259,10 +274,12 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    d = wl.to_torch(x, dev)
+    blocks = is_block_sparse(x)
+    d = wl.to_torch_msa(x, dev) if blocks else wl.to_torch(x, dev)
     code = {"f32": B.QSA_F32, "bf16": B.QSA_BF16, "e4m3": B.QSA_F8E4M3}[x.dtype]
-    plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, x.selection_width, x.group,
-                      kernel=args.kernel, splits=args.splits, ctas=args.ctas)
+    width = x.topk * x.kv_shape[3] if blocks else x.selection_width
+    plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
+                      kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
@@ -281,7 +298,10 @@ def main():
     flush_buf = _Flush()
 
     def call():
-        B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas)
+        if blocks:
+            B.qsa_msa_attention_ragged_paged(**d, splits=args.splits)
+        else:
+            B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas)
 
     def barrier():
         torch.cuda.synchronize()
@@ -324,8 +344,9 @@ def main():
     # ---- end to end: per-step inputs from pinned host memory, output back ----
     e2e = None
     if not args.no_e2e:
+        sel_keys = ("d_indices",) if blocks else ("token_indices", "counts")
         host = {k: d[k].cpu().pin_memory() for k in
-                ("q", "input_row_offsets", "cache_lengths", "kv_lookup_table", "token_indices", "counts")}
+                ("q", "input_row_offsets", "cache_lengths", "kv_lookup_table") + sel_keys}
         out_host = torch.empty(d["output"].shape, dtype=d["output"].dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_host.numel() * out_host.element_size()
@@ -377,6 +398,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": x.dtype, "data": "synthetic (seeded numpy)", "config": cfg,
+            "ms_per_step_median": sorted(per_step)[len(per_step) // 2], "ms_per_step_min": min(per_step),
             "effective_gbs": achieved, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
             "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clocks, "device_status": flags,
