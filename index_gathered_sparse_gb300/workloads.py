@@ -667,3 +667,113 @@ def to_torch_msa(x: MSAInputs, device, out_dtype: Optional[str] = None) -> dict:
     d.pop("counts")
     d["d_indices"] = torch.from_numpy(np.ascontiguousarray(x.d_indices, dtype=np.int32)).to(device)
     return d
+
+
+# ----------------------------------------------------------------------------
+# block-key compression (QSACompressKeysPaged): raw index keys -> block keys
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class CompressInputs:
+    """One block-key compression call, host arrays in raw storage.  ``cache``
+    holds the raw keys in a one-head paged cache (K at axis-1 index 0)."""
+
+    name: str
+    dtype: str        # keys, gamma and output
+    freq_dtype: str
+    cache: QSAInputs  # kv_flat / kv_shape / page_stride / table / cache_lengths / layer_idx
+    key_counts: np.ndarray  # [batch] int32
+    gamma: np.ndarray       # [head_dim] raw storage
+    freqs_cis: np.ndarray   # [positions, rotary_dim] raw storage: cos, sin pairs
+    max_blocks: int
+    ratio: int
+    rotary_dim: int
+    eps: float
+
+    @property
+    def batch(self) -> int:
+        return int(self.key_counts.shape[0])
+
+    @property
+    def head_dim(self) -> int:
+        return int(self.cache.kv_shape[5])
+
+    def algorithmic_bytes(self) -> int:
+        """Raw keys of complete blocks read once, block keys written, plus
+        gamma and the rotary rows used."""
+        e = ELEM_BYTES[self.dtype]
+        D = self.head_dim
+        nblk = np.minimum(np.maximum(self.key_counts, 0) // self.ratio, self.max_blocks)
+        return int(nblk.sum() * self.ratio * D * e + self.batch * self.max_blocks * D * e + D * e
+                   + min(int(nblk.max()) if nblk.size else 0, self.freqs_cis.shape[0]) * self.rotary_dim
+                   * ELEM_BYTES[self.freq_dtype])
+
+
+def rope_table(positions: int, rotary_dim: int, theta: float = 10000.0) -> np.ndarray:
+    """[positions, rotary_dim] cos/sin pairs: angle pos * theta^(-2k/rotary_dim)
+    for pair k (the usual rotary frequencies)."""
+    k = np.arange(rotary_dim // 2, dtype=np.float64)
+    ang = np.arange(positions, dtype=np.float64)[:, None] * theta ** (-2.0 * k / max(rotary_dim, 1))[None, :]
+    out = np.empty((positions, rotary_dim), np.float64)
+    out[:, 0::2] = np.cos(ang)
+    out[:, 1::2] = np.sin(ang)
+    return out
+
+
+@dataclasses.dataclass
+class CompressSpec:
+    name: str
+    seed: int
+    key_counts: Sequence[int]
+    head_dim: int = 128
+    page_size: int = 64
+    num_layers: int = 1
+    layer_idx: int = 0
+    ratio: int = 4
+    rotary_dim: int = 64
+    dtype: str = "bf16"
+    freq_dtype: str = "f32"
+    eps: float = 1e-6
+    extra_blocks: int = 2  # rows past the longest sequence's last block (written as zeros)
+    page_pad: Optional[int] = None
+
+    def build(self, keep_logical: bool = False) -> CompressInputs:
+        rng = np.random.default_rng(self.seed)
+        counts = np.asarray(self.key_counts, dtype=np.int64)
+        B, D, P = counts.size, self.head_dim, self.page_size
+        n_keys = np.maximum(counts, 0)
+        perm = rng.permutation(int((-(-n_keys // P)).sum()))
+        keys = [encode(rng.standard_normal((int(n), 1, D), dtype=np.float32), self.dtype) for n in n_keys]
+        vals = [encode(np.zeros((int(n), 1, D), dtype=np.float32), self.dtype) for n in n_keys]
+        cache = assemble(self.name, self.dtype, self.dtype, np.zeros((0, 1, D), np.float32).astype(_STORAGE[self.dtype]),
+                         keys, vals, [0] * B, n_keys, P, self.num_layers, self.layer_idx,
+                         np.zeros((0, 0), np.int32), np.zeros(0, np.int32), 1.0, page_perm=perm,
+                         page_pad=self.page_pad, keep_logical=keep_logical)
+        max_blocks = int((n_keys // self.ratio).max()) + self.extra_blocks if B else 0
+        gamma = encode((1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32), self.dtype)
+        freqs = rope_table(max(max_blocks, 1), self.rotary_dim)
+        freqs = freqs.astype(np.float32) if self.freq_dtype == "f32" else encode(freqs.astype(np.float32), self.freq_dtype)
+        return CompressInputs(name=self.name, dtype=self.dtype, freq_dtype=self.freq_dtype, cache=cache,
+                              key_counts=counts.astype(np.int32), gamma=gamma, freqs_cis=np.ascontiguousarray(freqs),
+                              max_blocks=max_blocks, ratio=self.ratio, rotary_dim=self.rotary_dim, eps=self.eps)
+
+
+def compress_bf16(seed: int = 9, batch: int = 64, count_range=(1024, 65536), ratio: int = 4,
+                  name: str = "compress_bf16") -> CompressSpec:
+    """Block-key compression, bf16: 64 sequences of U[1024, 65536] raw index
+    keys (head_dim 128), page 64, ratio 4, rotary over 64 channels."""
+    rng = np.random.default_rng(seed + 1000)
+    counts = rng.integers(count_range[0], count_range[1] + 1, size=batch)
+    return CompressSpec(name=name, seed=seed, key_counts=counts.tolist(), ratio=ratio)
+
+
+COMPRESS_WORKLOADS = {"compress_bf16": compress_bf16}
+
+
+def compress_small_variants() -> dict:
+    return {
+        "compress_bf16_small": compress_bf16(seed=19, batch=5, count_range=(0, 300), name="compress_bf16_small"),
+        "compress_f32_small": dataclasses.replace(
+            compress_bf16(seed=20, batch=4, count_range=(3, 200), ratio=3, name="compress_f32_small"),
+            dtype="f32", rotary_dim=128, page_size=16, page_pad=64),
+    }

@@ -72,6 +72,15 @@ def load():
             p, p, i64,
             i64, p, i64, ctypes.c_double, i64, ctypes.POINTER(i64),
         ]
+        lib.qsa_oracle_compress_keys.restype = ctypes.c_int
+        lib.qsa_oracle_compress_keys.argtypes = [
+            p, i64, i64, i64,
+            p, p, ctypes.c_int, i64,
+            i64, p, p, ctypes.c_int,
+            i64, i64, i64, i64,
+            p, i64, i64, i64,
+            ctypes.c_double,
+        ]
         lib.qsa_oracle_decode.restype = None
         lib.qsa_oracle_decode.argtypes = [p, p, ctypes.c_int, i64]
         _lib = lib
@@ -150,4 +159,30 @@ def msa_attention(x, rows=None) -> np.ndarray:
     )
     if code != 0:
         raise OracleError(code, bad.value)
+    return out
+
+
+def compress_keys(x) -> np.ndarray:
+    """float64 block keys [batch * max_blocks, head_dim] of a block-key
+    compression call ``x`` (see qsa_oracle_compress_keys for the readings)."""
+    lib = load()
+    c = x.cache
+    num_pages, two, L, P, nkv, D = c.kv_shape
+    assert nkv == 1 and two == 2
+    out = np.empty((x.batch * x.max_blocks, D), dtype=np.float64)
+    kv = np.ascontiguousarray(c.kv_flat)
+    tab = np.ascontiguousarray(c.kv_lookup_table, dtype=np.uint32)
+    cnt = np.ascontiguousarray(x.key_counts, dtype=np.int32)
+    gamma = np.ascontiguousarray(x.gamma)
+    fr = np.ascontiguousarray(x.freqs_cis)
+    code = lib.qsa_oracle_compress_keys(
+        _ptr(out), x.batch, x.max_blocks, D,
+        _ptr(gamma), _ptr(fr), ORACLE_DTYPES[x.freq_dtype], fr.shape[0],
+        x.rotary_dim, _ptr(cnt), _ptr(kv), ORACLE_DTYPES[x.dtype],
+        num_pages, int(c.page_stride), L, P,
+        _ptr(tab), tab.shape[1], int(c.layer_idx), int(x.ratio),
+        float(x.eps),
+    )
+    if code != 0:
+        raise OracleError(code, -1)
     return out

@@ -325,3 +325,81 @@ int qsa_oracle_msa_attention(
   free(koff);
   return ORACLE_OK;
 }
+
+/*
+ * Block-key compression: QSACompressKeysPaged ("Pools a paged group of raw QSA
+ * index keys into dense block keys"; tensor shapes block_keys
+ * [batch * max_blocks, head_dim], gamma [head_dim], freqs_cis [positions,
+ * rotary_dim], key_counts [batch], kv_blocks [num_pages, 2, num_layers,
+ * page_size, 1, head_dim]; parameters ratio, rotary_dim, eps).
+ *
+ * Readings taken where the page is silent (the page names the steps -
+ * pooling by `ratio`, the k_layernorm weight gamma with rms_norm_eps, the
+ * rotary table - but not their order or exact form):
+ *   raw key j of sequence b (j < key_counts[b]) is
+ *     kv_blocks[kv_lookup_table[b, j / page_size], 0, layer_idx, j % page_size, 0, :];
+ *   block i (i < max_blocks = rows of block_keys / batch) covers raw keys
+ *     i*ratio .. i*ratio + ratio - 1 and exists when all of them do; the rows
+ *     of missing blocks are zero;
+ *   x = mean of the block's raw keys; y_d = x_d / sqrt(mean_d x_d^2 + eps) * gamma_d;
+ *   the channel pairs (2k, 2k+1) below rotary_dim turn by the angle whose
+ *     cosine and sine are freqs_cis[i, 2k] and freqs_cis[i, 2k+1] (the block's
+ *     index is its position); channels at or past rotary_dim pass through.
+ * Keys, gamma and the output share one element type; freqs_cis has its own.
+ */
+int qsa_oracle_compress_keys(double* out, int64_t batch, int64_t max_blocks, int64_t head_dim,
+                             const void* gamma, const void* freqs, int freq_dtype, int64_t positions,
+                             int64_t rotary_dim, const int32_t* key_counts, const void* kv_blocks, int dtype,
+                             int64_t num_pages, int64_t page_stride, int64_t num_layers, int64_t page_size,
+                             const uint32_t* kv_lookup_table, int64_t max_pages, int64_t layer_idx, int64_t ratio,
+                             double eps) {
+  int64_t pitch, b, i, d, j;
+  double* x;
+  if (ratio <= 0 || head_dim <= 0 || rotary_dim < 0 || rotary_dim > head_dim || (rotary_dim & 1)) return ORACLE_BAD_ARGUMENT;
+  if (layer_idx < 0 || layer_idx >= num_layers) return ORACLE_BAD_ARGUMENT;
+  pitch = page_stride == -1 ? 2 * num_layers * page_size * head_dim : page_stride;
+  x = (double*)malloc(sizeof(double) * (size_t)head_dim);
+  if (!x) return ORACLE_NO_MEMORY;
+  for (b = 0; b < batch; ++b) {
+    int64_t nblk = key_counts[b] > 0 ? key_counts[b] / ratio : 0;
+    for (i = 0; i < max_blocks; ++i) {
+      double* o = out + (b * max_blocks + i) * head_dim;
+      double ss = 0.0, inv;
+      for (d = 0; d < head_dim; ++d) o[d] = 0.0;
+      if (i >= nblk) continue;
+      if (rotary_dim > 0 && i >= positions) {
+        free(x);
+        return ORACLE_BAD_ARGUMENT;
+      }
+      for (d = 0; d < head_dim; ++d) x[d] = 0.0;
+      for (j = i * ratio; j < (i + 1) * ratio; ++j) {
+        int64_t lp = j / page_size, page, off;
+        if (lp >= max_pages) {
+          free(x);
+          return ORACLE_BAD_PAGE;
+        }
+        page = (int64_t)kv_lookup_table[b * max_pages + lp];
+        if (page >= num_pages) {
+          free(x);
+          return ORACLE_BAD_PAGE;
+        }
+        off = page * pitch + ((0 * num_layers + layer_idx) * page_size + j % page_size) * head_dim;
+        for (d = 0; d < head_dim; ++d) x[d] += decode(dtype, kv_blocks, off + d);
+      }
+      for (d = 0; d < head_dim; ++d) {
+        x[d] /= (double)ratio;
+        ss += x[d] * x[d];
+      }
+      inv = 1.0 / sqrt(ss / (double)head_dim + eps);
+      for (d = 0; d < head_dim; ++d) o[d] = x[d] * inv * decode(dtype, gamma, d);
+      for (d = 0; d + 1 < rotary_dim; d += 2) {
+        double c = decode(freq_dtype, freqs, i * rotary_dim + d), s = decode(freq_dtype, freqs, i * rotary_dim + d + 1);
+        double a = o[d], e = o[d + 1];
+        o[d] = a * c - e * s;
+        o[d + 1] = a * s + e * c;
+      }
+    }
+  }
+  free(x);
+  return ORACLE_OK;
+}
