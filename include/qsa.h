@@ -200,6 +200,43 @@ QSA_API qsa_status qsa_msa_attention_ragged_paged(
     uint32_t max_prompt_length, uint32_t max_cache_length, uint32_t layer_idx,
     qsa_tensor d_indices, float scale, int32_t group, void* stream, const qsa_options* options);
 
+/*
+ * qsa_compress_keys_paged - block-key compression of raw QSA index keys
+ * (MAX page "QSACompressKeysPaged": "Pools a paged group of raw QSA index
+ * keys into dense block keys"; its tensor shapes, its gamma / freqs_cis /
+ * key_counts arguments and its ratio, rotary_dim and eps parameters).
+ *
+ *   block_keys       [batch * max_blocks, head_dim]  F32 or BF16, written
+ *   gamma            [head_dim] same type (k_layernorm weight)
+ *   freqs_cis        [positions, rotary_dim] F32 or BF16: cos, sin pairs
+ *   key_counts       [batch] I32, raw keys per sequence, this step included
+ *   kv_blocks        [num_pages, 2, num_layers, page_size, 1, head_dim]
+ *                    same type as block_keys; K at axis-1 index 0 is read
+ *   page_stride, cache_lengths [batch] U32 (shape-checked only),
+ *   kv_lookup_table, max_prompt_length, max_cache_length, layer_idx as for
+ *   qsa_sparse_attention_ragged_paged
+ *   ratio            raw keys per block (>= 1)
+ *   rotary_dim       channels the rotation covers (even, <= head_dim)
+ *   eps              RMS-norm epsilon (>= 0)
+ *
+ * Computes, for block i of sequence b (max_blocks = rows / batch): x = mean of
+ * raw keys i*ratio .. i*ratio + ratio - 1 (raw key j is kv_blocks[page
+ * kv_lookup_table[b, j / page_size], 0, layer_idx, j % page_size, 0, :]);
+ * y = x / sqrt(mean(x^2) + eps) * gamma; channel pairs (2k, 2k+1) below
+ * rotary_dim turned by freqs_cis[i, 2k] (cos) and [i, 2k+1] (sin).  Readings
+ * where the page is silent: the pooling is a mean over complete blocks only
+ * (rows of incomplete or missing blocks are zero), the order is pool, norm,
+ * rotate, and the rotary position of a block is its index.  A raw key with no
+ * page is skipped: its block's row is zero and QSA_STATUS_BAD_PAGE is set.
+ * head_dim 128 or 256; f32 arithmetic; block_keys, gamma and kv_blocks
+ * 16-byte aligned.
+ */
+QSA_API qsa_status qsa_compress_keys_paged(
+    qsa_tensor block_keys, qsa_tensor gamma, qsa_tensor freqs_cis, qsa_tensor key_counts,
+    qsa_tensor kv_blocks, int64_t page_stride, qsa_tensor cache_lengths, qsa_tensor kv_lookup_table,
+    uint32_t max_prompt_length, uint32_t max_cache_length, uint32_t layer_idx, int32_t ratio,
+    int32_t rotary_dim, float eps, void* stream);
+
 /* Describes the launch a call with these extents would make, without
  * launching: kernel (1 CUDA-core, 2 tensor-core), CTAs per (row, kv head)
  * along the selection, total CTAs and split-K workspace bytes.  dtype is the

@@ -71,6 +71,8 @@ def load_library():
     lib.qsa_msa_attention_ragged_paged.argtypes = [T, T, T, T, i64, T, T, u32, u32, u32, T, ctypes.c_float, i32, P,
                                                    ctypes.POINTER(qsa_options)]
     lib.qsa_msa_attention_ragged_paged.restype = ctypes.c_int
+    lib.qsa_compress_keys_paged.argtypes = [T, T, T, T, T, i64, T, T, u32, u32, u32, i32, i32, ctypes.c_float, P]
+    lib.qsa_compress_keys_paged.restype = ctypes.c_int
     lib.qsa_plan.argtypes = [i32, i64, i64, i64, i64, i32, ctypes.POINTER(qsa_options), ctypes.POINTER(i32),
                              ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_size_t)]
     lib.qsa_plan.restype = ctypes.c_int
@@ -195,6 +197,25 @@ def qsa_msa_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, page
         int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length),
         int(max_cache_length), int(layer_idx), _contig(d_indices, "d_indices"), float(scale), int(group),
         ctypes.c_void_p(stream), ctypes.byref(opt)))
+
+
+def qsa_compress_keys_paged(block_keys, gamma, freqs_cis, key_counts, kv_blocks, page_stride, cache_lengths,
+                            kv_lookup_table, max_prompt_length, max_cache_length, layer_idx, ratio, rotary_dim, eps,
+                            stream=None) -> None:
+    """Block-key compression on the GPU (see qsa.h): ``block_keys``
+    [batch * max_blocks, head_dim] from the raw keys in ``kv_blocks``."""
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(kv_blocks.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    if key_counts.dtype != torch.int32:
+        raise TypeError("key_counts must be int32")
+    _check(lib.qsa_compress_keys_paged(
+        _contig(block_keys, "block_keys"), _contig(gamma, "gamma"), _contig(freqs_cis, "freqs_cis"),
+        _contig(key_counts, "key_counts"), _kv_desc(kv_blocks, int(page_stride)), int(page_stride),
+        _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length), int(max_cache_length), int(layer_idx),
+        int(ratio), int(rotary_dim), float(eps), ctypes.c_void_p(stream)))
 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,

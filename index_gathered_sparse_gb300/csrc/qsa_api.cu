@@ -554,6 +554,101 @@ qsa_status qsa_msa_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_t
                         stream, dev);
 }
 
+qsa_status qsa_compress_keys_paged(qsa_tensor block_keys, qsa_tensor gamma, qsa_tensor freqs_cis,
+                                   qsa_tensor key_counts, qsa_tensor kv_blocks, int64_t page_stride,
+                                   qsa_tensor cache_lengths, qsa_tensor kv_lookup_table, uint32_t max_prompt_length,
+                                   uint32_t max_cache_length, uint32_t layer_idx, int32_t ratio, int32_t rotary_dim,
+                                   float eps, void* stream) {
+  (void)max_prompt_length;
+  (void)max_cache_length;
+  struct {
+    const qsa_tensor* t;
+    int ndim;
+    const char* name;
+  } ranks[] = {{&block_keys, 2, "block_keys"}, {&gamma, 1, "gamma"}, {&freqs_cis, 2, "freqs_cis"},
+               {&key_counts, 1, "key_counts"}, {&kv_blocks, 6, "kv_blocks"}, {&cache_lengths, 1, "cache_lengths"},
+               {&kv_lookup_table, 2, "kv_lookup_table"}};
+  for (auto& x : ranks) {
+    if (x.t->ndim != x.ndim)
+      return fail(QSA_ERR_SHAPE, std::string(x.name) + ": rank " + std::to_string(x.t->ndim) + ", expected " +
+                                     std::to_string(x.ndim));
+    for (int i = 0; i < x.ndim; ++i)
+      if (x.t->shape[i] < 0) return fail(QSA_ERR_SHAPE, std::string(x.name) + ": negative extent");
+  }
+  if (kv_blocks.dtype != QSA_F32 && kv_blocks.dtype != QSA_BF16)
+    return fail(QSA_ERR_DTYPE, "kv_blocks: the keys must be F32 or BF16");
+  if (block_keys.dtype != kv_blocks.dtype || gamma.dtype != kv_blocks.dtype)
+    return fail(QSA_ERR_DTYPE, "block_keys and gamma must have the keys' element type");
+  if (freqs_cis.dtype != QSA_F32 && freqs_cis.dtype != QSA_BF16) return fail(QSA_ERR_DTYPE, "freqs_cis: F32 or BF16");
+  if (key_counts.dtype != QSA_I32) return fail(QSA_ERR_DTYPE, "key_counts: element type must be I32");
+  if (cache_lengths.dtype != QSA_U32 || kv_lookup_table.dtype != QSA_U32)
+    return fail(QSA_ERR_DTYPE, "cache_lengths and kv_lookup_table must be U32");
+  const int64_t batch = key_counts.shape[0], D = kv_blocks.shape[5], L = kv_blocks.shape[2], P = kv_blocks.shape[3];
+  if (kv_blocks.shape[1] != 2) return fail(QSA_ERR_SHAPE, "kv_blocks: axis 1 must have extent 2 (K, V)");
+  if (kv_blocks.shape[4] != 1) return fail(QSA_ERR_SHAPE, "kv_blocks: the index-key cache has one head (axis 4 == 1)");
+  if (block_keys.shape[1] != D || gamma.shape[0] != D) return fail(QSA_ERR_SHAPE, "block_keys / gamma: head_dim differs from kv_blocks");
+  if (cache_lengths.shape[0] != batch || kv_lookup_table.shape[0] != batch)
+    return fail(QSA_ERR_SHAPE, "cache_lengths / kv_lookup_table: first extent must be batch");
+  if (batch == 0 ? block_keys.shape[0] != 0 : block_keys.shape[0] % batch != 0)
+    return fail(QSA_ERR_SHAPE, "block_keys: rows must be batch * max_blocks");
+  const int64_t max_blocks = batch ? block_keys.shape[0] / batch : 0;
+  if (ratio < 1) return fail(QSA_ERR_ARG, "ratio must be >= 1");
+  if (rotary_dim < 0 || rotary_dim > D || (rotary_dim & 1)) return fail(QSA_ERR_ARG, "rotary_dim must be even and <= head_dim");
+  if (rotary_dim > 0 && freqs_cis.shape[1] != rotary_dim) return fail(QSA_ERR_SHAPE, "freqs_cis: second extent must be rotary_dim");
+  if (rotary_dim > 0 && freqs_cis.shape[0] < max_blocks)
+    return fail(QSA_ERR_SHAPE, "freqs_cis: needs a row per block (positions >= max_blocks)");
+  if (!(eps >= 0.f)) return fail(QSA_ERR_ARG, "eps must be >= 0");
+  if ((int64_t)layer_idx >= L) return fail(QSA_ERR_ARG, "layer_idx >= num_layers");
+  const int eb = elem_bytes(kv_blocks.dtype);
+  const int64_t packed = 2 * L * P * D;
+  if (page_stride != -1 && page_stride < packed) return fail(QSA_ERR_ARG, "page_stride must be -1 or >= the packed page size");
+  const int64_t pitch = page_stride == -1 ? packed : page_stride;
+  if (D != 128 && D != 256) return fail(QSA_ERR_UNSUPPORTED, "head_dim must be 128 or 256");
+  if ((pitch * eb) % 16) return fail(QSA_ERR_UNSUPPORTED, "page_stride * element size must be a multiple of 16 bytes");
+  const int64_t rows = block_keys.shape[0];
+  if (rows > 0 && (!block_keys.data || !gamma.data || !key_counts.data || (!kv_lookup_table.data && numel(kv_lookup_table)) ||
+                   (!kv_blocks.data && numel(kv_blocks)) || (rotary_dim > 0 && !freqs_cis.data)))
+    return fail(QSA_ERR_NULL, "a needed pointer is NULL");
+  if (!aligned16(block_keys.data) || !aligned16(gamma.data) || !aligned16(kv_blocks.data))
+    return fail(QSA_ERR_UNSUPPORTED, "block_keys, gamma and kv_blocks must be 16-byte aligned");
+  if (rows > 0x7FFFFFFF || kv_blocks.shape[0] > 0xFFFFFFFFLL || kv_lookup_table.shape[1] > 0x7FFFFFFF)
+    return fail(QSA_ERR_UNSUPPORTED, "an extent exceeds the supported range");
+  if (rows == 0) return QSA_OK;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  qsa::CompressParams p;
+  std::memset(&p, 0, sizeof(p));
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    qsa_status s = ensure_status(g_dev[dev]);
+    if (s != QSA_OK) return s;
+    p.status = g_dev[dev].status;
+  }
+  p.out = static_cast<unsigned char*>(block_keys.data);
+  p.gamma = static_cast<const unsigned char*>(gamma.data);
+  p.freqs = static_cast<const unsigned char*>(freqs_cis.data);
+  p.key_counts = static_cast<const int32_t*>(key_counts.data);
+  p.kv = static_cast<const unsigned char*>(kv_blocks.data);
+  p.table = static_cast<const uint32_t*>(kv_lookup_table.data);
+  p.page_pitch_bytes = pitch * eb;
+  p.k_layer_bytes = (int64_t)layer_idx * P * D * eb;
+  p.slot_bytes = D * eb;
+  p.batch = (int32_t)batch;
+  p.max_blocks = (int32_t)max_blocks;
+  p.max_pages = (int32_t)kv_lookup_table.shape[1];
+  p.P = (int32_t)P;
+  p.ratio = ratio;
+  p.rotary_dim = rotary_dim;
+  p.num_pages = (uint32_t)kv_blocks.shape[0];
+  p.eps = eps;
+  e = qsa::launch_compress(p, kv_blocks.dtype == QSA_BF16 ? qsa::kBF16 : qsa::kF32,
+                           freqs_cis.dtype == QSA_BF16 ? qsa::kBF16 : qsa::kF32, (int)D, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return QSA_OK;
+}
+
 qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
                     int64_t selection_width, int32_t group, const qsa_options* options, int32_t* kernel,
                     int32_t* splits, int64_t* ctas, size_t* workspace_bytes) {

@@ -71,6 +71,22 @@ enum Elem { kF32 = 0, kBF16 = 1, kE4M3 = 2 };
 cudaError_t launch_simt(const Params& p, int elem, cudaStream_t stream);
 cudaError_t launch_mma_bf16(const Params& p, cudaStream_t stream);
 cudaError_t launch_mma_e4m3(const Params& p, cudaStream_t stream);
+// Block-key compression (one warp per output row).
+struct CompressParams {
+  unsigned char* out;              // [batch * max_blocks, head_dim], key element type
+  const unsigned char* gamma;      // [head_dim]
+  const unsigned char* freqs;      // [positions, rotary_dim]
+  const int32_t* key_counts;       // [batch]
+  const unsigned char* kv;         // kv_blocks base (one kv head)
+  const uint32_t* table;           // [batch, max_pages]
+  uint32_t* status;                // device status word
+  int64_t page_pitch_bytes, k_layer_bytes, slot_bytes;
+  int32_t batch, max_blocks, max_pages, P, ratio, rotary_dim;
+  uint32_t num_pages;
+  float eps;
+};
+cudaError_t launch_compress(const CompressParams& p, int elem, int freq_elem, int head_dim, cudaStream_t stream);
+
 cudaError_t launch_stream_bf16(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_e4m3(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_bf16_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);

@@ -777,3 +777,29 @@ def compress_small_variants() -> dict:
             compress_bf16(seed=20, batch=4, count_range=(3, 200), ratio=3, name="compress_f32_small"),
             dtype="f32", rotary_dim=128, page_size=16, page_pad=64),
     }
+
+
+def to_torch_compress(x: CompressInputs, device) -> dict:
+    """Uploads a block-key compression call: the keyword arguments of
+    ``binding.qsa_compress_keys_paged`` (block_keys freshly allocated)."""
+    import torch
+
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16}
+
+    def raw(a: np.ndarray, dtype: str):
+        a = np.ascontiguousarray(a)
+        if dtype == "f32":
+            return torch.from_numpy(a.astype(np.float32, copy=False))
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+    c = x.cache
+    d = to_torch(c, device)
+    return dict(
+        block_keys=torch.empty((x.batch * x.max_blocks, x.head_dim), dtype=tdt[x.dtype], device=device),
+        gamma=raw(x.gamma, x.dtype).to(device),
+        freqs_cis=raw(x.freqs_cis, x.freq_dtype).to(device),
+        key_counts=torch.from_numpy(np.ascontiguousarray(x.key_counts, dtype=np.int32)).to(device),
+        kv_blocks=d["kv_blocks"], page_stride=c.page_stride, cache_lengths=d["cache_lengths"],
+        kv_lookup_table=d["kv_lookup_table"], max_prompt_length=0, max_cache_length=c.max_cache_length,
+        layer_idx=c.layer_idx, ratio=x.ratio, rotary_dim=x.rotary_dim, eps=x.eps,
+    )
