@@ -246,9 +246,125 @@ def workload_config(x) -> dict:
     return cfg
 
 
+def run_compress(args, spec, rank, world, local):
+    """Block-key compression (QSACompressKeysPaged) on the GPU or, for the
+    reference arm, in the float64 oracle on one host core."""
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    x = spec.build()
+    metric, unit = "block-key compression rows/s; effective HBM GB/s", "block-key rows/s"
+    rows = x.batch * x.max_blocks
+    cfg = {"workload": x.name, "batch": x.batch, "max_blocks": x.max_blocks, "head_dim": x.head_dim,
+           "ratio": x.ratio, "rotary_dim": x.rotary_dim, "page_size": x.cache.kv_shape[3], "dtype": x.dtype,
+           "raw_keys": int(x.key_counts.clip(0).sum()),
+           "l2": "flushed before every timed step (2x L2 buffer written, then a second 2x L2 buffer read)"}
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+
+        oracle.build()
+        oracle.compress_keys(x)
+        t0 = time.perf_counter()
+        for _ in range(max(1, min(args.steps, 3))):
+            oracle.compress_keys(x)
+        n = max(1, min(args.steps, 3))
+        el = (time.perf_counter() - t0) / n
+        line = {"impl": "reference", "metric": metric, "value": rows / el, "unit": unit, "n_gpus": world,
+                "steps": n, "warmup": 1, "ms_per_step": el * 1e3, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded numpy)", "config": cfg,
+                "cpu_baseline": {"value": rows / el, "unit": unit, "cores": 1, "kind": "oracle",
+                                 "sample": f"the whole {x.name} call per step"},
+                "e2e": {"value": rows / el, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    import torch
+
+    from index_gathered_sparse_gb300 import binding as B
+    from index_gathered_sparse_gb300 import build as libbuild
+
+    libbuild.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    d = wl.to_torch_compress(x, dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(None)
+    t0, n_warm = time.perf_counter(), 0
+    while n_warm < max(3, args.warmup) or time.perf_counter() - t0 < args.min_warmup_s:
+        flush_w.fill_(n_warm & 0xFF)
+        flush_r.sum()
+        B.qsa_compress_keys_paged(**d)
+        n_warm += 1
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush_w.fill_(i & 0xFF)
+        flush_r.sum()
+        ev[i][0].record(stream)
+        B.qsa_compress_keys_paged(**d)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    per_step = [a.elapsed_time(b) for a, b in ev]
+    clocks = sampler.stop()
+    ms = sum(per_step) / args.steps
+    flags = B.qsa_read_device_status(clear=True)
+    alg = x.algorithmic_bytes()
+    peak, peak_src = measured_peaks()
+    achieved = alg / (ms / 1e3) / 1e9
+    # end to end: counts and page table in from pinned memory, block keys back
+    host = {k: d[k].cpu().pin_memory() for k in ("key_counts", "cache_lengths", "kv_lookup_table")}
+    out_host = torch.empty(d["block_keys"].shape, dtype=d["block_keys"].dtype).pin_memory()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n_e2e = max(3, min(args.steps, 20))
+    e0.record(stream)
+    for _ in range(n_e2e):
+        for k, t in host.items():
+            d[k].copy_(t, non_blocking=True)
+        B.qsa_compress_keys_paged(**d)
+        out_host.copy_(d["block_keys"], non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    te = e0.elapsed_time(e1) / n_e2e
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+
+        oracle.build()
+        t1 = time.perf_counter()
+        oracle.compress_keys(x)
+        el = time.perf_counter() - t1
+        cpu = {"value": rows / el, "unit": unit, "cores": 1, "kind": "oracle",
+               "sample": f"the whole {x.name} call ({rows} rows) in {el:.1f}s, one thread"}
+    line = {
+        "metric": metric, "value": rows / (ms / 1e3), "unit": unit, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": sorted(per_step)[len(per_step) // 2],
+        "ms_per_step_min": min(per_step), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": x.dtype, "data": "synthetic (seeded numpy)", "config": cfg, "effective_gbs": achieved,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": recorded_traffic(x.name), "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs copy)",
+                     "kernel": "qsa compress_kernel", "algorithmic_bytes_per_launch": alg},
+        "cpu_baseline": cpu,
+        "e2e": {"value": rows / (te / 1e3), "unit": unit,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+                "d2h_bytes_per_step": out_host.numel() * out_host.element_size(), "steps": n_e2e},
+        "gpu_launches": args.steps, "clocks": clocks, "device_status": flags,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    if args.workload in wl.COMPRESS_WORKLOADS:
+        spec = wl.COMPRESS_WORKLOADS[args.workload]()
+        if world > 1:
+            spec.seed += 100 * rank
+        run_compress(args, spec, rank, world, local)
+        return
     import numpy as np  # noqa: F401
 
     from index_gathered_sparse_gb300 import workloads as wl

@@ -215,7 +215,7 @@ QSA_API qsa_status qsa_msa_attention_ragged_paged(
  *   page_stride, cache_lengths [batch] U32 (shape-checked only),
  *   kv_lookup_table, max_prompt_length, max_cache_length, layer_idx as for
  *   qsa_sparse_attention_ragged_paged
- *   ratio            raw keys per block (>= 1)
+ *   ratio            raw keys per block (1 .. 64)
  *   rotary_dim       channels the rotation covers (even, <= head_dim)
  *   eps              RMS-norm epsilon (>= 0)
  *

@@ -593,6 +593,7 @@ qsa_status qsa_compress_keys_paged(qsa_tensor block_keys, qsa_tensor gamma, qsa_
     return fail(QSA_ERR_SHAPE, "block_keys: rows must be batch * max_blocks");
   const int64_t max_blocks = batch ? block_keys.shape[0] / batch : 0;
   if (ratio < 1) return fail(QSA_ERR_ARG, "ratio must be >= 1");
+  if (ratio > 64) return fail(QSA_ERR_UNSUPPORTED, "ratio above 64 (a CTA stages at most 64 raw keys)");
   if (rotary_dim < 0 || rotary_dim > D || (rotary_dim & 1)) return fail(QSA_ERR_ARG, "rotary_dim must be even and <= head_dim");
   if (rotary_dim > 0 && freqs_cis.shape[1] != rotary_dim) return fail(QSA_ERR_SHAPE, "freqs_cis: second extent must be rotary_dim");
   if (rotary_dim > 0 && freqs_cis.shape[0] < max_blocks)

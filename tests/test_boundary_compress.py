@@ -53,6 +53,7 @@ CASES = {
     "gamma_dtype": (dict(gamma=_t((128,), B.QSA_F32)), 3),
     "counts_dtype": (dict(key_counts=_t((3,), B.QSA_U32)), 3),
     "ratio_zero": (dict(ratio=0), 5),
+    "ratio_above_64": (dict(ratio=65), 4),
     "rotary_odd": (dict(rotary_dim=63, freqs_cis=_t((10, 63), B.QSA_F32)), 5),
     "rotary_too_wide": (dict(rotary_dim=130, freqs_cis=_t((10, 130), B.QSA_F32)), 5),
     "layer_out_of_range": (dict(layer_idx=2), 5),
