@@ -803,3 +803,141 @@ def to_torch_compress(x: CompressInputs, device) -> dict:
         kv_lookup_table=d["kv_lookup_table"], max_prompt_length=0, max_cache_length=c.max_cache_length,
         layer_idx=c.layer_idx, ratio=x.ratio, rotary_dim=x.rotary_dim, eps=x.eps,
     )
+
+
+# ----------------------------------------------------------------------------
+# latent sparse attention: sliding window + listed compressed entries + sinks
+# ----------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class LatentInputs:
+    """One latent sparse attention call: ``swa`` holds q, the row offsets and
+    the token-paged window cache (one latent head); ``comp`` the entry-paged
+    compressed cache (its cache_lengths = entries per sequence)."""
+
+    name: str
+    swa: QSAInputs
+    comp: QSAInputs
+    comp_indices: np.ndarray  # [total_q, num_comp] int32, -1 = unused
+    attn_sink: np.ndarray     # [num_heads] float32
+    window: int
+
+    @property
+    def dtype(self) -> str:
+        return self.swa.dtype
+
+    @property
+    def total_q(self) -> int:
+        return self.swa.total_q
+
+    @property
+    def num_heads(self) -> int:
+        return self.swa.num_q_heads
+
+    def query_positions(self) -> np.ndarray:
+        x = self.swa
+        seq = x.row_sequence()
+        off = x.input_row_offsets.astype(np.int64)
+        return x.cache_lengths.astype(np.int64)[seq] + np.arange(x.total_q) - off[seq]
+
+    def attended_keys(self) -> np.ndarray:
+        pos = self.query_positions()
+        win = np.minimum(pos + 1, self.window)
+        return win + (self.comp_indices >= 0).sum(axis=1)
+
+    def algorithmic_bytes(self) -> int:
+        """Each attended K and V row once per row (one latent head), q, the
+        output, the entry lists and the sinks."""
+        x = self.swa
+        e, eo = ELEM_BYTES[x.dtype], ELEM_BYTES[x.out_dtype]
+        D = x.head_dim
+        n = int(self.attended_keys().sum())
+        return (n * 2 * D * e + x.total_q * x.num_q_heads * D * (e + eo) + self.comp_indices.size * 4
+                + self.attn_sink.size * 4)
+
+
+@dataclasses.dataclass
+class LatentSpec:
+    name: str
+    seed: int
+    rows: Sequence[int]
+    cache_lengths: Sequence[int]
+    num_heads: int
+    window: int
+    num_comp: int
+    comp_ratio: int = 4       # compressed entries per sequence = (cache + rows) // comp_ratio
+    head_dim: int = 128
+    page_size: int = 64
+    comp_page_size: int = 64
+    num_layers: int = 1
+    layer_idx: int = 0
+    dtype: str = "bf16"
+    out_dtype: str = "bf16"
+
+    def build(self, keep_logical: bool = False) -> LatentInputs:
+        rng = np.random.default_rng(self.seed)
+        B = len(self.rows)
+        rows = np.asarray(self.rows, dtype=np.int64)
+        cache = np.asarray(self.cache_lengths, dtype=np.int64)
+        H, D = self.num_heads, self.head_dim
+        kv_len = cache + rows
+        n_comp = kv_len // self.comp_ratio
+        total_q = int(rows.sum())
+        q = encode(rng.standard_normal((total_q, H, D), dtype=np.float32), self.dtype)
+        lk = [encode(rng.standard_normal((int(n), 1, D), dtype=np.float32), self.dtype) for n in kv_len]
+        lv = [encode(rng.standard_normal((int(n), 1, D), dtype=np.float32), self.dtype) for n in kv_len]
+        ck = [encode(rng.standard_normal((int(n), 1, D), dtype=np.float32), self.dtype) for n in n_comp]
+        cv = [encode(rng.standard_normal((int(n), 1, D), dtype=np.float32), self.dtype) for n in n_comp]
+        idx = np.full((total_q, self.num_comp), -1, dtype=np.int32)
+        seq = np.repeat(np.arange(B), rows)
+        for r in range(total_q):
+            n = int(n_comp[seq[r]])
+            k = min(self.num_comp, n)
+            if k:
+                idx[r, :k] = rng.choice(n, size=k, replace=False)
+        sink = rng.standard_normal(H).astype(np.float32)
+        swa = assemble(self.name, self.dtype, self.out_dtype, q, lk, lv, rows, cache, self.page_size,
+                       self.num_layers, self.layer_idx, np.zeros((total_q, 0), np.int32),
+                       np.zeros(total_q, np.int32), 1.0 / math.sqrt(D),
+                       page_perm=rng.permutation(int((-(-kv_len // self.page_size)).sum())), keep_logical=keep_logical)
+        comp = assemble(self.name + "_comp", self.dtype, self.out_dtype, np.zeros((0, H, D), q.dtype), ck, cv,
+                        [0] * B, n_comp, self.comp_page_size, self.num_layers, self.layer_idx,
+                        np.zeros((0, 0), np.int32), np.zeros(0, np.int32), 1.0,
+                        page_perm=rng.permutation(int((-(-n_comp // self.comp_page_size)).sum())),
+                        keep_logical=keep_logical)
+        return LatentInputs(name=self.name, swa=swa, comp=comp, comp_indices=idx, attn_sink=sink, window=self.window)
+
+
+def latent_bf16_decode(seed: int = 10, batch: int = 64, cache_range=(2048, 32768), num_heads: int = 16,
+                       window: int = 128, num_comp: int = 512, name: str = "latent_bf16_decode") -> LatentSpec:
+    """Latent sparse attention, bf16 decode: 64 x 1 row, cache U[2048, 32768],
+    16 query heads on one latent head of 128, window 128 tokens, 512 listed
+    compressed entries of (kv_len // 4) per sequence, per-head sinks."""
+    rng = np.random.default_rng(seed + 1000)
+    cache = rng.integers(cache_range[0], cache_range[1] + 1, size=batch)
+    return LatentSpec(name=name, seed=seed, rows=[1] * batch, cache_lengths=cache.tolist(), num_heads=num_heads,
+                      window=window, num_comp=num_comp)
+
+
+def latent_bf16_prefill(seed: int = 11, rows=(256, 512, 128), cache=(0, 2048, 8192), num_heads: int = 64,
+                        window: int = 128, num_comp: int = 256, name: str = "latent_bf16_prefill") -> LatentSpec:
+    """Latent sparse attention, bf16 chunked prefill: rows [256,512,128] on
+    cache [0,2048,8192], 64 query heads (four groups of 16 on the one latent
+    head), window 128, 256 listed compressed entries, per-head sinks."""
+    return LatentSpec(name=name, seed=seed, rows=list(rows), cache_lengths=list(cache), num_heads=num_heads,
+                      window=window, num_comp=num_comp)
+
+
+LATENT_WORKLOADS = {"latent_bf16_decode": latent_bf16_decode, "latent_bf16_prefill": latent_bf16_prefill}
+
+
+def latent_small_variants() -> dict:
+    return {
+        "latent_bf16_decode_small": latent_bf16_decode(seed=21, batch=5, cache_range=(40, 700), window=48,
+                                                       num_comp=40, name="latent_bf16_decode_small"),
+        "latent_bf16_prefill_small": latent_bf16_prefill(seed=22, rows=(17, 30, 5), cache=(0, 90, 300), num_heads=32,
+                                                         window=24, num_comp=30, name="latent_bf16_prefill_small"),
+        "latent_fp8_small": dataclasses.replace(
+            latent_bf16_decode(seed=23, batch=4, cache_range=(100, 900), window=64, num_comp=24, num_heads=8,
+                               name="latent_fp8_small"), dtype="e4m3", page_size=32, comp_page_size=16),
+    }

@@ -4,5 +4,5 @@ TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the bench's
 CPU-baseline leg use it to check and time the CUDA path.  The product library
 never imports it, and it imports nothing from the product package.
 """
-from .oracle import (ORACLE_DTYPES, OracleError, build, compress_keys, decode, load, msa_attention,  # noqa: F401
-                     sparse_attention)
+from .oracle import (ORACLE_DTYPES, OracleError, build, compress_keys, decode, latent_attention,  # noqa: F401
+                     load, msa_attention, sparse_attention)

@@ -81,6 +81,18 @@ def load():
             p, i64, i64, i64,
             ctypes.c_double,
         ]
+        lib.qsa_oracle_latent_attention.restype = ctypes.c_int
+        lib.qsa_oracle_latent_attention.argtypes = [
+            p, p, i64,
+            p, ctypes.c_int, i64, i64, i64,
+            p, i64,
+            p, i64, i64, i64, i64,
+            p, p, i64,
+            p, i64, i64, i64, i64,
+            p, p, i64,
+            i64, p, i64, p,
+            i64, ctypes.c_double, ctypes.POINTER(i64),
+        ]
         lib.qsa_oracle_decode.restype = None
         lib.qsa_oracle_decode.argtypes = [p, p, ctypes.c_int, i64]
         _lib = lib
@@ -185,4 +197,37 @@ def compress_keys(x) -> np.ndarray:
     )
     if code != 0:
         raise OracleError(code, -1)
+    return out
+
+
+def latent_attention(x, rows=None) -> np.ndarray:
+    """float64 latent sparse attention (window + listed compressed entries +
+    sinks) for the query rows ``rows`` (all if None)."""
+    lib = load()
+    a, c = x.swa, x.comp
+    total_q, H, D = a.q.shape
+    rows = np.arange(total_q, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, H, D), dtype=np.float64)
+    keep = []
+
+    def arr(v, dt=None):
+        v = np.ascontiguousarray(v, dtype=dt) if dt is not None else np.ascontiguousarray(v)
+        keep.append(v)
+        return _ptr(v)
+
+    ci = np.ascontiguousarray(x.comp_indices, dtype=np.int32)
+    bad = ctypes.c_int64(-1)
+    code = lib.qsa_oracle_latent_attention(
+        _ptr(out), _ptr(rows), rows.size,
+        arr(a.q), ORACLE_DTYPES[a.dtype], total_q, H, D,
+        arr(a.input_row_offsets, np.uint32), a.batch,
+        arr(a.kv_flat), a.kv_shape[0], int(a.page_stride), a.kv_shape[2], a.kv_shape[3],
+        arr(a.cache_lengths, np.uint32), arr(a.kv_lookup_table, np.uint32), a.kv_lookup_table.shape[1],
+        arr(c.kv_flat), c.kv_shape[0], int(c.page_stride), c.kv_shape[2], c.kv_shape[3],
+        arr(c.cache_lengths, np.uint32), arr(c.kv_lookup_table, np.uint32), c.kv_lookup_table.shape[1],
+        int(a.layer_idx), _ptr(ci), ci.shape[1], arr(x.attn_sink, np.float32),
+        int(x.window), float(a.scale), ctypes.byref(bad),
+    )
+    if code != 0:
+        raise OracleError(code, bad.value)
     return out

@@ -403,3 +403,130 @@ int qsa_oracle_compress_keys(double* out, int64_t batch, int64_t max_blocks, int
   free(x);
   return ORACLE_OK;
 }
+
+/*
+ * Latent sparse attention: latent_sparse_attention_ragged_paged ("Attends
+ * every query row to its window keys and its listed compressed entries"): a
+ * sliding window of `window` tokens (a query at pos sees positions
+ * max(0, pos - window + 1) .. pos) from a cache paged by token position, the
+ * entries comp_indices[r, :] (-1 marks an unused slot) from a cache paged by
+ * entry, both with one latent head shared by all query heads, and per-head
+ * sink logits attn_sink.
+ *
+ * Readings taken where the page is silent: each cache stores K at axis-1
+ * index 0 and V at index 1 like the paged KV caches of the other ops; the
+ * row's position is swa_cache_lengths[b] + (r - input_row_offsets[b]); a sink
+ * is one more softmax term with logit attn_sink[h] (not scaled) and no value,
+ * so it only enlarges the denominator; a repeated entry counts twice; an
+ * entry at or past comp_cache_lengths[b] is a precondition violation.
+ */
+int qsa_oracle_latent_attention(
+    double* out, const int64_t* rows, int64_t n_rows,
+    const void* q, int dtype, int64_t total_q, int64_t num_heads, int64_t head_dim,
+    const uint32_t* input_row_offsets, int64_t batch,
+    const void* swa_blocks, int64_t swa_pages, int64_t swa_stride, int64_t swa_layers, int64_t swa_page_size,
+    const uint32_t* swa_cache_lengths, const uint32_t* swa_table, int64_t swa_max_pages,
+    const void* comp_blocks, int64_t comp_pages, int64_t comp_stride, int64_t comp_layers, int64_t comp_page_size,
+    const uint32_t* comp_cache_lengths, const uint32_t* comp_table, int64_t comp_max_pages,
+    int64_t layer_idx, const int32_t* comp_indices, int64_t num_comp, const float* attn_sink,
+    int64_t window, double scale, int64_t* bad_row) {
+  int64_t swa_pitch, comp_pitch, ri, cap;
+  double* s;
+  int64_t* koff;
+  int* src;
+
+  *bad_row = -1;
+  if (dtype < 0 || dtype > 2 || window < 0 || num_comp < 0) return ORACLE_BAD_ARGUMENT;
+  if (layer_idx < 0 || layer_idx >= swa_layers || layer_idx >= comp_layers) return ORACLE_BAD_ARGUMENT;
+  swa_pitch = swa_stride == -1 ? 2 * swa_layers * swa_page_size * head_dim : swa_stride;
+  comp_pitch = comp_stride == -1 ? 2 * comp_layers * comp_page_size * head_dim : comp_stride;
+  cap = window + num_comp > 0 ? window + num_comp : 1;
+  s = (double*)malloc(sizeof(double) * (size_t)cap);
+  koff = (int64_t*)malloc(sizeof(int64_t) * (size_t)cap);
+  src = (int*)malloc(sizeof(int) * (size_t)cap);
+  if (!s || !koff || !src) {
+    free(s);
+    free(koff);
+    free(src);
+    return ORACLE_NO_MEMORY;
+  }
+  for (ri = 0; ri < n_rows; ++ri) {
+    int64_t r = rows[ri], b = -1, k, pos, n = 0, p, e, h, d, j;
+    if (r < 0 || r >= total_q) goto lat_bad_row;
+    for (k = 0; k < batch; ++k)
+      if ((int64_t)input_row_offsets[k] <= r && r < (int64_t)input_row_offsets[k + 1]) {
+        b = k;
+        break;
+      }
+    if (b < 0) goto lat_bad_row;
+    pos = (int64_t)swa_cache_lengths[b] + (r - (int64_t)input_row_offsets[b]);
+    /* window keys, oldest first */
+    for (p = pos - window + 1; p <= pos; ++p) {
+      int64_t lp, page;
+      if (p < 0) continue;
+      lp = p / swa_page_size;
+      if (lp >= swa_max_pages) goto lat_bad_page;
+      page = (int64_t)swa_table[b * swa_max_pages + lp];
+      if (page >= swa_pages) goto lat_bad_page;
+      koff[n] = page * swa_pitch + ((0 * swa_layers + layer_idx) * swa_page_size + p % swa_page_size) * head_dim;
+      src[n++] = 0;
+    }
+    /* listed compressed entries */
+    for (k = 0; k < num_comp; ++k) {
+      int64_t lp, page;
+      e = comp_indices[r * num_comp + k];
+      if (e < 0) continue;
+      if (e >= (int64_t)comp_cache_lengths[b]) {
+        *bad_row = r;
+        free(s);
+        free(koff);
+        free(src);
+        return ORACLE_INDEX_OUT_OF_RANGE;
+      }
+      lp = e / comp_page_size;
+      if (lp >= comp_max_pages) goto lat_bad_page;
+      page = (int64_t)comp_table[b * comp_max_pages + lp];
+      if (page >= comp_pages) goto lat_bad_page;
+      koff[n] = page * comp_pitch + ((0 * comp_layers + layer_idx) * comp_page_size + e % comp_page_size) * head_dim;
+      src[n++] = 1;
+    }
+    for (h = 0; h < num_heads; ++h) {
+      int64_t q_off = (r * num_heads + h) * head_dim;
+      double* o = out + (ri * num_heads + h) * head_dim;
+      double m = (double)attn_sink[h], z;
+      for (d = 0; d < head_dim; ++d) o[d] = 0.0;
+      for (j = 0; j < n; ++j) {
+        const void* base = src[j] ? comp_blocks : swa_blocks;
+        double dot = 0.0;
+        for (d = 0; d < head_dim; ++d) dot += decode(dtype, q, q_off + d) * decode(dtype, base, koff[j] + d);
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+      }
+      z = exp((double)attn_sink[h] - m); /* the sink: denominator only */
+      for (j = 0; j < n; ++j) z += exp(s[j] - m);
+      for (j = 0; j < n; ++j) {
+        const void* base = src[j] ? comp_blocks : swa_blocks;
+        int64_t v_off = koff[j] + (src[j] ? comp_layers * comp_page_size : swa_layers * swa_page_size) * head_dim;
+        double a = exp(s[j] - m) / z;
+        for (d = 0; d < head_dim; ++d) o[d] += a * decode(dtype, base, v_off + d);
+      }
+    }
+    continue;
+  lat_bad_page:
+    *bad_row = r;
+    free(s);
+    free(koff);
+    free(src);
+    return ORACLE_BAD_PAGE;
+  lat_bad_row:
+    *bad_row = r;
+    free(s);
+    free(koff);
+    free(src);
+    return ORACLE_BAD_ROW;
+  }
+  free(s);
+  free(koff);
+  free(src);
+  return ORACLE_OK;
+}
