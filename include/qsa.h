@@ -201,6 +201,54 @@ QSA_API qsa_status qsa_msa_attention_ragged_paged(
     qsa_tensor d_indices, float scale, int32_t group, void* stream, const qsa_options* options);
 
 /*
+ * qsa_latent_attention_ragged_paged - latent sparse attention: every query
+ * row attends its sliding window and its listed compressed entries, with
+ * per-head sinks (MAX page "latent_sparse_attention_ragged_paged": "Attends
+ * every query row to its window keys and its listed compressed entries"; its
+ * window, comp_indices, attn_sink and two-cache parameters).
+ *
+ *   output, q           [total_q, num_heads, 128]  (BF16 or F8E4M3 q; output F32/BF16)
+ *   input_row_offsets   [batch + 1] U32
+ *   swa_blocks          [pages, 2, num_layers, page_size, 1, 128]: the window
+ *                       cache, paged by token position (swa_page_stride,
+ *                       swa_cache_lengths [batch] U32: the row position is
+ *                       swa_cache_lengths[b] + (r - input_row_offsets[b]),
+ *                       swa_lookup_table [batch, max_pages] U32)
+ *   comp_blocks         [pages2, 2, num_layers2, page_size2, 1, 128]: the
+ *                       compressed cache, paged by entry (comp_page_stride)
+ *   comp_cache_lengths  DEVICE pointer, [batch] U32 entries per sequence
+ *   comp_lookup_table   DEVICE pointer, [batch, comp_max_pages] U32
+ *   layer_idx           layer of both caches
+ *   comp_indices        DEVICE pointer, [total_q, num_comp] I32 entry ids,
+ *                       -1 = unused slot
+ *   attn_sink           DEVICE pointer, [num_heads] F32 sink logits
+ * (the per-row and per-sequence arrays of the compressed cache are plain
+ * pointers with their extents given alongside, so that no descriptor is
+ * passed after the eighth argument register)
+ *   window              tokens: a row at pos sees positions max(0, pos -
+ *                       window + 1) .. pos
+ *
+ * For query head h of row r: softmax over the scores scale * q.K of the
+ * window keys and the listed entries plus one extra term attn_sink[h] that
+ * has no value, then the weighted sum of V.  Readings where the page is
+ * silent: both caches hold K at axis-1 index 0 and V at 1 with one latent
+ * head shared by every query head; the sink logit is not scaled and only
+ * enlarges the denominator; a repeated entry counts twice; an entry at or
+ * past comp_cache_lengths[b] is skipped and sets QSA_STATUS_BAD_INDEX; a row
+ * with nothing attended is zero.  num_heads <= 16 or a multiple of 16 (each
+ * group of 16 query heads is one unit reading the latent head); each cache
+ * below 32 GiB; runs on the per-(row, head group) tensor-core kernel with
+ * split-K (options: kernel 0 or 2, splits).
+ */
+QSA_API qsa_status qsa_latent_attention_ragged_paged(
+    qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor swa_blocks,
+    int64_t swa_page_stride, qsa_tensor swa_cache_lengths, qsa_tensor swa_lookup_table,
+    qsa_tensor comp_blocks, int64_t comp_page_stride, const uint32_t* comp_cache_lengths,
+    const uint32_t* comp_lookup_table, int64_t comp_max_pages, uint32_t layer_idx,
+    const int32_t* comp_indices, int64_t num_comp, const float* attn_sink, int32_t window, float scale,
+    void* stream, const qsa_options* options);
+
+/*
  * qsa_compress_keys_paged - block-key compression of raw QSA index keys
  * (MAX page "QSACompressKeysPaged": "Pools a paged group of raw QSA index
  * keys into dense block keys"; its tensor shapes, its gamma / freqs_cis /

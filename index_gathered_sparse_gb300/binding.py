@@ -73,6 +73,9 @@ def load_library():
     lib.qsa_msa_attention_ragged_paged.restype = ctypes.c_int
     lib.qsa_compress_keys_paged.argtypes = [T, T, T, T, T, i64, T, T, u32, u32, u32, i32, i32, ctypes.c_float, P]
     lib.qsa_compress_keys_paged.restype = ctypes.c_int
+    lib.qsa_latent_attention_ragged_paged.argtypes = [T, T, T, T, i64, T, T, T, i64, P, P, i64, u32, P, i64, P,
+                                                      i32, ctypes.c_float, P, ctypes.POINTER(qsa_options)]
+    lib.qsa_latent_attention_ragged_paged.restype = ctypes.c_int
     lib.qsa_plan.argtypes = [i32, i64, i64, i64, i64, i32, ctypes.POINTER(qsa_options), ctypes.POINTER(i32),
                              ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_size_t)]
     lib.qsa_plan.restype = ctypes.c_int
@@ -216,6 +219,39 @@ def qsa_compress_keys_paged(block_keys, gamma, freqs_cis, key_counts, kv_blocks,
         _contig(key_counts, "key_counts"), _kv_desc(kv_blocks, int(page_stride)), int(page_stride),
         _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length), int(max_cache_length), int(layer_idx),
         int(ratio), int(rotary_dim), float(eps), ctypes.c_void_p(stream)))
+
+
+def qsa_latent_attention_ragged_paged(output, q, input_row_offsets, swa_blocks, swa_page_stride, swa_cache_lengths,
+                                      swa_lookup_table, comp_blocks, comp_page_stride, comp_cache_lengths,
+                                      comp_lookup_table, layer_idx, comp_indices, attn_sink, window, scale,
+                                      stream=None, *, splits: int = 0) -> None:
+    """Latent sparse attention on the GPU: sliding window + listed compressed
+    entries + per-head sinks (see qsa.h).  The compressed cache's lengths,
+    page table and entry lists and the sinks go across as plain pointers."""
+    lib = load_library()
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device).cuda_stream
+    elif isinstance(stream, torch.cuda.Stream):
+        stream = stream.cuda_stream
+    checks = ((comp_cache_lengths, (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ()), 1),
+              (comp_lookup_table, (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ()), 2),
+              (comp_indices, (torch.int32,), 2), (attn_sink, (torch.float32,), 1))
+    for t, dts, nd in checks:
+        if t.dtype not in dts or t.dim() != nd or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError("comp_cache_lengths, comp_lookup_table, comp_indices and attn_sink must be contiguous "
+                             "CUDA tensors of 32-bit elements with ranks 1, 2, 2 and 1")
+    if comp_cache_lengths.numel() != swa_cache_lengths.numel() or comp_lookup_table.shape[0] != swa_cache_lengths.numel():
+        raise ValueError("comp_cache_lengths / comp_lookup_table: first extent must be batch")
+    if comp_indices.shape[0] != q.shape[0] or attn_sink.numel() != q.shape[1]:
+        raise ValueError("comp_indices must have total_q rows and attn_sink num_heads entries")
+    opt = qsa_options(kernel=0, splits=splits, ctas=0)
+    ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t.numel() else None)
+    _check(lib.qsa_latent_attention_ragged_paged(
+        _contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets), _kv_desc(swa_blocks, int(swa_page_stride)),
+        int(swa_page_stride), _u32(swa_cache_lengths), _u32(swa_lookup_table), _kv_desc(comp_blocks, int(comp_page_stride)),
+        int(comp_page_stride), ptr(comp_cache_lengths), ptr(comp_lookup_table), int(comp_lookup_table.shape[1]),
+        int(layer_idx), ptr(comp_indices), int(comp_indices.shape[1]), ptr(attn_sink), int(window), float(scale),
+        ctypes.c_void_p(stream), ctypes.byref(opt)))
 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,

@@ -398,11 +398,25 @@ qsa_status ensure_status(DeviceState& st) {
 // Everything after the plan: status word and workspace of (device, stream),
 // the kernel parameters, and the launch.  `indices`/`counts` carry a token
 // selection, or `blocks`/`topk` a block selection (kernel 2 only).
+// The latent mode's second source and sinks (see Params).
+struct LatentArgs {
+  const int32_t* comp;
+  const float* sinks;
+  const unsigned char* kv2;
+  const uint32_t* table2;
+  const uint32_t* cache_lengths2;
+  int64_t pitch_bytes2, k_layer_bytes2, v_minus_k_bytes2, slot_bytes2;
+  int32_t num_comp, window, P2, max_pages2;
+  uint32_t num_pages2;
+  // the window cache has one head whatever the number of query-head groups
+  int64_t k_layer_bytes1, v_minus_k_bytes1, slot_bytes1;
+};
+
 qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tensor& q,
                           const qsa_tensor& input_row_offsets, const qsa_tensor& kv_blocks,
                           const qsa_tensor& cache_lengths, const qsa_tensor& kv_lookup_table, uint32_t layer_idx,
                           const int32_t* indices, const int32_t* counts, const int32_t* blocks, int32_t topk,
-                          float scale, int32_t group, void* stream, int dev) {
+                          float scale, int32_t group, void* stream, int dev, const LatentArgs* lat = nullptr) {
   qsa_status s = QSA_OK;
   cudaError_t e = cudaSuccess;
   Params p;
@@ -454,6 +468,26 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
   p.out_bf16 = R.out_bf16;
   p.splits = R.splits;
   p.band = R.band;
+  if (lat) {
+    p.comp = lat->comp;
+    p.sinks = lat->sinks;
+    p.kv2 = lat->kv2;
+    p.table2 = lat->table2;
+    p.cache_lengths2 = lat->cache_lengths2;
+    p.page_pitch_bytes2 = lat->pitch_bytes2;
+    p.k_layer_bytes2 = lat->k_layer_bytes2;
+    p.v_minus_k_bytes2 = lat->v_minus_k_bytes2;
+    p.slot_bytes2 = lat->slot_bytes2;
+    p.num_comp = lat->num_comp;
+    p.window = lat->window;
+    p.P2 = lat->P2;
+    p.max_pages2 = lat->max_pages2;
+    p.num_pages2 = lat->num_pages2;
+    p.k_layer_bytes = lat->k_layer_bytes1;
+    p.v_minus_k_bytes = lat->v_minus_k_bytes1;
+    p.slot_bytes = lat->slot_bytes1;
+    p.head_bytes = 0;  // every query-head group reads the one latent head
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (R.kernel == 1)
@@ -552,6 +586,120 @@ qsa_status qsa_msa_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_t
   return launch_planned(R, output, q, input_row_offsets, kv_blocks, cache_lengths, kv_lookup_table, layer_idx,
                         nullptr, nullptr, static_cast<const int32_t*>(d_indices.data), (int32_t)topk, scale, group,
                         stream, dev);
+}
+
+qsa_status qsa_latent_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets,
+                                             qsa_tensor swa_blocks, int64_t swa_page_stride,
+                                             qsa_tensor swa_cache_lengths, qsa_tensor swa_lookup_table,
+                                             qsa_tensor comp_blocks, int64_t comp_page_stride,
+                                             const uint32_t* comp_cache_lengths, const uint32_t* comp_lookup_table,
+                                             int64_t comp_max_pages, uint32_t layer_idx, const int32_t* comp_indices,
+                                             int64_t num_comp, const float* attn_sink, int32_t window, float scale,
+                                             void* stream, const qsa_options* options) {
+  struct {
+    const qsa_tensor* t;
+    int ndim;
+    const char* name;
+  } ranks[] = {{&output, 3, "output"}, {&q, 3, "q"}, {&input_row_offsets, 1, "input_row_offsets"},
+               {&swa_blocks, 6, "swa_blocks"}, {&swa_cache_lengths, 1, "swa_cache_lengths"},
+               {&swa_lookup_table, 2, "swa_lookup_table"}, {&comp_blocks, 6, "comp_blocks"}};
+  for (auto& x : ranks) {
+    if (x.t->ndim != x.ndim)
+      return fail(QSA_ERR_SHAPE, std::string(x.name) + ": rank " + std::to_string(x.t->ndim) + ", expected " +
+                                     std::to_string(x.ndim));
+    for (int i = 0; i < x.ndim; ++i)
+      if (x.t->shape[i] < 0) return fail(QSA_ERR_SHAPE, std::string(x.name) + ": negative extent");
+  }
+  if (q.dtype != QSA_BF16 && q.dtype != QSA_F8E4M3) return fail(QSA_ERR_UNSUPPORTED, "q must be BF16 or F8E4M3");
+  if (swa_blocks.dtype != q.dtype || comp_blocks.dtype != q.dtype)
+    return fail(QSA_ERR_DTYPE, "swa_blocks and comp_blocks must have q's element type");
+  if (output.dtype != QSA_F32 && output.dtype != QSA_BF16) return fail(QSA_ERR_DTYPE, "output: F32 or BF16");
+  if (input_row_offsets.dtype != QSA_U32 || swa_cache_lengths.dtype != QSA_U32 || swa_lookup_table.dtype != QSA_U32)
+    return fail(QSA_ERR_DTYPE, "offsets, cache lengths and page tables must be U32");
+  if (comp_max_pages < 0 || num_comp < 0) return fail(QSA_ERR_SHAPE, "comp_max_pages and num_comp must be >= 0");
+  Resolved R;
+  R.elem = q.dtype == QSA_BF16 ? qsa::kBF16 : qsa::kE4M3;
+  R.total_q = q.shape[0];
+  R.nq = q.shape[1];
+  R.D = q.shape[2];
+  R.batch = swa_cache_lengths.shape[0];
+  R.num_pages = swa_blocks.shape[0];
+  R.L = swa_blocks.shape[2];
+  R.P = swa_blocks.shape[3];
+  R.max_pages = swa_lookup_table.shape[1];
+  for (int i = 0; i < 3; ++i)
+    if (output.shape[i] != q.shape[i]) return fail(QSA_ERR_SHAPE, "output: shape differs from q");
+  if (swa_blocks.shape[1] != 2 || comp_blocks.shape[1] != 2) return fail(QSA_ERR_SHAPE, "caches: axis 1 must be 2 (K, V)");
+  if (swa_blocks.shape[4] != 1 || comp_blocks.shape[4] != 1) return fail(QSA_ERR_SHAPE, "caches: one latent head (axis 4 == 1)");
+  if (swa_blocks.shape[5] != R.D || comp_blocks.shape[5] != R.D) return fail(QSA_ERR_SHAPE, "caches: head_dim differs from q");
+  if (input_row_offsets.shape[0] != R.batch + 1) return fail(QSA_ERR_SHAPE, "input_row_offsets: extent must be batch + 1");
+  if (swa_lookup_table.shape[0] != R.batch) return fail(QSA_ERR_SHAPE, "swa_lookup_table: first extent must be batch");
+  if (R.batch == 0 && R.total_q > 0) return fail(QSA_ERR_SHAPE, "query rows without any sequence (batch == 0)");
+  if (window < 0) return fail(QSA_ERR_ARG, "window must be >= 0");
+  if ((int64_t)layer_idx >= R.L || (int64_t)layer_idx >= comp_blocks.shape[2])
+    return fail(QSA_ERR_ARG, "layer_idx >= num_layers of a cache");
+  if (R.P < 1 || comp_blocks.shape[3] < 1) return fail(QSA_ERR_SHAPE, "page sizes must be >= 1");
+  const int64_t eb = elem_bytes(q.dtype), D = R.D, L2 = comp_blocks.shape[2], P2 = comp_blocks.shape[3];
+  const int64_t packed1 = 2 * R.L * R.P * D, packed2 = 2 * L2 * P2 * D;
+  if ((swa_page_stride != -1 && swa_page_stride < packed1) || (comp_page_stride != -1 && comp_page_stride < packed2))
+    return fail(QSA_ERR_ARG, "page_stride must be -1 (packed) or >= the packed page size");
+  R.pitch = swa_page_stride == -1 ? packed1 : swa_page_stride;
+  const int64_t pitch2 = comp_page_stride == -1 ? packed2 : comp_page_stride;
+  if (D != 128) return fail(QSA_ERR_UNSUPPORTED, "head_dim must be 128");
+  // query-head groups of up to 16 on the one latent head
+  const int64_t group = R.nq <= 16 ? R.nq : 16;
+  if (R.nq < 1 || R.nq % group) return fail(QSA_ERR_UNSUPPORTED, "num_heads must be <= 16 or a multiple of 16");
+  R.nkv = R.nq / group;
+  R.W = (int64_t)window + num_comp;
+  R.out_bf16 = output.dtype == QSA_BF16;
+  if (R.W > 0x7FFFFFFF || R.total_q > 0x7FFFFFFF || comp_max_pages > 0x7FFFFFFF)
+    return fail(QSA_ERR_UNSUPPORTED, "an extent exceeds 2^31 - 1");
+  if ((R.pitch * eb) % 16 || (pitch2 * eb) % 16)
+    return fail(QSA_ERR_UNSUPPORTED, "page_stride * element size must be a multiple of 16 bytes");
+  const double kv1 = ((double)(R.num_pages > 0 ? R.num_pages - 1 : 0) * R.pitch + packed1) * eb;
+  const double kv2 = ((double)(comp_blocks.shape[0] > 0 ? comp_blocks.shape[0] - 1 : 0) * pitch2 + packed2) * eb;
+  if (kv1 >= 34359738368.0 - 16.0 || kv2 >= 34359738368.0 - 16.0)
+    return fail(QSA_ERR_UNSUPPORTED, "a cache larger than 32 GiB");
+  if (R.total_q > 0 && (!output.data || !q.data || !input_row_offsets.data || !swa_cache_lengths.data ||
+                        !attn_sink || !comp_cache_lengths || (!comp_indices && num_comp) ||
+                        (!comp_lookup_table && comp_max_pages) ||
+                        (!swa_blocks.data && numel(swa_blocks)) || (!comp_blocks.data && numel(comp_blocks))))
+    return fail(QSA_ERR_NULL, "a needed pointer is NULL");
+  if (!aligned16(output.data) || !aligned16(q.data) || !aligned16(swa_blocks.data) || !aligned16(comp_blocks.data))
+    return fail(QSA_ERR_UNSUPPORTED, "q, output and the caches must be 16-byte aligned");
+  qsa_options opt;
+  std::memset(&opt, 0, sizeof(opt));
+  if (options) opt = *options;
+  if (opt.kernel != 0 && opt.kernel != 2) return fail(QSA_ERR_UNSUPPORTED, "latent attention runs on kernel 2");
+  if (opt.ctas != 0 || opt.splits < 0) return fail(QSA_ERR_ARG, "only options.splits applies");
+  opt.kernel = 2;
+  R.kernel = 2;
+  if (R.total_q == 0) return QSA_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  qsa_status s = plan_launch(R, (int32_t)group, &opt, dev);
+  if (s != QSA_OK) return s;
+  LatentArgs lat;
+  lat.comp = comp_indices;
+  lat.sinks = attn_sink;
+  lat.kv2 = static_cast<const unsigned char*>(comp_blocks.data);
+  lat.table2 = comp_lookup_table;
+  lat.cache_lengths2 = comp_cache_lengths;
+  lat.pitch_bytes2 = pitch2 * eb;
+  lat.k_layer_bytes2 = (int64_t)layer_idx * P2 * D * eb;
+  lat.v_minus_k_bytes2 = L2 * P2 * D * eb;
+  lat.slot_bytes2 = D * eb;
+  lat.num_comp = (int32_t)num_comp;
+  lat.window = window;
+  lat.P2 = (int32_t)P2;
+  lat.max_pages2 = (int32_t)comp_max_pages;
+  lat.num_pages2 = (uint32_t)comp_blocks.shape[0];
+  lat.k_layer_bytes1 = (int64_t)layer_idx * R.P * D * eb;
+  lat.v_minus_k_bytes1 = R.L * R.P * D * eb;
+  lat.slot_bytes1 = D * eb;
+  return launch_planned(R, output, q, input_row_offsets, swa_blocks, swa_cache_lengths, swa_lookup_table, layer_idx,
+                        nullptr, nullptr, nullptr, 0, scale, (int32_t)group, stream, dev, &lat);
 }
 
 qsa_status qsa_compress_keys_paged(qsa_tensor block_keys, qsa_tensor gamma, qsa_tensor freqs_cis,

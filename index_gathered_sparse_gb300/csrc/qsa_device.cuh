@@ -83,6 +83,14 @@ __device__ __forceinline__ void store_out(const Params& p, int64_t idx, float v)
     reinterpret_cast<float*>(p.out)[idx] = v;
 }
 
+// The latent mode's sink of query head `head`, as a denominator term relative
+// to the running max M of the base-2 scores: 2^(sink * log2(e) - M) (0 when
+// there are no sinks).  The sink is one more softmax term without a value.
+__device__ __forceinline__ float sink_term(const Params& p, int head, float M) {
+  if (!p.sinks) return 0.f;
+  return exp2f(__ldg(p.sinks + head) * 1.4426950408889634f - M);
+}
+
 // Finishes one (row r, kv head h) unit from NW per-warp softmax states held in
 // shared memory: sm_m[w*GP + i] (running max of the base-2 scores),
 // sm_l[w*GP + i] (sum of exponentials) and sm_o[(w*GP + i)*D + d]
@@ -113,7 +121,7 @@ __device__ __forceinline__ void finish_unit(const Params& p, int r, int h, int s
           L += sm_l[w * GP + i] * e;
           O += sm_o[(w * GP + i) * D + d] * e;
         }
-        val = O / L;
+        val = O / (L + sink_term(p, h * G + i, M));
       }
       store_out(p, out_base + idx, val);
     }
@@ -173,6 +181,7 @@ __device__ __forceinline__ void finish_unit(const Params& p, int r, int h, int s
     if (M != -CUDART_INF_F)
       for (int s = 0; s < S; ++s) L += s_w[s * G + i] * exp2f(s_m[s * G + i] - M);
     const bool live = row_ok && M != -CUDART_INF_F;
+    if (live) L += sink_term(p, h * G + i, M);
     for (int s = 0; s < S; ++s) s_w[s * G + i] = live ? exp2f(s_m[s * G + i] - M) / L : 0.f;
   }
   __syncthreads();

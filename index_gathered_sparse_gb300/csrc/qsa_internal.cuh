@@ -42,6 +42,19 @@ struct Params {
   // unused.
   const int32_t* blocks;  // [nkv, total_q, topk] or nullptr
   int32_t topk;
+  // Latent mode (kernel 2 only): when `comp` is set, the key list of row r is
+  // its window (positions pos - window + 1 .. pos of the cache above) then
+  // the entries comp[r, :] (-1 unused) of a second, entry-paged cache; W ==
+  // window + num_comp.  Both caches have one head (head_bytes == 0: every
+  // query-head group reads it); offsets into the second cache carry bit 31.
+  const int32_t* comp;            // [total_q, num_comp] or nullptr
+  const float* sinks;             // [nq] sink logits (natural log units) or nullptr
+  const unsigned char* kv2;       // entry-paged cache base
+  const uint32_t* table2;         // [batch, max_pages2]
+  const uint32_t* cache_lengths2; // [batch] entries per sequence
+  int64_t page_pitch_bytes2, k_layer_bytes2, v_minus_k_bytes2, slot_bytes2;
+  int32_t num_comp, window, P2, max_pages2;
+  uint32_t num_pages2;
 };
 
 // Launch plan of the persistent stream-K kernel (computed on the host).

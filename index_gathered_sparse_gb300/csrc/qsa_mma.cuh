@@ -134,8 +134,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 
   const RowInfo ri = row_info(p, r);
   const bool block_sel = p.blocks != nullptr;
+  const bool latent = p.comp != nullptr;
   const int j0 = split * p.band;
-  const int n_row = block_sel ? p.W : ri.n;  // block lists are masked per key instead
+  const int n_row = block_sel || latent ? p.W : ri.n;  // block and latent lists are masked per key instead
   const int band_n = ri.ok ? max(0, min(n_row - j0, p.band)) : 0;
   uint32_t bad = ri.ok ? 0u : QSA_STATUS_BAD_ROW;
 
@@ -143,8 +144,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   {
     const int32_t* idx_row = p.indices + (int64_t)r * p.W + j0;
     const int32_t* blk_row = p.blocks + ((int64_t)h * p.total_q + r) * p.topk;
-    // the row's own position, for the block lists' causal rule
-    const int64_t pos_q = block_sel && ri.ok ? (int64_t)__ldg(p.cache_lengths + ri.b) + r - (int64_t)__ldg(p.row_offsets + ri.b) : 0;
+    // the row's own position, for the block lists' causal rule and the window
+    const int64_t pos_q =
+        (block_sel || latent) && ri.ok ? (int64_t)__ldg(p.cache_lengths + ri.b) + r - (int64_t)__ldg(p.row_offsets + ri.b) : 0;
     const uint32_t* trow = p.table + (int64_t)ri.b * p.max_pages;
     for (int k0 = 0; k0 < band_n; k0 += kMmaThreads * 8) {
       int32_t pos[8];
@@ -160,6 +162,13 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
           const int32_t beta = k < band_n ? __ldg(blk_row + j / p.P) : -1;
           const int64_t q = (int64_t)beta * p.P + (j - (j / p.P) * p.P);
           pos[u] = beta >= 0 && q <= pos_q ? (int32_t)q : -1;
+        } else if (latent) {
+          // window key j (position pos - window + 1 + j; -1 before the start of
+          // the sequence), then entry j - window of the compressed list
+          const int j = j0 + k;
+          if (k >= band_n) pos[u] = -1;
+          else if (j < p.window) pos[u] = pos_q - p.window + 1 + j >= 0 ? (int32_t)(pos_q - p.window + 1 + j) : -1;
+          else pos[u] = __ldg(p.comp + (int64_t)r * p.num_comp + (j - p.window));
         } else {
           pos[u] = k < band_n ? __ldg(idx_row + k) : 0;
         }
@@ -167,14 +176,41 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kMmaThreads + tid;
-        const bool skip = block_sel && pos[u] < 0;
-        lp[u] = k < band_n && !skip ? logical_page(p, ri.kv_len, pos[u], bad) : -1;
-        page[u] = lp[u] >= 0 ? __ldg(trow + lp[u]) : 0u;
+        const bool skip = (block_sel || latent) && pos[u] < 0;
+        const bool entry = latent && j0 + k >= p.window;  // in the compressed cache
+        if (entry && k < band_n && !skip) {
+          const int64_t ent = pos[u];
+          if (ent >= (int64_t)__ldg(p.cache_lengths2 + ri.b)) {
+            bad |= QSA_STATUS_BAD_INDEX;
+            lp[u] = -1;
+          } else if (ent / p.P2 >= p.max_pages2) {
+            bad |= QSA_STATUS_BAD_PAGE;
+            lp[u] = -1;
+          } else {
+            lp[u] = ent / p.P2;
+          }
+          page[u] = lp[u] >= 0 ? __ldg(p.table2 + (int64_t)ri.b * p.max_pages2 + lp[u]) : 0u;
+        } else {
+          lp[u] = k < band_n && !skip ? logical_page(p, ri.kv_len, pos[u], bad) : -1;
+          page[u] = lp[u] >= 0 ? __ldg(trow + lp[u]) : 0u;
+        }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kMmaThreads + tid;
-        if (k < band_n) s_off[k] = lp[u] >= 0 ? k_row_offset16(p, page[u], pos[u], h, bad) : kInvalidOff;
+        if (k >= band_n) continue;
+        if (latent && j0 + k >= p.window && lp[u] >= 0) {
+          if (page[u] >= p.num_pages2) {
+            bad |= QSA_STATUS_BAD_PAGE;
+            s_off[k] = kInvalidOff;
+          } else {
+            const int64_t ent = pos[u];
+            const int64_t off = (int64_t)page[u] * p.page_pitch_bytes2 + p.k_layer_bytes2 + (ent - lp[u] * p.P2) * p.slot_bytes2;
+            s_off[k] = (uint32_t)(off >> 4) | 0x80000000u;  // bit 31: the compressed cache
+          }
+        } else {
+          s_off[k] = lp[u] >= 0 ? k_row_offset16(p, page[u], pos[u], h, bad) : kInvalidOff;
+        }
       }
     }
   }
@@ -212,7 +248,11 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
       const int kk = t * C::TILE + key;
       const uint32_t off = kk < band_n ? s_off[kk] : kInvalidOff;
       const bool live = off != kInvalidOff;
-      const unsigned char* src = live ? p.kv + (int64_t)off * 16 + (kv ? p.v_minus_k_bytes : 0) + ch * 16 : p.kv;
+      // bit 31 of a live offset names the latent mode's compressed cache
+      const bool second = live && (off & 0x80000000u);
+      const unsigned char* base = second ? p.kv2 : p.kv;
+      const int64_t vk = second ? p.v_minus_k_bytes2 : p.v_minus_k_bytes;
+      const unsigned char* src = live ? base + (int64_t)(off & 0x7FFFFFFFu) * 16 + (kv ? vk : 0) + ch * 16 : p.kv;
       cp_async16(smem_addr(sb + kv * C::KV_BYTES + key * C::SROW + ch * 16), src, live ? 16u : 0u);
     }
   };

@@ -941,3 +941,21 @@ def latent_small_variants() -> dict:
             latent_bf16_decode(seed=23, batch=4, cache_range=(100, 900), window=64, num_comp=24, num_heads=8,
                                name="latent_fp8_small"), dtype="e4m3", page_size=32, comp_page_size=16),
     }
+
+
+def to_torch_latent(x: LatentInputs, device, out_dtype: Optional[str] = None) -> dict:
+    """Uploads a latent sparse attention call: the keyword arguments of
+    ``binding.qsa_latent_attention_ragged_paged``."""
+    import torch
+
+    a = to_torch(x.swa, device, out_dtype)
+    c = to_torch(x.comp, device)
+    return dict(
+        output=a["output"], q=a["q"], input_row_offsets=a["input_row_offsets"], swa_blocks=a["kv_blocks"],
+        swa_page_stride=x.swa.page_stride, swa_cache_lengths=a["cache_lengths"], swa_lookup_table=a["kv_lookup_table"],
+        comp_blocks=c["kv_blocks"], comp_page_stride=x.comp.page_stride, comp_cache_lengths=c["cache_lengths"],
+        comp_lookup_table=c["kv_lookup_table"], layer_idx=x.swa.layer_idx,
+        comp_indices=torch.from_numpy(np.ascontiguousarray(x.comp_indices, dtype=np.int32)).to(device),
+        attn_sink=torch.from_numpy(np.ascontiguousarray(x.attn_sink, dtype=np.float32)).to(device),
+        window=x.window, scale=x.swa.scale,
+    )
