@@ -134,7 +134,7 @@ def replica_spec(name: str, rank: int, world: int):
     """The workload one rank runs: every rank gets its own seeded batch."""
     from index_gathered_sparse_gb300 import workloads as wl
 
-    spec = (wl.WORKLOADS.get(name) or wl.MSA_WORKLOADS[name])()
+    spec = (wl.WORKLOADS.get(name) or wl.MSA_WORKLOADS.get(name) or wl.LATENT_WORKLOADS[name])()
     if world > 1:
         spec.seed += 100 * rank
     return spec
@@ -169,10 +169,17 @@ def is_block_sparse(x) -> bool:
     return getattr(x, "d_indices", None) is not None
 
 
+def is_latent(x) -> bool:
+    return getattr(x, "comp_indices", None) is not None
+
+
 def oracle_fn(x):
-    """The oracle function for ``x``: token lists or block lists."""
+    """The oracle function for ``x``: token lists, block lists or latent
+    (window + compressed entries + sinks)."""
     import oracle
 
+    if is_latent(x):
+        return oracle.latent_attention
     return oracle.msa_attention if is_block_sparse(x) else oracle.sparse_attention
 
 
@@ -233,6 +240,13 @@ def run_reference(args, x, rank, world):
 
 
 def workload_config(x) -> dict:
+    if is_latent(x):
+        cfg = workload_config(x.swa)
+        cfg.update({"workload": x.name, "selection": "sliding window + listed compressed entries + per-head sinks",
+                    "window": x.window, "num_comp": int(x.comp_indices.shape[1]), "num_kv_heads": 1,
+                    "group": x.num_heads, "comp_page_size": x.comp.kv_shape[3],
+                    "selection_width": x.window + int(x.comp_indices.shape[1])})
+        return cfg
     cfg = {
         "workload": x.name, "batch": x.batch, "total_q": x.total_q, "num_q_heads": x.num_q_heads,
         "num_kv_heads": x.num_kv_heads, "group": x.group, "head_dim": x.head_dim, "page_size": x.kv_shape[3],
@@ -390,12 +404,17 @@ def main():
         torch.cuda.set_device(local)
         dist.init_process_group("nccl")
     dev = torch.device("cuda", torch.cuda.current_device())
-    blocks = is_block_sparse(x)
-    d = wl.to_torch_msa(x, dev) if blocks else wl.to_torch(x, dev)
+    blocks, latent = is_block_sparse(x), is_latent(x)
+    d = wl.to_torch_latent(x, dev) if latent else wl.to_torch_msa(x, dev) if blocks else wl.to_torch(x, dev)
     code = {"f32": B.QSA_F32, "bf16": B.QSA_BF16, "e4m3": B.QSA_F8E4M3}[x.dtype]
-    width = x.topk * x.kv_shape[3] if blocks else x.selection_width
-    plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
-                      kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas)
+    if latent:  # groups of up to 16 query heads on the one latent head
+        lg = min(x.num_heads, 16)
+        plan = B.qsa_plan(code, x.total_q, x.num_heads // lg, 128, x.window + x.comp_indices.shape[1], lg,
+                          kernel=2, splits=args.splits)
+    else:
+        width = x.topk * x.kv_shape[3] if blocks else x.selection_width
+        plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
+                          kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
@@ -414,7 +433,9 @@ def main():
     flush_buf = _Flush()
 
     def call():
-        if blocks:
+        if latent:
+            B.qsa_latent_attention_ragged_paged(**d, splits=args.splits)
+        elif blocks:
             B.qsa_msa_attention_ragged_paged(**d, splits=args.splits)
         else:
             B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas)
@@ -460,9 +481,13 @@ def main():
     # ---- end to end: per-step inputs from pinned host memory, output back ----
     e2e = None
     if not args.no_e2e:
-        sel_keys = ("d_indices",) if blocks else ("token_indices", "counts")
-        host = {k: d[k].cpu().pin_memory() for k in
-                ("q", "input_row_offsets", "cache_lengths", "kv_lookup_table") + sel_keys}
+        if latent:
+            keys = ("q", "input_row_offsets", "swa_cache_lengths", "swa_lookup_table", "comp_cache_lengths",
+                    "comp_lookup_table", "comp_indices", "attn_sink")
+        else:
+            keys = ("q", "input_row_offsets", "cache_lengths", "kv_lookup_table") + (
+                ("d_indices",) if blocks else ("token_indices", "counts"))
+        host = {k: d[k].cpu().pin_memory() for k in keys}
         out_host = torch.empty(d["output"].shape, dtype=d["output"].dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_host.numel() * out_host.element_size()
