@@ -346,6 +346,8 @@ int qsa_oracle_msa_attention(
  *     cosine and sine are freqs_cis[i, 2k] and freqs_cis[i, 2k+1] (the block's
  *     index is its position); channels at or past rotary_dim pass through.
  * Keys, gamma and the output share one element type; freqs_cis has its own.
+ * Parity unpinned against the pages on the step order and the rotary
+ * position: the tests pin each step's arithmetic, not which order was meant.
  */
 int qsa_oracle_compress_keys(double* out, int64_t batch, int64_t max_blocks, int64_t head_dim,
                              const void* gamma, const void* freqs, int freq_dtype, int64_t positions,
