@@ -65,6 +65,7 @@ struct Resolved {
   int out_bf16 = 0;
   int kernel = 0;  // 1 CUDA-core, 2 tensor-core
   int splits = 1;
+  int cluster = 0;  // kernel 2: the bands of a unit merge inside one thread-block cluster
   int band = 0;
   int64_t ctas = 0;
   size_t ws_partial_bytes = 0, ws_bytes = 0;
@@ -227,6 +228,13 @@ struct DeviceState {
   std::map<void*, Workspace> workspaces;  // keyed by stream
   int sms = 0;
   int occ[2][2] = {{0, 0}, {0, 0}};  // [bf16, e4m3][nt - 1]
+  // resident clusters of s CTAs of the tensor-core kernel ([bf16, e4m3][nt - 1][s]; -1 unknown)
+  int clusters[2][2][qsa::kMaxClusterSplits + 1];
+  DeviceState() {
+    for (auto& a : clusters)
+      for (auto& b : a)
+        for (int& c : b) c = -1;
+  }
 };
 
 std::mutex g_mu;
@@ -287,7 +295,16 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     if (splits < min_splits)
       return fail(QSA_ERR_ARG, "options.splits below " + std::to_string(min_splits) + " for this selection width");
     if (splits > qsa::kMaxSplits) return fail(QSA_ERR_ARG, "options.splits above " + std::to_string(qsa::kMaxSplits));
-  } else {
+  }
+  const int kk = R.elem == qsa::kBF16 ? 0 : 1, knt = group <= 8 ? 0 : 1;
+  // resident clusters of s bands (s <= kMaxClusterSplits), queried once per device
+  auto clusters_of = [&](int64_t s) -> int {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int& c = g_dev[dev].clusters[kk][knt][s];
+    if (c < 0) c = kk == 0 ? qsa::mma_max_clusters_bf16(group, (int)s) : qsa::mma_max_clusters_e4m3(group, (int)s);
+    return c;
+  };
+  if (!(opt && opt->splits > 0)) {
     int sms = 0, occ = 0;
     {
       std::lock_guard<std::mutex> lk(g_mu);
@@ -296,20 +313,25 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
         const cudaError_t e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
       }
-      const int k = R.elem == qsa::kBF16 ? 0 : 1, nt = group <= 8 ? 0 : 1;
-      if (!st.occ[k][nt]) st.occ[k][nt] = k == 0 ? qsa::mma_ctas_per_sm_bf16(group) : qsa::mma_ctas_per_sm_e4m3(group);
+      if (!st.occ[kk][knt]) st.occ[kk][knt] = kk == 0 ? qsa::mma_ctas_per_sm_bf16(group) : qsa::mma_ctas_per_sm_e4m3(group);
       sms = st.sms;
-      occ = st.occ[k][nt];
+      occ = st.occ[kk][knt];
     }
     const int64_t units = R.total_q * R.nkv;
-    const int64_t slots = (int64_t)sms * occ;
     // Wave model: a CTA costs about (kPrologueKeys + keys it gathers); the
     // launch costs waves x that.  Pick the split count that minimises it.
+    // Split counts that merge inside a cluster have as many slots as whole
+    // clusters fit on the device.
     constexpr int64_t kPrologueKeys = 384;
     const int64_t most = std::max<int64_t>(min_splits, std::min<int64_t>(qsa::kMaxSplits, (R.W + T - 1) / T));
     splits = min_splits;
     double best = -1.0;
     for (int64_t sp = min_splits; units > 0 && sp <= most; ++sp) {
+      int64_t slots = (int64_t)sms * occ;
+      if (sp > 1 && sp <= qsa::kMaxClusterSplits) {
+        const int nc = clusters_of(sp);
+        if (nc > 0) slots = (int64_t)nc * sp;
+      }
       const int64_t waves = (units * sp + slots - 1) / slots;
       const double cost = (double)waves * (double)(kPrologueKeys + (R.W + sp - 1) / sp);
       if (best < 0 || cost < best) {
@@ -325,8 +347,9 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     R.band = (int)band;
   }
   R.splits = (int)splits;
+  R.cluster = splits > 1 && splits <= qsa::kMaxClusterSplits && clusters_of(splits) > 0 ? 1 : 0;
   R.ctas = R.total_q * R.nkv * R.splits;
-  if (R.splits > 1) {
+  if (R.splits > 1 && !R.cluster) {
     const int64_t units = R.total_q * R.nkv;
     R.ws_partial_bytes = ((size_t)(units * R.splits * qsa::partial_stride(group, R.D) * 4) + 255) / 256 * 256;
     R.ws_tickets = (size_t)units;
@@ -467,6 +490,7 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
   p.scale_log2 = scale * 1.4426950408889634f;  // log2(e): softmax in base 2
   p.out_bf16 = R.out_bf16;
   p.splits = R.splits;
+  p.cluster = R.cluster;
   p.band = R.band;
   if (lat) {
     p.comp = lat->comp;

@@ -34,6 +34,8 @@ struct Params {
   float scale_log2;  // scale * log2(e): the softmax runs in base 2
   int32_t out_bf16;
   int32_t splits;    // CTAs per (row, kv head)
+  int32_t cluster;   // kernel 2, splits > 1: the bands of a unit run as one thread-block
+                     // cluster and merge through distributed shared memory (no workspace)
   int32_t band;      // keys per split band (multiple of the key tile)
   // Block-granular selection (kernel 2 only): when `blocks` is set, key j of
   // (row r, kv head h) is slot j % P of logical block
@@ -107,6 +109,9 @@ cudaError_t launch_stream_e4m3_scan(const Params& p, const StreamPlan& sp, cudaS
 // CTAs of the tensor-core kernel that fit on one SM (for the split planner).
 int mma_ctas_per_sm_bf16(int group);
 int mma_ctas_per_sm_e4m3(int group);
+// Clusters of `splits` CTAs of the tensor-core kernel resident at once (0: none fit).
+int mma_max_clusters_bf16(int group, int splits);
+int mma_max_clusters_e4m3(int group, int splits);
 
 // Floats of one split-K partial: o[group][D], m[group], l[group], padded to a
 // multiple of 4 so every partial starts 16-byte aligned.
@@ -121,5 +126,8 @@ constexpr int kMmaThreads = 128;
 // Largest split count the fused split-K combine accepts (its per-split
 // weights live in shared memory).
 constexpr int kMaxSplits = 128;
+// Largest split count merged inside one thread-block cluster (the portable
+// cluster size).
+constexpr int kMaxClusterSplits = 8;
 
 }  // namespace qsa

@@ -113,6 +113,175 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// ---- thread-block cluster: barrier and distributed shared memory ----
+// All threads of every CTA of the cluster arrive; writes before the barrier
+// are visible cluster-wide after it.
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(out) : "r"(addr), "r"(rank));
+  return out;
+}
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];\n" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];\n"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// End of a (row r, kv head h) unit, or of band `split` of it, from NW
+// per-warp softmax states in shared memory: sm_m[w*GP + i] (running max of
+// the base-2 scores), sm_l[w*GP + i] (sum of exponentials) and
+// sm_o[(w*GP + i)*D + d] (unnormalised output), query heads i < group.
+// First one thread per head merges the warps' maxima and sums and keeps each
+// warp's weight (s_e: NW*GP + 2*GP floats of shared memory); then every
+// output element is a weighted sum of NW values, four channels per thread.
+//   - one band (splits == 1): writes output[r, h*group + i, :];
+//   - bands merged through the workspace: stores this band's partial and
+//     runs the ticket merge (the last band to arrive merges);
+//   - bands of one thread-block cluster (CTA rank = band): keeps the partial
+//     o[G][D], m[G], l[G] in its own shared memory (`part`); after a cluster
+//     barrier every CTA reads all bands' maxima and sums, and the o values
+//     of its 1/S slice of the output, through distributed shared memory and
+//     writes that slice; a second barrier keeps each partial alive until
+//     the other CTAs have read it.  No global workspace, fence or ticket.
+template <int NW>
+__device__ __forceinline__ void finish_unit_mma(const Params& p, int r, int h, int split, bool row_ok,
+                                                const float* sm_m, const float* sm_l, const float* sm_o, int GP,
+                                                float* scratch, float* part, float* s_e) {
+  const int G = p.group, D = p.D, S = p.splits;
+  float* s_M = s_e + NW * GP;
+  float* s_L = s_M + GP;
+  // one thread per (head, warp), NW adjacent lanes per head
+  static_assert(NW == 4, "four warp states per head");
+  const int wid = threadIdx.x >> 5;
+  if (wid < (G * NW + 31) / 32) {
+    const int i = threadIdx.x >> 2, w = threadIdx.x & 3;
+    const bool on = i < G;
+    const float m = on ? sm_m[w * GP + i] : -CUDART_INF_F;
+    float M = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, 2));
+    const float e = M == -CUDART_INF_F ? 0.f : exp2f(m - M);
+    float L = on ? sm_l[w * GP + i] * e : 0.f;
+    L += __shfl_xor_sync(0xffffffffu, L, 1);
+    L += __shfl_xor_sync(0xffffffffu, L, 2);
+    if (on) {
+      s_e[w * GP + i] = e;
+      if (w == 0) {
+        s_M[i] = M;
+        s_L[i] = L;
+      }
+    }
+  }
+  __syncthreads();
+  const int n4 = G * D / 4;
+  const int64_t out_base = ((int64_t)r * p.nq + (int64_t)h * G) * D;
+  if (S == 1) {
+    for (int q4 = threadIdx.x; q4 < n4; q4 += blockDim.x) {
+      const int idx = q4 * 4, i = idx / D, d = idx - i * D;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < NW; ++w) {
+        const float e = s_e[w * GP + i];
+        const float4 o = *reinterpret_cast<const float4*>(sm_o + (w * GP + i) * D + d);
+        acc.x = fmaf(e, o.x, acc.x);
+        acc.y = fmaf(e, o.y, acc.y);
+        acc.z = fmaf(e, o.z, acc.z);
+        acc.w = fmaf(e, o.w, acc.w);
+      }
+      const float M = s_M[i];
+      const bool live = row_ok && M != -CUDART_INF_F;
+      const float den = live ? s_L[i] + sink_term(p, h * G + i, M) : 1.f;
+      store_out(p, out_base + idx, live ? acc.x / den : 0.f);
+      store_out(p, out_base + idx + 1, live ? acc.y / den : 0.f);
+      store_out(p, out_base + idx + 2, live ? acc.z / den : 0.f);
+      store_out(p, out_base + idx + 3, live ? acc.w / den : 0.f);
+    }
+    return;
+  }
+  // this band's partial: o[G][D], m[G], l[G]
+  float* dst = p.cluster ? part : p.ws_partial + ((int64_t)(r * p.nkv + h) * S + split) * partial_stride(G, D);
+  for (int q4 = threadIdx.x; q4 < n4; q4 += blockDim.x) {
+    const int idx = q4 * 4, i = idx / D, d = idx - i * D;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      const float e = s_e[w * GP + i];
+      const float4 o = *reinterpret_cast<const float4*>(sm_o + (w * GP + i) * D + d);
+      acc.x = fmaf(e, o.x, acc.x);
+      acc.y = fmaf(e, o.y, acc.y);
+      acc.z = fmaf(e, o.z, acc.z);
+      acc.w = fmaf(e, o.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(dst + idx) = acc;
+  }
+  for (int i = threadIdx.x; i < G; i += blockDim.x) {
+    dst[G * D + i] = s_M[i];
+    dst[G * D + G + i] = s_L[i];
+  }
+  if (!p.cluster) {
+    merge_split_partials(p, r, h, row_ok, scratch);
+    return;
+  }
+  cluster_sync_all();
+  const uint32_t part_a = smem_addr(part);
+  // every band's max and sum, one thread per (head, band): SP adjacent lanes
+  // per head (SP = S rounded up to a power of two), reduced by shuffles
+  float* s_w = scratch;  // [S][G]: weight of band s for head i
+  {
+    const int SP = S <= 2 ? 2 : S <= 4 ? 4 : 8;
+    if (wid < (G * SP + 31) / 32) {
+      const int i = threadIdx.x / SP, sb = threadIdx.x - i * SP;
+      const bool on = i < G && sb < S;
+      const float m = on ? ld_cluster_f32(cluster_map(part_a + (uint32_t)(G * D + i) * 4u, (uint32_t)sb)) : -CUDART_INF_F;
+      const float l = on ? ld_cluster_f32(cluster_map(part_a + (uint32_t)(G * D + G + i) * 4u, (uint32_t)sb)) : 0.f;
+      float M = m;
+      for (int o = 1; o < SP; o <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float e = M == -CUDART_INF_F ? 0.f : exp2f(m - M);
+      float L = l * e;
+      for (int o = 1; o < SP; o <<= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      const bool live = row_ok && M != -CUDART_INF_F;
+      if (live) L += sink_term(p, h * G + (i < G ? i : 0), M);
+      if (on) s_w[sb * G + i] = live ? e / L : 0.f;
+    }
+  }
+  __syncthreads();
+  const int q_lo = split * n4 / S, q_hi = (split + 1) * n4 / S;
+  for (int q4 = q_lo + (int)threadIdx.x; q4 < q_hi; q4 += blockDim.x) {
+    const int idx = q4 * 4, i = idx / D;
+    // every band's four values in flight at once
+    float4 o[kMaxClusterSplits];
+#pragma unroll
+    for (int s = 0; s < kMaxClusterSplits; ++s)
+      if (s < S) o[s] = ld_cluster_f32x4(cluster_map(part_a + (uint32_t)idx * 4u, (uint32_t)s));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int s = 0; s < kMaxClusterSplits; ++s)
+      if (s < S) {
+        const float w = s_w[s * G + i];
+        acc.x = fmaf(w, o[s].x, acc.x);
+        acc.y = fmaf(w, o[s].y, acc.y);
+        acc.z = fmaf(w, o[s].z, acc.z);
+        acc.w = fmaf(w, o[s].w, acc.w);
+      }
+    store_out(p, out_base + idx, acc.x);
+    store_out(p, out_base + idx + 1, acc.y);
+    store_out(p, out_base + idx + 2, acc.z);
+    store_out(p, out_base + idx + 3, acc.w);
+  }
+  cluster_sync_all();
+}
+
 template <int KIND, int NT>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   using C = MmaCfg<KIND>;
@@ -124,30 +293,95 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
 
-  // CTA -> (kv head, split, row): kv heads of one row are adjacent in the grid
-  // (their K/V rows sit side by side in a cache slot), rows run latest first.
+  // CTA -> (split, kv head, row): the bands of one unit are adjacent in the
+  // grid (one thread-block cluster when they merge through distributed shared
+  // memory), then the kv heads of one row (their K/V rows sit side by side in
+  // a cache slot); rows run latest first.
   int cta = blockIdx.x;
-  const int h = cta % p.nkv;
-  cta /= p.nkv;
   const int split = cta % p.splits;
-  const int r = p.total_q - 1 - cta / p.splits;
-
-  const RowInfo ri = row_info(p, r);
+  cta /= p.splits;
+  const int h = cta % p.nkv;
+  const int r = p.total_q - 1 - cta / p.nkv;
   const bool block_sel = p.blocks != nullptr;
   const bool latent = p.comp != nullptr;
   const int j0 = split * p.band;
-  const int n_row = block_sel || latent ? p.W : ri.n;  // block and latent lists are masked per key instead
-  const int band_n = ri.ok ? max(0, min(n_row - j0, p.band)) : 0;
-  uint32_t bad = ri.ok ? 0u : QSA_STATUS_BAD_ROW;
 
-  // ---- translate the band's positions into K-row offsets (16-byte units) ----
-  {
-    const int32_t* idx_row = p.indices + (int64_t)r * p.W + j0;
+  // The translation takes three dependent trips to memory, each issuing all
+  // the loads it can: (1) counts[r], the Q fragments and the search for the
+  // row's sequence; (2) the sequence's offsets and cache length, and the
+  // band's list entries (index entries after counts, block ids, compressed
+  // entries); (3) the page-table entries.
+
+  // ---- trip 1 ----
+  const int cnt = block_sel || latent ? p.W : __ldg(p.counts + r);
+  // Q^T fragments (the MMA B operand), zero for padded heads
+  uint32_t qf[NT][C::KSTEPS][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int head = nt * 8 + gid;
+    const bool live = head < p.group;
+    const unsigned char* qrow = p.q + (((int64_t)r * p.nq + (int64_t)h * p.group + (live ? head : 0)) * C::D) * C::ELEM;
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS; ++ks) {
+      // bf16: k-step of 16 elements, thread pair (2 tig, 2 tig + 1) and +8
+      // e4m3: k-step of 32 elements, thread quad (4 tig .. 4 tig + 3) and +16
+      const int e0 = KIND == kBF16 ? ks * 16 + 2 * tig : ks * 32 + 4 * tig;
+      const int e1 = KIND == kBF16 ? e0 + 8 : e0 + 16;
+      qf[nt][ks][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + e0 * C::ELEM)) : 0u;
+      qf[nt][ks][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + e1 * C::ELEM)) : 0u;
+    }
+  }
+  const int b = row_sequence_warp(p, r);
+
+  // ---- trip 2 ----
+  const bool in_batch = b < p.batch;
+  const uint32_t o0 = in_batch ? __ldg(p.row_offsets + b) : 0u;
+  const uint32_t o1 = in_batch ? __ldg(p.row_offsets + b + 1) : 0u;
+  const uint32_t cl = in_batch ? __ldg(p.cache_lengths + b) : 0u;
+  const bool row_ok = in_batch && o0 <= (uint32_t)r && (uint32_t)r < o1;
+  const int64_t kv_len = (int64_t)cl + (int64_t)(o1 - o0);
+  const int64_t pos_q = (int64_t)cl + (int64_t)r - (int64_t)o0;  // the row's own position (when row_ok)
+  // keys of the band: valid index entries (counts clamped to [0, W]), or the
+  // whole block / latent list (masked per key); none when the row is not in a sequence
+  const int n_row = block_sel || latent ? p.W : min(max(cnt, 0), p.W);
+  const int band_n = max(0, min(n_row - j0, p.band));
+  const int band_keys = row_ok ? band_n : 0;
+  uint32_t bad = row_ok ? 0u : QSA_STATUS_BAD_ROW;
+  const uint32_t* trow = p.table + (int64_t)(in_batch ? b : 0) * p.max_pages;
+
+  if (block_sel) {
+    // one page-table lookup per listed block that meets the band, kept in
+    // the (still unused) stage ring; then every key's offset from its block
+    int32_t* s_beta = reinterpret_cast<int32_t*>(smem);
+    uint32_t* s_page = reinterpret_cast<uint32_t*>(smem) + (kMmaMaxBand + 2);
+    const int jb0 = j0 / p.P;
+    const int nbk = band_n > 0 ? (j0 + band_n - 1) / p.P - jb0 + 1 : 0;
     const int32_t* blk_row = p.blocks + ((int64_t)h * p.total_q + r) * p.topk;
-    // the row's own position, for the block lists' causal rule and the window
-    const int64_t pos_q =
-        (block_sel || latent) && ri.ok ? (int64_t)__ldg(p.cache_lengths + ri.b) + r - (int64_t)__ldg(p.row_offsets + ri.b) : 0;
-    const uint32_t* trow = p.table + (int64_t)ri.b * p.max_pages;
+    for (int t = tid; t < nbk; t += kMmaThreads) {
+      const int32_t beta = __ldg(blk_row + jb0 + t);  // trip 2
+      const bool in_table = in_batch && beta >= 0 && beta < p.max_pages;
+      s_beta[t] = beta;
+      s_page[t] = in_table ? __ldg(trow + beta) : kInvalidOff;  // trip 3
+    }
+    __syncthreads();
+    for (int k = tid; k < band_keys; k += kMmaThreads) {
+      const int j = j0 + k, jb = j / p.P;
+      const int32_t beta = s_beta[jb - jb0];
+      // slot j % P of block beta; -1 blocks and positions after the row's own
+      // are never attended (not an error)
+      const int64_t q = (int64_t)beta * p.P + (j - jb * p.P);
+      uint32_t off = kInvalidOff;
+      if (beta >= 0 && q <= pos_q) {
+        if (beta >= p.max_pages)
+          bad |= QSA_STATUS_BAD_PAGE;
+        else
+          off = k_row_offset16(p, s_page[jb - jb0], (int32_t)q, h, bad);
+      }
+      s_off[k] = off;
+    }
+  } else {
+    // ---- translate the band's positions into K-row offsets (16-byte units) ----
+    const int32_t* idx_row = p.indices + (int64_t)r * p.W + j0;
     for (int k0 = 0; k0 < band_n; k0 += kMmaThreads * 8) {
       int32_t pos[8];
       int64_t lp[8];
@@ -155,14 +389,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kMmaThreads + tid;
-        if (block_sel) {
-          // slot (j0 + k) % P of listed block (j0 + k) / P; -1 when unused or
-          // after the row's position (never attended, not an error)
-          const int j = j0 + k;
-          const int32_t beta = k < band_n ? __ldg(blk_row + j / p.P) : -1;
-          const int64_t q = (int64_t)beta * p.P + (j - (j / p.P) * p.P);
-          pos[u] = beta >= 0 && q <= pos_q ? (int32_t)q : -1;
-        } else if (latent) {
+        if (latent) {
           // window key j (position pos - window + 1 + j; -1 before the start of
           // the sequence), then entry j - window of the compressed list
           const int j = j0 + k;
@@ -170,17 +397,17 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
           else if (j < p.window) pos[u] = pos_q - p.window + 1 + j >= 0 ? (int32_t)(pos_q - p.window + 1 + j) : -1;
           else pos[u] = __ldg(p.comp + (int64_t)r * p.num_comp + (j - p.window));
         } else {
-          pos[u] = k < band_n ? __ldg(idx_row + k) : 0;
+          pos[u] = k < band_n ? __ldg(idx_row + k) : 0;  // entries past counts are never read
         }
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int k = k0 + u * kMmaThreads + tid;
-        const bool skip = (block_sel || latent) && pos[u] < 0;
+        const bool live = row_ok && k < band_n && !(latent && pos[u] < 0);
         const bool entry = latent && j0 + k >= p.window;  // in the compressed cache
-        if (entry && k < band_n && !skip) {
+        if (entry && live) {
           const int64_t ent = pos[u];
-          if (ent >= (int64_t)__ldg(p.cache_lengths2 + ri.b)) {
+          if (ent >= (int64_t)__ldg(p.cache_lengths2 + b)) {
             bad |= QSA_STATUS_BAD_INDEX;
             lp[u] = -1;
           } else if (ent / p.P2 >= p.max_pages2) {
@@ -189,9 +416,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
           } else {
             lp[u] = ent / p.P2;
           }
-          page[u] = lp[u] >= 0 ? __ldg(p.table2 + (int64_t)ri.b * p.max_pages2 + lp[u]) : 0u;
+          page[u] = lp[u] >= 0 ? __ldg(p.table2 + (int64_t)b * p.max_pages2 + lp[u]) : 0u;
         } else {
-          lp[u] = k < band_n && !skip ? logical_page(p, ri.kv_len, pos[u], bad) : -1;
+          lp[u] = live ? logical_page(p, kv_len, pos[u], bad) : -1;
           page[u] = lp[u] >= 0 ? __ldg(trow + lp[u]) : 0u;
         }
       }
@@ -215,27 +442,9 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
     }
   }
   if (bad) atomicOr(p.status, bad);
-
-  // ---- Q^T fragments (the MMA B operand), zero for padded heads ----
-  uint32_t qf[NT][C::KSTEPS][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int head = nt * 8 + gid;
-    const bool live = head < p.group;
-    const unsigned char* qrow = p.q + (((int64_t)r * p.nq + (int64_t)h * p.group + (live ? head : 0)) * C::D) * C::ELEM;
-#pragma unroll
-    for (int ks = 0; ks < C::KSTEPS; ++ks) {
-      // bf16: k-step of 16 elements, thread pair (2 tig, 2 tig + 1) and +8
-      // e4m3: k-step of 32 elements, thread quad (4 tig .. 4 tig + 3) and +16
-      const int e0 = KIND == kBF16 ? ks * 16 + 2 * tig : ks * 32 + 4 * tig;
-      const int e1 = KIND == kBF16 ? e0 + 8 : e0 + 16;
-      qf[nt][ks][0] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + e0 * C::ELEM)) : 0u;
-      qf[nt][ks][1] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + e1 * C::ELEM)) : 0u;
-    }
-  }
   __syncthreads();  // s_off complete
 
-  const int ntiles = (band_n + C::TILE - 1) / C::TILE;
+  const int ntiles = (band_keys + C::TILE - 1) / C::TILE;
   auto issue = [&](int t) {
     unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
     constexpr int TOTAL = C::TILE * 2 * C::CPR;
@@ -246,7 +455,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
       const int w = c - key * (2 * C::CPR);
       const int kv = w / C::CPR, ch = w - kv * C::CPR;
       const int kk = t * C::TILE + key;
-      const uint32_t off = kk < band_n ? s_off[kk] : kInvalidOff;
+      const uint32_t off = kk < band_keys ? s_off[kk] : kInvalidOff;
       const bool live = off != kInvalidOff;
       // bit 31 of a live offset names the latent mode's compressed cache
       const bool second = live && (off & 0x80000000u);
@@ -285,8 +494,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 
     const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
     const int kA = t * C::TILE + warp * 16 + gid, kB = kA + 8;
-    const bool vA = kA < band_n && s_off[kA] != kInvalidOff;
-    const bool vB = kB < band_n && s_off[kB] != kInvalidOff;
+    const bool vA = kA < band_keys && s_off[kA] != kInvalidOff;
+    const bool vB = kB < band_keys && s_off[kB] != kInvalidOff;
     if (!__any_sync(0xffffffffu, vA || vB)) continue;
     const uint32_t kbase = smem_addr(sb) + warp * 16 * C::SROW;
     const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + warp * 16 * C::SROW;
@@ -387,7 +596,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   float* sm_m = sm_o + NW * GP * C::D;
   float* sm_l = sm_m + NW * GP;
   float* scratch = sm_l + NW * GP;  // split-K merge: 2 * kMaxSplits * group floats
-  static_assert((NW * GP * C::D + 2 * NW * GP + 2 * kMaxSplits * GP) * 4 <= C::STAGES * C::STAGE_BYTES,
+  float* part = scratch + 2 * kMaxSplits * GP;  // cluster merge: this band's o[G][D], m[G], l[G]
+  float* s_e = part + GP * (C::D + 2);          // per-warp weights, merged max and sum
+  static_assert((NW * GP * C::D + 2 * NW * GP + 2 * kMaxSplits * GP + GP * (C::D + 2) + NW * GP + 2 * GP) * 4 <=
+                    C::STAGES * C::STAGE_BYTES,
                 "epilogue buffers must fit in the drained ring");
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
@@ -414,7 +626,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
         sm_o[(warp * GP + head) * C::D + d] = o[mt][nt][c];
       }
   __syncthreads();
-  finish_unit<NW>(p, r, h, split, ri.ok, sm_m, sm_l, sm_o, GP, scratch);
+  finish_unit_mma<NW>(p, r, h, split, row_ok, sm_m, sm_l, sm_o, GP, scratch, part, s_e);
 }
 
 template <int KIND, int NT>
@@ -430,8 +642,54 @@ cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
   }
   const int64_t ctas = (int64_t)p.total_q * p.nkv * p.splits;
   if (ctas == 0) return cudaSuccess;
+  if (p.cluster) {
+    // the bands of one unit form one cluster (splits <= kMaxClusterSplits)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas);
+    cfg.blockDim = dim3(kMmaThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = (unsigned)p.splits;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT>, p);
+  }
   mma_kernel<KIND, NT><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
   return cudaGetLastError();
+}
+
+// Clusters of `splits` CTAs of the tensor-core kernel that can be resident
+// at once on the device (0 when such a cluster cannot be placed).
+template <int KIND, int NT>
+int mma_max_clusters_nt(int splits) {
+  using C = MmaCfg<KIND>;
+  if (cudaFuncSetAttribute(mma_kernel<KIND, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)splits);
+  cfg.blockDim = dim3(kMmaThreads);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = (unsigned)splits;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT>, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // a refused query is not a launch error
+    return 0;
+  }
+  return n;
+}
+template <int KIND>
+int mma_max_clusters(int group, int splits) {
+  return group <= 8 ? mma_max_clusters_nt<KIND, 1>(splits) : mma_max_clusters_nt<KIND, 2>(splits);
 }
 
 template <int KIND>

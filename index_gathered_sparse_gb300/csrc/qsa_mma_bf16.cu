@@ -9,5 +9,6 @@ cudaError_t launch_mma_bf16(const Params& p, cudaStream_t s) {
 }
 
 int mma_ctas_per_sm_bf16(int group) { return mma_occupancy<kBF16>(group); }
+int mma_max_clusters_bf16(int group, int splits) { return mma_max_clusters<kBF16>(group, splits); }
 
 }  // namespace qsa

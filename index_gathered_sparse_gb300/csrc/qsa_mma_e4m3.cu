@@ -9,5 +9,6 @@ cudaError_t launch_mma_e4m3(const Params& p, cudaStream_t s) {
 }
 
 int mma_ctas_per_sm_e4m3(int group) { return mma_occupancy<kE4M3>(group); }
+int mma_max_clusters_e4m3(int group, int splits) { return mma_max_clusters<kE4M3>(group, splits); }
 
 }  // namespace qsa
