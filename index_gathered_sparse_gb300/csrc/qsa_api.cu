@@ -66,6 +66,7 @@ struct Resolved {
   int kernel = 0;  // 1 CUDA-core, 2 tensor-core
   int splits = 1;
   int cluster = 0;  // kernel 2: the bands of a unit merge inside one thread-block cluster
+  int tiles = 0;    // kernel 2: the variant with tile copies (block lists)
   int band = 0;
   int64_t ctas = 0;
   size_t ws_partial_bytes = 0, ws_bytes = 0;
@@ -227,13 +228,14 @@ struct DeviceState {
   uint32_t* status = nullptr;
   std::map<void*, Workspace> workspaces;  // keyed by stream
   int sms = 0;
-  int occ[2][2] = {{0, 0}, {0, 0}};  // [bf16, e4m3][nt - 1]
-  // resident clusters of s CTAs of the tensor-core kernel ([bf16, e4m3][nt - 1][s]; -1 unknown)
-  int clusters[2][2][qsa::kMaxClusterSplits + 1];
+  int occ[2][2][2] = {};  // [bf16, e4m3][nt - 1][tile copies]
+  // resident clusters of s CTAs of the tensor-core kernel ([bf16, e4m3][nt - 1][tile copies][s]; -1 unknown)
+  int clusters[2][2][2][qsa::kMaxClusterSplits + 1];
   DeviceState() {
     for (auto& a : clusters)
       for (auto& b : a)
-        for (int& c : b) c = -1;
+        for (auto& c : b)
+          for (int& d : c) d = -1;
   }
 };
 
@@ -300,8 +302,9 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   // resident clusters of s bands (s <= kMaxClusterSplits), queried once per device
   auto clusters_of = [&](int64_t s) -> int {
     std::lock_guard<std::mutex> lk(g_mu);
-    int& c = g_dev[dev].clusters[kk][knt][s];
-    if (c < 0) c = kk == 0 ? qsa::mma_max_clusters_bf16(group, (int)s) : qsa::mma_max_clusters_e4m3(group, (int)s);
+    int& c = g_dev[dev].clusters[kk][knt][R.tiles][s];
+    if (c < 0)
+      c = kk == 0 ? qsa::mma_max_clusters_bf16(group, (int)s, R.tiles != 0) : qsa::mma_max_clusters_e4m3(group, (int)s, R.tiles != 0);
     return c;
   };
   if (!(opt && opt->splits > 0)) {
@@ -313,9 +316,10 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
         const cudaError_t e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
       }
-      if (!st.occ[kk][knt]) st.occ[kk][knt] = kk == 0 ? qsa::mma_ctas_per_sm_bf16(group) : qsa::mma_ctas_per_sm_e4m3(group);
+      int& o = st.occ[kk][knt][R.tiles];
+      if (!o) o = kk == 0 ? qsa::mma_ctas_per_sm_bf16(group, R.tiles != 0) : qsa::mma_ctas_per_sm_e4m3(group, R.tiles != 0);
       sms = st.sms;
-      occ = st.occ[kk][knt];
+      occ = st.occ[kk][knt][R.tiles];
     }
     const int64_t units = R.total_q * R.nkv;
     // Wave model: a CTA costs about (kPrologueKeys + keys it gathers); the
@@ -422,6 +426,51 @@ qsa_status ensure_status(DeviceState& st) {
 // the kernel parameters, and the launch.  `indices`/`counts` carry a token
 // selection, or `blocks`/`topk` a block selection (kernel 2 only).
 // The latent mode's second source and sinks (see Params).
+// The driver's tensor-map encoder, looked up once through the runtime (no
+// link-time dependency on the driver library); null when unavailable.
+using TensorMapEncode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                     const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                     CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+TensorMapEncode tensor_map_encoder() {
+  static const TensorMapEncode fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      f = nullptr;
+    }
+    return reinterpret_cast<TensorMapEncode>(f);
+  }();
+  return fn;
+}
+
+// Kernel 2's tile copies: encodes the 5-D map of the first cache described
+// with qsa::Params::tmap (p.tma = 1), or leaves p.tma = 0 when a tile copy
+// cannot describe the layout (pages shorter than a tile, strides that are
+// not multiples of 16 bytes, ...): every tile then takes 16-byte copies.
+void encode_tile_map(Params& p, const void* kv, int elem, int64_t num_pages) {
+  p.tma = 0;
+  const TensorMapEncode encode = tensor_map_encoder();
+  const int64_t plane = (int64_t)p.P * p.slot_bytes;
+  if (!encode || elem == qsa::kF32 || p.P < qsa::kMmaTile || p.slot_bytes <= 0 || p.slot_bytes % 128 != 0 ||
+      p.k_layer_bytes % plane != 0 || p.v_minus_k_bytes % plane != 0 || p.page_pitch_bytes % 16 != 0 ||
+      (reinterpret_cast<uintptr_t>(kv) & 15u) != 0 || num_pages <= 0 || num_pages > 0xFFFFFFFFll)
+    return;
+  const cuuint64_t dims[5] = {elem == qsa::kBF16 ? 64u : 128u, (cuuint64_t)(p.slot_bytes / 128), (cuuint64_t)p.P,
+                              (cuuint64_t)(2 * (p.v_minus_k_bytes / plane)), (cuuint64_t)num_pages};
+  const cuuint64_t strides[4] = {128u, (cuuint64_t)p.slot_bytes, (cuuint64_t)plane, (cuuint64_t)p.page_pitch_bytes};
+  const cuuint32_t box[5] = {(cuuint32_t)dims[0], 1u, (cuuint32_t)qsa::kMmaTile, 1u, 1u};
+  const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
+  const CUresult r = encode(&p.tmap, elem == qsa::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
+                            const_cast<void*>(kv), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return;
+  p.tma = 1;
+  p.tma_plane_k = (int32_t)(p.k_layer_bytes / plane);
+  p.tma_plane_v = (int32_t)((p.k_layer_bytes + p.v_minus_k_bytes) / plane);
+}
+
 struct LatentArgs {
   const int32_t* comp;
   const float* sinks;
@@ -512,6 +561,8 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
     p.slot_bytes = lat->slot_bytes1;
     p.head_bytes = 0;  // every query-head group reads the one latent head
   }
+
+  if (R.kernel == 2 && R.tiles) encode_tile_map(p, kv_blocks.data, R.elem, R.num_pages);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (R.kernel == 1)
@@ -605,6 +656,7 @@ qsa_status qsa_msa_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qsa_t
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  R.tiles = 1;  // listed blocks are whole pages: most key tiles are one tile copy
   s = plan_launch(R, group, &opt, dev);
   if (s != QSA_OK) return s;
   return launch_planned(R, output, q, input_row_offsets, kv_blocks, cache_lengths, kv_lookup_table, layer_idx,

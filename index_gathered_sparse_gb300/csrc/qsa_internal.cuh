@@ -1,6 +1,7 @@
 // Internal declarations shared by libqsa's translation units (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -57,6 +58,14 @@ struct Params {
   int64_t page_pitch_bytes2, k_layer_bytes2, v_minus_k_bytes2, slot_bytes2;
   int32_t num_comp, window, P2, max_pages2;
   uint32_t num_pages2;
+  // Kernel 2's tile copies (when tma != 0): a 5-D tiled TMA map of the first
+  // cache, innermost first: the elements of a 128-byte line, the lines of a
+  // slot (stride 128 B), the P slots of a page (stride slot_bytes), the 2 x L
+  // K/V planes (stride P * slot_bytes) and the pages (stride
+  // page_pitch_bytes), with a box of one line of 64 slots and the 128-byte
+  // swizzle.  tma_plane_k / tma_plane_v: the planes of layer_idx.
+  int32_t tma, tma_plane_k, tma_plane_v;
+  CUtensorMap tmap;
 };
 
 // Launch plan of the persistent stream-K kernel (computed on the host).
@@ -107,11 +116,12 @@ cudaError_t launch_stream_e4m3(const Params& p, const StreamPlan& sp, cudaStream
 cudaError_t launch_stream_bf16_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_e4m3_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 // CTAs of the tensor-core kernel that fit on one SM (for the split planner).
-int mma_ctas_per_sm_bf16(int group);
-int mma_ctas_per_sm_e4m3(int group);
+// (`tiles`: the variant with tile copies, used for block lists.)
+int mma_ctas_per_sm_bf16(int group, bool tiles);
+int mma_ctas_per_sm_e4m3(int group, bool tiles);
 // Clusters of `splits` CTAs of the tensor-core kernel resident at once (0: none fit).
-int mma_max_clusters_bf16(int group, int splits);
-int mma_max_clusters_e4m3(int group, int splits);
+int mma_max_clusters_bf16(int group, int splits, bool tiles);
+int mma_max_clusters_e4m3(int group, int splits, bool tiles);
 
 // Floats of one split-K partial: o[group][D], m[group], l[group], padded to a
 // multiple of 4 so every partial starts 16-byte aligned.

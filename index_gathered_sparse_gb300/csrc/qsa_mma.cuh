@@ -33,20 +33,40 @@
 
 namespace qsa {
 
-template <int KIND>
+// TILES: the variant with tile copies (block lists, whose tiles are mostly
+// whole pages) and the 128-byte-swizzled stage layout they write; without,
+// 16-byte copies only into rows padded by 16 bytes (no tile-copy code in the
+// loop, which measurably slows the per-row path).
+template <int KIND, bool TILES>
 struct MmaCfg {
   static constexpr int D = 128;
   static constexpr int ELEM = KIND == kBF16 ? 2 : 1;
   static constexpr int ROWB = D * ELEM;            // bytes of one K or V row
-  static constexpr int SROW = ROWB + 16;           // padded shared-memory row
+  static constexpr int LINES = ROWB / 128;         // 128-byte lines per row
   static constexpr int TILE = kMmaTile;            // keys per stage
-  static constexpr int KV_BYTES = TILE * SROW;     // the K (or V) half of a stage
+  static constexpr int LINE_BYTES = TILE * 128;    // one line of every key of a stage (swizzled layout)
+  static constexpr int SROW = ROWB + 16;           // padded shared-memory row (16-byte copies only)
+  static constexpr int KV_BYTES = TILES ? LINES * LINE_BYTES : TILE * SROW;  // the K (or V) half of a stage
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int STAGES = KIND == kBF16 ? 3 : 4;
+  static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int CPR = ROWB / 16;            // 16-byte chunks per row
   static constexpr int KSTEPS = KIND == kBF16 ? 8 : 4;  // MMA k-steps over head_dim for S
-  static constexpr int SMEM = STAGES * STAGE_BYTES + kMmaMaxBand * 4;
+  static constexpr int MAXT = kMmaMaxBand / TILE;  // most tiles of a band
+  // ring (1024-byte aligned with tile copies: the 128-byte swizzle repeats
+  // every 8 lines), band offsets, and with tile copies one barrier per stage
+  // and the tile-copy coordinates
+  static constexpr int SMEM = TILES ? 1024 + RING + kMmaMaxBand * 4 + STAGES * 8 + MAXT * 8 : RING + kMmaMaxBand * 4;
 };
+
+// Shared-memory layout of a stage's K (or V) half: line x of key k's row
+// (x < LINES) sits at x * TILE * 128 + k * 128, and its 16-byte chunk c at
+// chunk c XOR (k mod 8) inside that line: the 128-byte swizzle a TMA tile
+// copy applies, which also keeps ldmatrix's eight 16-byte rows in eight
+// different bank groups.
+__device__ __forceinline__ uint32_t swz_off(int k, int chunk) {
+  return (uint32_t)((chunk >> 3) * (kMmaTile * 128) + k * 128 + (((chunk & 7) ^ (k & 7)) << 4));
+}
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -75,6 +95,83 @@ __device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
   uint32_t y;
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;\n" : "=r"(y) : "r"(x));
   return y;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `bar` with this parity; false after kSpinLimit polls
+// (each poll may block for a while in hardware), which never happens unless a
+// copy was lost.
+constexpr int kSpinLimit = 1 << 20;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+// The same bounded wait as one asm statement (its loop stays out of the
+// compiler's view of the surrounding loop): 1 when the phase completed, 0
+// after kSpinLimit polls.  Kernel 2's tile-copy helpers carry no memory
+// clobber: the stage is read only by volatile asm (ldmatrix), which keeps
+// its order, and written only after a __syncthreads.
+__device__ __forceinline__ uint32_t mbar_wait_asm(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n"
+      " .reg .pred p;\n"
+      " .reg .u32 n;\n"
+      " mov.u32 n, %3;\n"
+      "WAIT:\n"
+      " mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " @p bra.uni DONE;\n"
+      " sub.u32 n, n, 1;\n"
+      " setp.ne.u32 p, n, 0;\n"
+      " @p bra.uni WAIT;\n"
+      "DONE:\n"
+      " selp.u32 %0, 1, 0, p;\n"
+      "}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(kSpinLimit));
+  return ok;
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+}
+// One-dimensional bulk copy global -> this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+// The arrive fires on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];\n" ::"r"(bar) : "memory");
+}
+// Tiled TMA copy of one box of a 5-D tensor map into this CTA's shared
+// memory, completing on `bar` (the map is a __grid_constant__ kernel parameter).
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const void* map, int c0, int c1, int c2, int c3, int c4,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5, %6}], "
+      "[%7];\n" ::"r"(dst),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar));
+}
+__device__ __forceinline__ void tile_fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;\n" ::); }
+__device__ __forceinline__ void tile_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes));
 }
 
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
@@ -282,16 +379,25 @@ __device__ __forceinline__ void finish_unit_mma(const Params& p, int r, int h, i
   cluster_sync_all();
 }
 
-template <int KIND, int NT>
-__global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
-  using C = MmaCfg<KIND>;
+template <int KIND, int NT, bool TILES>
+__global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ Params p) {
+  using C = MmaCfg<KIND, TILES>;
   constexpr int NW = kMmaThreads / 32;
   constexpr int GP = 8 * NT;  // padded query heads
-  extern __shared__ __align__(128) unsigned char smem[];
-  uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = TILES ? smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u) : smem_raw;  // the stage ring
+  uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + C::RING);
+  uint64_t* s_full = reinterpret_cast<uint64_t*>(s_off + kMmaMaxBand);  // TILES: one barrier per stage
+  int2* s_tile = reinterpret_cast<int2*>(s_full + C::STAGES);           // TILES: tile copy (page, first slot) or (-1, 0)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
+  if (TILES && tid == 0) {
+    // a stage's barrier completes a phase when a tile copy into it landed
+    // (16-byte copies complete through per-thread cp.async groups instead)
+    for (int k = 0; k < C::STAGES; ++k) mbar_init(smem_addr(&s_full[k]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
 
   // CTA -> (split, kv head, row): the bands of one unit are adjacent in the
   // grid (one thread-block cluster when they merge through distributed shared
@@ -378,6 +484,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
           off = k_row_offset16(p, s_page[jb - jb0], (int32_t)q, h, bad);
       }
       s_off[k] = off;
+      if (TILES && k % C::TILE == 0) s_tile[k / C::TILE] = make_int2((int)s_page[jb - jb0], j - jb * p.P);
     }
   } else {
     // ---- translate the band's positions into K-row offsets (16-byte units) ----
@@ -437,6 +544,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
           }
         } else {
           s_off[k] = lp[u] >= 0 ? k_row_offset16(p, page[u], pos[u], h, bad) : kInvalidOff;
+          if (TILES && k % C::TILE == 0) s_tile[k / C::TILE] = make_int2((int)page[u], (int)((uint32_t)pos[u] % (uint32_t)p.P));
         }
       }
     }
@@ -444,9 +552,51 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   if (bad) atomicOr(p.status, bad);
   __syncthreads();  // s_off complete
 
+  // Tiles whose 64 keys are consecutive slots of one page of the first cache
+  // (page-aligned runs, whole blocks) load with one TMA tile copy per 128-byte
+  // line of K and of V; the others with 16-byte copies per row.
   const int ntiles = (band_keys + C::TILE - 1) / C::TILE;
+  uint32_t tma_mask = 0;  // bit t: tile t is a tile copy (a band has at most 32 tiles)
+  if constexpr (TILES) {
+  if (p.tma) {
+    const uint32_t sstep = (uint32_t)(p.slot_bytes >> 4);
+    for (int t = warp; t < ntiles; t += NW) {
+      const uint32_t base = s_off[t * C::TILE];
+      const bool ok = (t + 1) * C::TILE <= band_keys && base != kInvalidOff && !(base & 0x80000000u) &&
+                      s_off[t * C::TILE + lane] == base + (uint32_t)lane * sstep &&
+                      s_off[t * C::TILE + 32 + lane] == base + (uint32_t)(32 + lane) * sstep;
+      // consecutive offsets are consecutive slots of one page (a page holds
+      // more than P slots of one plane); the translation recorded the page
+      // and slot of the tile's first key
+      if (!__all_sync(0xffffffffu, ok) && lane == 0) s_tile[t] = make_int2(-1, 0);
+    }
+  } else {
+    for (int t = tid; t < ntiles; t += kMmaThreads) s_tile[t] = make_int2(-1, 0);
+  }
+  __syncthreads();
+  static_assert(C::MAXT <= 32, "tile mask");
+  if (p.tma)
+    for (int t = 0; t < ntiles; ++t) tma_mask |= (s_tile[t].x >= 0 ? 1u : 0u) << t;
+  }
+
+  const int hc = p.head_bytes ? h : 0;  // the unit's head in the cache (the latent cache has one)
   auto issue = [&](int t) {
     unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
+    const uint32_t bar = smem_addr(&s_full[t % C::STAGES]);
+    if (TILES && (tma_mask >> t & 1u)) {
+      if (tid == 0) {
+        const int2 tc = s_tile[t];
+        tile_fence_proxy_async();  // earlier generic accesses of the stage before the async-proxy writes
+        tile_expect_tx(bar, C::STAGE_BYTES);
+#pragma unroll
+        for (int kv = 0; kv < 2; ++kv)
+#pragma unroll
+          for (int x = 0; x < C::LINES; ++x)
+            tma_load_5d(smem_addr(sb + kv * C::KV_BYTES + x * C::LINE_BYTES), &p.tmap, 0, hc * C::LINES + x, tc.y,
+                        kv ? p.tma_plane_v : p.tma_plane_k, tc.x, bar);
+      }
+      return;
+    }
     constexpr int TOTAL = C::TILE * 2 * C::CPR;
 #pragma unroll
     for (int i = 0; i < TOTAL / kMmaThreads; ++i) {
@@ -462,7 +612,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
       const unsigned char* base = second ? p.kv2 : p.kv;
       const int64_t vk = second ? p.v_minus_k_bytes2 : p.v_minus_k_bytes;
       const unsigned char* src = live ? base + (int64_t)(off & 0x7FFFFFFFu) * 16 + (kv ? vk : 0) + ch * 16 : p.kv;
-      cp_async16(smem_addr(sb + kv * C::KV_BYTES + key * C::SROW + ch * 16), src, live ? 16u : 0u);
+      const uint32_t dst = TILES ? swz_off(key, ch) : (uint32_t)(key * C::SROW + ch * 16);
+      cp_async16(smem_addr(sb + kv * C::KV_BYTES) + dst, src, live ? 16u : 0u);
     }
   };
 
@@ -482,23 +633,35 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
     for (int mt = 0; mt < 8; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
   }
 
-  // per-lane ldmatrix row / column: non-transposed A (K) and transposed A (V^T)
-  const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8, a_col = ((lane >> 4) & 1) * 16;
-  const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8, t_col = ((lane >> 3) & 1) * 16;
+  // per-lane ldmatrix rows: non-transposed A (K) and transposed A (V^T), and
+  // the swizzle term of each lane's 16-byte chunk (its row mod 8, and which
+  // chunk of the pair it reads)
+  const int a_row = (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int t_row = (lane & 7) + ((lane >> 4) & 1) * 8;
+  const uint32_t kx16 = (uint32_t)(((lane & 7) ^ ((lane >> 4) & 1)) << 4);
+  const uint32_t vx16 = (uint32_t)(((lane & 7) ^ ((lane >> 3) & 1)) << 4);
+  bool timed_out = false;
+  uint32_t tma_phase = 0;  // bit s: parity of the next tile-copy phase of stage s
 
   for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<C::STAGES - 2>();
-    __syncthreads();
+    cp_async_wait<C::STAGES - 2>();  // this thread's 16-byte copies of tile t
+    __syncthreads();  // everyone's copies of tile t landed; every warp is done with tile t - 1
     if (t + C::STAGES - 1 < ntiles) issue(t + C::STAGES - 1);
     cp_async_commit();
+    if (TILES && (tma_mask >> t & 1u)) {
+      const int st = t % C::STAGES;
+      if (!mbar_wait_asm(smem_addr(&s_full[st]), (tma_phase >> st) & 1u)) timed_out = true;
+      tma_phase ^= 1u << st;
+    }
 
     const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
     const int kA = t * C::TILE + warp * 16 + gid, kB = kA + 8;
     const bool vA = kA < band_keys && s_off[kA] != kInvalidOff;
     const bool vB = kB < band_keys && s_off[kB] != kInvalidOff;
     if (!__any_sync(0xffffffffu, vA || vB)) continue;
-    const uint32_t kbase = smem_addr(sb) + warp * 16 * C::SROW;
-    const uint32_t vbase = smem_addr(sb + C::KV_BYTES) + warp * 16 * C::SROW;
+    constexpr uint32_t RS = TILES ? 128u : (uint32_t)C::SROW;  // row stride of a stage half
+    const uint32_t krow = smem_addr(sb) + (uint32_t)(warp * 16 + a_row) * RS;
+    const uint32_t vrow = smem_addr(sb + C::KV_BYTES) + (uint32_t)(warp * 16 + t_row) * RS;
 
     // S^T = K Q^T over head_dim
     float s[NT][4];
@@ -507,7 +670,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       uint32_t a[4];
-      ldsm_x4(kbase + a_row * C::SROW + ks * 32 + a_col, a);
+      if constexpr (TILES)
+        ldsm_x4(krow + (uint32_t)((ks >> 2) * C::LINE_BYTES) + ((uint32_t)((2 * (ks & 3)) << 4) ^ kx16), a);
+      else
+        ldsm_x4(krow + ks * 32 + ((lane >> 4) & 1) * 16, a);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
         if constexpr (KIND == kBF16)
@@ -557,7 +723,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
         uint32_t a[4];
-        ldsm_x4_t(vbase + t_row * C::SROW + mt * 32 + t_col, a);
+        if constexpr (TILES)
+          ldsm_x4_t(vrow + (uint32_t)((mt >> 2) * C::LINE_BYTES) + ((uint32_t)((2 * (mt & 3)) << 4) ^ vx16), a);
+        else
+          ldsm_x4_t(vrow + mt * 32 + ((lane >> 3) & 1) * 16, a);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) mma_bf16(o[mt][nt], a, pb[nt][0], pb[nt][1]);
       }
@@ -569,7 +738,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
 #pragma unroll
       for (int pr = 0; pr < 4; ++pr) {
         uint32_t r4[4];
-        ldsm_x4_t(vbase + t_row * C::SROW + pr * 32 + t_col, r4);
+        if constexpr (TILES)
+          ldsm_x4_t(vrow + ((uint32_t)((2 * pr) << 4) ^ vx16), r4);
+        else
+          ldsm_x4_t(vrow + pr * 32 + ((lane >> 3) & 1) * 16, r4);
         uint32_t a_even[4], a_odd[4];
         const uint32_t s0 = __byte_perm(r4[0], 0, 0x3120), s1 = __byte_perm(r4[1], 0, 0x3120);
         const uint32_t s2 = __byte_perm(r4[2], 0, 0x3120), s3 = __byte_perm(r4[3], 0, 0x3120);
@@ -589,6 +761,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
       }
     }
   }
+  if (timed_out) atomicOr(p.status, QSA_STATUS_TIMEOUT);
   cp_async_wait<0>();
   __syncthreads();  // the ring is drained; its shared memory now holds the warp states
 
@@ -629,14 +802,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const Params p) {
   finish_unit_mma<NW>(p, r, h, split, row_ok, sm_m, sm_l, sm_o, GP, scratch, part, s_e);
 }
 
-template <int KIND, int NT>
-cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
-  using C = MmaCfg<KIND>;
+template <int KIND, int NT, bool TILES>
+cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
+  using C = MmaCfg<KIND, TILES>;
   static int configured_mask = 0;  // one bit per device (up to 32)
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured_mask |= 1 << (dev & 31);
   }
@@ -656,18 +829,22 @@ cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT>, p);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES>, p);
   }
-  mma_kernel<KIND, NT><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
+  mma_kernel<KIND, NT, TILES><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
   return cudaGetLastError();
+}
+template <int KIND, int NT>
+cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
+  return p.tma ? launch_mma_t<KIND, NT, true>(p, s) : launch_mma_t<KIND, NT, false>(p, s);
 }
 
 // Clusters of `splits` CTAs of the tensor-core kernel that can be resident
 // at once on the device (0 when such a cluster cannot be placed).
-template <int KIND, int NT>
+template <int KIND, int NT, bool TILES>
 int mma_max_clusters_nt(int splits) {
-  using C = MmaCfg<KIND>;
-  if (cudaFuncSetAttribute(mma_kernel<KIND, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+  using C = MmaCfg<KIND, TILES>;
+  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)splits);
@@ -681,29 +858,30 @@ int mma_max_clusters_nt(int splits) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES>, &cfg) != cudaSuccess) {
     cudaGetLastError();  // a refused query is not a launch error
     return 0;
   }
   return n;
 }
 template <int KIND>
-int mma_max_clusters(int group, int splits) {
-  return group <= 8 ? mma_max_clusters_nt<KIND, 1>(splits) : mma_max_clusters_nt<KIND, 2>(splits);
+int mma_max_clusters(int group, int splits, bool tiles) {
+  if (tiles) return group <= 8 ? mma_max_clusters_nt<KIND, 1, true>(splits) : mma_max_clusters_nt<KIND, 2, true>(splits);
+  return group <= 8 ? mma_max_clusters_nt<KIND, 1, false>(splits) : mma_max_clusters_nt<KIND, 2, false>(splits);
 }
 
-template <int KIND>
-int mma_occupancy(int group) {
-  using C = MmaCfg<KIND>;
+template <int KIND, int NT, bool TILES>
+int mma_occupancy_nt() {
+  using C = MmaCfg<KIND, TILES>;
   int n = 0;
-  if (group <= 8) {
-    cudaFuncSetAttribute(mma_kernel<KIND, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, 1>, kMmaThreads, C::SMEM);
-  } else {
-    cudaFuncSetAttribute(mma_kernel<KIND, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, 2>, kMmaThreads, C::SMEM);
-  }
+  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES>, kMmaThreads, C::SMEM);
   return n > 0 ? n : 1;
+}
+template <int KIND>
+int mma_occupancy(int group, bool tiles) {
+  if (tiles) return group <= 8 ? mma_occupancy_nt<KIND, 1, true>() : mma_occupancy_nt<KIND, 2, true>();
+  return group <= 8 ? mma_occupancy_nt<KIND, 1, false>() : mma_occupancy_nt<KIND, 2, false>();
 }
 
 }  // namespace qsa
