@@ -196,6 +196,15 @@ __device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz: relative error
+// near 2^-22, results below 2^-126 flushed to zero, 2^-inf = 0), for the
+// softmax terms 2^(s - max) <= 1 of the main loops.
+__device__ __forceinline__ float exp2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
@@ -204,10 +213,12 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   const __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&v);
 }
-// Two e4m3 bytes (low byte first) -> f16x2 with the low byte in the low half.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_bytes) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)two_bytes, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four e4m3 bytes [b0 b1 b2 b3] -> f16x2 (b0, b1) and f16x2 (b2, b3), each
+// conversion reading a 16-bit half of the word directly.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t four_bytes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi)
+      : "r"(four_bytes));
 }
 
 // ---- thread-block cluster: barrier and distributed shared memory ----
@@ -699,8 +710,8 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
         const float mnew = fmaxf(m_run[nt][c], mx);
         const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
-        const float alpha = exp2f(m_run[nt][c] - muse);
-        const float p0 = exp2f(x0 - muse), p1 = exp2f(x1 - muse);
+        const float alpha = exp2_fast(m_run[nt][c] - muse);
+        const float p0 = exp2_fast(x0 - muse), p1 = exp2_fast(x1 - muse);
         l_run[nt][c] = l_run[nt][c] * alpha + p0 + p1;
         m_run[nt][c] = mnew;
         pv[c] = p0;
@@ -745,14 +756,10 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         uint32_t a_even[4], a_odd[4];
         const uint32_t s0 = __byte_perm(r4[0], 0, 0x3120), s1 = __byte_perm(r4[1], 0, 0x3120);
         const uint32_t s2 = __byte_perm(r4[2], 0, 0x3120), s3 = __byte_perm(r4[3], 0, 0x3120);
-        a_even[0] = e4m3x2_to_f16x2(s0 & 0xFFFFu);
-        a_even[1] = e4m3x2_to_f16x2(s0 >> 16);
-        a_even[2] = e4m3x2_to_f16x2(s2 & 0xFFFFu);
-        a_even[3] = e4m3x2_to_f16x2(s2 >> 16);
-        a_odd[0] = e4m3x2_to_f16x2(s1 & 0xFFFFu);
-        a_odd[1] = e4m3x2_to_f16x2(s1 >> 16);
-        a_odd[2] = e4m3x2_to_f16x2(s3 & 0xFFFFu);
-        a_odd[3] = e4m3x2_to_f16x2(s3 >> 16);
+        e4m3x4_to_f16x2x2(s0, a_even[0], a_even[1]);
+        e4m3x4_to_f16x2x2(s2, a_even[2], a_even[3]);
+        e4m3x4_to_f16x2x2(s1, a_odd[0], a_odd[1]);
+        e4m3x4_to_f16x2x2(s3, a_odd[2], a_odd[3]);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           mma_f16(o[2 * pr][nt], a_even, pb[nt][0], pb[nt][1]);

@@ -767,11 +767,11 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           const float mnew = fmaxf(m_run[nt][c], mx);
           const float muse = mnew == -CUDART_INF_F ? 0.f : mnew;
-          const float alpha = exp2f(m_run[nt][c] - muse);
+          const float alpha = exp2_fast(m_run[nt][c] - muse);
           float lsum = 0.f;
 #pragma unroll
           for (int sl = 0; sl < MSL; ++sl) {
-            const float p0 = exp2f(sc[sl][nt][c] - muse), p1 = exp2f(sc[sl][nt][2 + c] - muse);
+            const float p0 = exp2_fast(sc[sl][nt][c] - muse), p1 = exp2_fast(sc[sl][nt][2 + c] - muse);
             pv[sl][c] = p0;
             pv[sl][2 + c] = p1;
             lsum += p0 + p1;
@@ -818,14 +818,10 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
             uint32_t ae[4], ao[4];
             const uint32_t q0 = __byte_perm(r4[0], 0, 0x3120), q1 = __byte_perm(r4[1], 0, 0x3120);
             const uint32_t q2 = __byte_perm(r4[2], 0, 0x3120), q3 = __byte_perm(r4[3], 0, 0x3120);
-            ae[0] = e4m3x2_to_f16x2(q0 & 0xFFFFu);
-            ae[1] = e4m3x2_to_f16x2(q0 >> 16);
-            ae[2] = e4m3x2_to_f16x2(q2 & 0xFFFFu);
-            ae[3] = e4m3x2_to_f16x2(q2 >> 16);
-            ao[0] = e4m3x2_to_f16x2(q1 & 0xFFFFu);
-            ao[1] = e4m3x2_to_f16x2(q1 >> 16);
-            ao[2] = e4m3x2_to_f16x2(q3 & 0xFFFFu);
-            ao[3] = e4m3x2_to_f16x2(q3 >> 16);
+            e4m3x4_to_f16x2x2(q0, ae[0], ae[1]);
+            e4m3x4_to_f16x2x2(q2, ae[2], ae[3]);
+            e4m3x4_to_f16x2x2(q1, ao[0], ao[1]);
+            e4m3x4_to_f16x2x2(q3, ao[2], ao[3]);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               mma_f16(o[2 * pr][nt], ae, pb[sl][nt][0], pb[sl][nt][1]);
