@@ -414,7 +414,7 @@ def main():
     else:
         width = x.topk * x.kv_shape[3] if blocks else x.selection_width
         plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
-                          kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas)
+                          kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas, block_lists=blocks)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)

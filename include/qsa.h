@@ -151,7 +151,10 @@ typedef struct qsa_options {
                         tensor-core kernel (the default where it applies) */
   int32_t splits;    /* kernel 2: 0 auto, else CTAs per (row, kv head) */
   int32_t ctas;      /* kernel 3: 0 auto (one per SM), else the persistent grid size */
-  int32_t reserved[5];
+  int32_t block_lists; /* qsa_plan only: nonzero plans a qsa_msa_attention_ragged_paged
+                          call (block lists run kernel 2's variant with tile copies,
+                          whose occupancy differs); other entry points ignore it */
+  int32_t reserved[4];
 } qsa_options;
 
 /* Same as qsa_sparse_attention_ragged_paged, with explicit launch controls

@@ -32,7 +32,7 @@ class qsa_tensor(ctypes.Structure):
 
 class qsa_options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("splits", ctypes.c_int32), ("ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("block_lists", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
 
 class LibraryMissing(RuntimeError):
@@ -255,11 +255,11 @@ def qsa_latent_attention_ragged_paged(output, q, input_row_offsets, swa_blocks, 
 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,
-             kernel: int = 0, splits: int = 0, ctas: int = 0) -> dict:
+             kernel: int = 0, splits: int = 0, ctas: int = 0, block_lists: bool = False) -> dict:
     lib = load_library()
     k, s = ctypes.c_int32(), ctypes.c_int32()
     c, w = ctypes.c_int64(), ctypes.c_size_t()
-    opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas)
+    opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas, block_lists=int(bool(block_lists)))
     _check(lib.qsa_plan(dtype, total_q, num_kv_heads, head_dim, selection_width, group, ctypes.byref(opt),
                         ctypes.byref(k), ctypes.byref(s), ctypes.byref(c), ctypes.byref(w)))
     return {"kernel": k.value, "splits": s.value, "ctas": c.value, "workspace_bytes": w.value}

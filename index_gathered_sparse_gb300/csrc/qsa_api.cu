@@ -895,6 +895,7 @@ qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  R.tiles = options && options->block_lists && R.kernel == 2 ? 1 : 0;
   s = plan_launch(R, group, options, dev);
   if (s != QSA_OK) return s;
   if (kernel) *kernel = R.kernel;
