@@ -464,7 +464,11 @@ void encode_tile_map(Params& p, const void* kv, int elem, int64_t num_pages) {
   const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
   const CUresult r = encode(&p.tmap, elem == qsa::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
                             const_cast<void*>(kv), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                            CU_TENSOR_MAP_SWIZZLE_128B,
+                            // L2 fills as wide as one head's row: 256 B (bf16, both lines are
+                            // read) or 128 B (e4m3: a wider fill would bring in the next head's row)
+                            elem == qsa::kBF16 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return;
   p.tma = 1;
   p.tma_plane_k = (int32_t)(p.k_layer_bytes / plane);
