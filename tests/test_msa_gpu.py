@@ -56,6 +56,20 @@ def test_small_block_workloads_match_oracle(name, launch):
     assert B.qsa_read_device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("page_size", [32, 96, 192])
+@pytest.mark.parametrize("base", ["msa_bf16_prefill_small", "msa_fp8_decode_small"])
+def test_page_sizes_mix_tile_and_row_copies(base, page_size):
+    """Blocks of 96 or 192 slots straddle the 64-key tiles: whole-page tiles
+    (some starting mid-page) take tile copies, the straddling ones 16-byte
+    copies; blocks of 32 slots take 16-byte copies only.  Bands merge in a
+    cluster (3) or through the workspace tickets (12)."""
+    x = dataclasses.replace(SMALL[base], page_size=page_size).build()
+    ref = oracle.msa_attention(x)
+    for kw in (dict(), dict(splits=3), dict(splits=12)):
+        assert_close(run_gpu(x, **kw), ref, x.dtype, f"{base} P={page_size} {kw}")
+        assert B.qsa_read_device_status(clear=True) == 0
+
+
 def test_block_list_edge_cases():
     x = SMALL["msa_bf16_prefill_small"].build()
     P = x.kv_shape[3]

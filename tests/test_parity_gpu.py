@@ -65,9 +65,12 @@ def _launches(dtype):
     if dtype == "f32":
         return [dict(kernel=1)]
     # auto (the persistent stream-K kernel), the CUDA-core kernel, the per-unit
-    # tensor-core kernel with and without split-K, and stream-K grids small
-    # and large enough that units are shared by several CTAs
+    # tensor-core kernel without split-K, with bands merged inside a cluster
+    # (3, 8) and through the workspace tickets (12, 40: more bands than a
+    # cluster holds, some of them empty), and stream-K grids small and large
+    # enough that units are shared by several CTAs
     return [dict(), dict(kernel=1), dict(kernel=2, splits=1), dict(kernel=2, splits=3), dict(kernel=2, splits=8),
+            dict(kernel=2, splits=12), dict(kernel=2, splits=40),
             dict(kernel=3, ctas=1), dict(kernel=3, ctas=7), dict(kernel=3, ctas=64), dict(kernel=3, ctas=1000)]
 
 
