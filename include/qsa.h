@@ -322,7 +322,7 @@ QSA_API qsa_status qsa_read_device_status(void* stream, int32_t clear, uint32_t*
  * the GPU's memory for its own pools at start-up and passes plugins only
  * buffers it owns, or a latency-bound loop that cannot take the device-wide
  * synchronisation cudaMalloc/cudaFree imply.  This entry point is a library
- * addition; the paper has no counterpart.
+ * addition with no counterpart among the operations the method describes.
  *
  * It never calls cudaMalloc, cudaFree or any allocating routine.  It always
  * runs the persistent stream-K tensor-core kernel, so q / kv_blocks must be
