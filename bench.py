@@ -68,12 +68,38 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C/C++/CUDA source without comments and blank lines (string and
+    character literals kept), so comment edits do not change the hash."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(l.rstrip() for l in "".join(out).splitlines() if l.strip())
+
+
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources' code (comments ignored): recorded ncu
+    traffic is reported only while it matches."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "index_gathered_sparse_gb300", "csrc")
     for n in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, n), "rb") as f:
-            h.update(n.encode() + f.read())
+        with open(os.path.join(csrc, n), encoding="utf-8") as f:
+            h.update(n.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

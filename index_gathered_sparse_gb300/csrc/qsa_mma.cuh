@@ -17,12 +17,19 @@
 //
 // Memory.  CTA = 4 warps = one (row, kv head) unit, or one band of its
 // selection under split-K.  A prologue translates the band's positions into
-// 16-byte cache-row offsets once (page table lookups overlapped 8 deep per
-// thread) and keeps them in shared memory.  Gathered K and V rows then stream
-// through a cp.async ring of 64-key stages (16 keys per warp) with
-// STAGES - 1 stages in flight; rows are padded by 16 bytes in shared memory
-// so ldmatrix is conflict-free.  Skipped keys (past the band, or positions
-// that fail the range checks) are zero-filled by cp.async and masked to -inf.
+// 16-byte cache-row offsets once, in three dependent trips to memory (row
+// search, counts and Q; list entries; page table), and keeps them in shared
+// memory.  Gathered K and V rows then stream through a ring of 64-key stages
+// (16 keys per warp) with STAGES - 1 stages in flight.  Two variants:
+//   - 16-byte cp.async per row chunk into rows padded by 16 bytes (ldmatrix
+//     is conflict-free); skipped keys (past the band, or positions that fail
+//     the range checks) are zero-filled and masked to -inf;
+//   - for block lists, TILES: a tile of 64 consecutive slots of one page is
+//     one TMA tile copy per 128-byte line of K and of V into a 128-byte-
+//     swizzled layout, completing on a per-stage mbarrier; other tiles take
+//     16-byte copies into the same layout.
+// The bands of a unit merge through distributed shared memory when they form
+// one thread-block cluster (2 to 8 bands), else through a workspace ticket.
 #pragma once
 
 #include <cuda_bf16.h>
