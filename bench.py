@@ -69,8 +69,9 @@ def measured_peaks():
 
 
 def _code_only(text: str) -> str:
-    """C/C++/CUDA source without comments and blank lines (string and
-    character literals kept), so comment edits do not change the hash."""
+    """C/C++/CUDA source without comments, blank lines and runs of spaces
+    (string and character literals kept), so comment and layout edits do not
+    change the hash."""
     out, i, n = [], 0, len(text)
     while i < n:
         c = text[i]
@@ -89,7 +90,7 @@ def _code_only(text: str) -> str:
         else:
             out.append(c)
             i += 1
-    return "\n".join(l.rstrip() for l in "".join(out).splitlines() if l.strip())
+    return "\n".join(" ".join(l.split()) for l in "".join(out).splitlines() if l.strip())
 
 
 def kernel_source_hash() -> str:
