@@ -1,7 +1,8 @@
-"""GPU: the entry points inside a captured CUDA graph.  After the workspace of
-the capturing stream is reserved (qsa_plan's figure) and one warm-up call has
-run on it, a call captured with torch.cuda.graph and replayed writes the same
-output bits as a direct call.  Cases cover each launch form: the persistent
+"""GPU: qsa_sparse_attention_ragged_paged(_ex) and
+qsa_msa_attention_ragged_paged inside a captured CUDA graph.  After the
+workspace of the capturing stream is reserved (qsa_plan's figure) and one
+warm-up call has run on it, a call captured with torch.cuda.graph and
+replayed writes the same output bits as a direct call.  Cases cover each launch form: the persistent
 kernel, kernel 2 with bands merged inside a thread-block cluster
 (cudaLaunchKernelEx) and through the workspace tickets, and block lists
 with tile copies (a tensor map encoded on the host at capture time).
