@@ -566,7 +566,18 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
     p.head_bytes = 0;  // every query-head group reads the one latent head
   }
 
-  if (R.kernel == 2 && R.tiles) encode_tile_map(p, kv_blocks.data, R.elem, R.num_pages);
+  if (R.kernel == 2 && R.tiles) {
+    encode_tile_map(p, kv_blocks.data, R.elem, R.num_pages);
+    // grids of eight or more CTAs per SM (prefill-like: many waves, gathers
+    // mostly from L2) take the two-stage BF16 variant, three CTAs per SM;
+    // shorter grids keep three stages
+    int sms = 0;
+    {
+      std::lock_guard<std::mutex> lk(g_mu);
+      sms = g_dev[dev].sms;
+    }
+    p.shallow = R.elem == qsa::kBF16 && sms > 0 && R.ctas >= 8 * (int64_t)sms ? 1 : 0;
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (R.kernel == 1)

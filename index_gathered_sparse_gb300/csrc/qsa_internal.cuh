@@ -65,6 +65,7 @@ struct Params {
   // page_pitch_bytes), with a box of one line of 64 slots and the 128-byte
   // swizzle.  tma_plane_k / tma_plane_v: the planes of layer_idx.
   int32_t tma, tma_plane_k, tma_plane_v;
+  int32_t shallow;  // BF16 tile copies, group <= 8: the two-stage variant (three CTAs per SM)
   CUtensorMap tmap;
 };
 

@@ -43,8 +43,10 @@ namespace qsa {
 // TILES: the variant with tile copies (block lists, whose tiles are mostly
 // whole pages) and the 128-byte-swizzled stage layout they write; without,
 // 16-byte copies only into rows padded by 16 bytes (no tile-copy code in the
-// loop, which measurably slows the per-row path).
-template <int KIND, bool TILES>
+// loop, which measurably slows the per-row path).  SHALLOW (BF16 tile copies
+// only): two stages instead of three, so three CTAs fit on an SM, for grids
+// of many waves whose gathers mostly hit L2.
+template <int KIND, bool TILES, bool SHALLOW = false>
 struct MmaCfg {
   static constexpr int D = 128;
   static constexpr int ELEM = KIND == kBF16 ? 2 : 1;
@@ -55,7 +57,7 @@ struct MmaCfg {
   static constexpr int SROW = ROWB + 16;           // padded shared-memory row (16-byte copies only)
   static constexpr int KV_BYTES = TILES ? LINES * LINE_BYTES : TILE * SROW;  // the K (or V) half of a stage
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr int STAGES = KIND == kBF16 ? 3 : 4;
+  static constexpr int STAGES = KIND == kBF16 ? (SHALLOW ? 2 : 3) : 4;
   static constexpr int RING = STAGES * STAGE_BYTES;
   static constexpr int CPR = ROWB / 16;            // 16-byte chunks per row
   static constexpr int KSTEPS = KIND == kBF16 ? 8 : 4;  // MMA k-steps over head_dim for S
@@ -397,9 +399,9 @@ __device__ __forceinline__ void finish_unit_mma(const Params& p, int r, int h, i
   cluster_sync_all();
 }
 
-template <int KIND, int NT, bool TILES>
+template <int KIND, int NT, bool TILES, bool SHALLOW>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ Params p) {
-  using C = MmaCfg<KIND, TILES>;
+  using C = MmaCfg<KIND, TILES, SHALLOW>;
   constexpr int NW = kMmaThreads / 32;
   constexpr int GP = 8 * NT;  // padded query heads
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -816,14 +818,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   finish_unit_mma<NW>(p, r, h, split, row_ok, sm_m, sm_l, sm_o, GP, scratch, part, s_e);
 }
 
-template <int KIND, int NT, bool TILES>
+template <int KIND, int NT, bool TILES, bool SHALLOW>
 cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
-  using C = MmaCfg<KIND, TILES>;
+  using C = MmaCfg<KIND, TILES, SHALLOW>;
   static int configured_mask = 0;  // one bit per device (up to 32)
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, SHALLOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured_mask |= 1 << (dev & 31);
   }
@@ -843,14 +845,18 @@ cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES>, p);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES, SHALLOW>, p);
   }
-  mma_kernel<KIND, NT, TILES><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
+  mma_kernel<KIND, NT, TILES, SHALLOW><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
   return cudaGetLastError();
 }
 template <int KIND, int NT>
 cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
-  return p.tma ? launch_mma_t<KIND, NT, true>(p, s) : launch_mma_t<KIND, NT, false>(p, s);
+  if (!p.tma) return launch_mma_t<KIND, NT, false, false>(p, s);
+  // (groups of up to 8 heads: with two N tiles the registers allow two CTAs anyway)
+  if constexpr (KIND == kBF16 && NT == 1)
+    if (p.shallow) return launch_mma_t<KIND, NT, true, true>(p, s);
+  return launch_mma_t<KIND, NT, true, false>(p, s);
 }
 
 // Clusters of `splits` CTAs of the tensor-core kernel that can be resident
@@ -858,7 +864,7 @@ cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
 template <int KIND, int NT, bool TILES>
 int mma_max_clusters_nt(int splits) {
   using C = MmaCfg<KIND, TILES>;
-  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)splits);
@@ -872,7 +878,7 @@ int mma_max_clusters_nt(int splits) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();  // a refused query is not a launch error
     return 0;
   }
@@ -888,8 +894,8 @@ template <int KIND, int NT, bool TILES>
 int mma_occupancy_nt() {
   using C = MmaCfg<KIND, TILES>;
   int n = 0;
-  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES>, kMmaThreads, C::SMEM);
+  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES, false>, kMmaThreads, C::SMEM);
   return n > 0 ? n : 1;
 }
 template <int KIND>
