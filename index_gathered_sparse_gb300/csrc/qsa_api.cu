@@ -67,6 +67,7 @@ struct Resolved {
   int splits = 1;
   int cluster = 0;  // kernel 2: the bands of a unit merge inside one thread-block cluster
   int tiles = 0;    // kernel 2: the variant with tile copies (block lists)
+  int groups = 0;   // kernel 2, latent mode: a CTA serves four head groups of a row
   int band = 0;
   int64_t ctas = 0;
   size_t ws_partial_bytes = 0, ws_bytes = 0;
@@ -544,6 +545,7 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
   p.out_bf16 = R.out_bf16;
   p.splits = R.splits;
   p.cluster = R.cluster;
+  p.groups = R.groups;
   p.band = R.band;
   if (lat) {
     p.comp = lat->comp;
@@ -771,6 +773,13 @@ qsa_status qsa_latent_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qs
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   qsa_status s = plan_launch(R, (int32_t)group, &opt, dev);
   if (s != QSA_OK) return s;
+  // with one band and the 16-head groups in fours, a CTA serves four groups
+  // of a row (one gather of each key for the four)
+  if (R.splits == 1 && group == 16 && R.nkv % 4 == 0) {
+    R.groups = 1;
+    R.nkv /= 4;
+    R.ctas = R.total_q * R.nkv;
+  }
   LatentArgs lat;
   lat.comp = comp_indices;
   lat.sinks = attn_sink;

@@ -66,6 +66,7 @@ struct Params {
   // swizzle.  tma_plane_k / tma_plane_v: the planes of layer_idx.
   int32_t tma, tma_plane_k, tma_plane_v;
   int32_t shallow;  // BF16 tile copies, group <= 8: the two-stage variant (three CTAs per SM)
+  int32_t groups;   // latent mode, one band, group 16: a CTA serves four head groups (nkv = groups / 4)
   CUtensorMap tmap;
 };
 

@@ -399,7 +399,11 @@ __device__ __forceinline__ void finish_unit_mma(const Params& p, int r, int h, i
   cluster_sync_all();
 }
 
-template <int KIND, int NT, bool TILES, bool SHALLOW>
+// GROUPS (latent mode, one band): a CTA serves NW query-head groups of one
+// row that read the same keys; warp w owns group w over every key of a tile
+// (all NW 16-key slices) and writes its heads from registers, so each key is
+// gathered once per row instead of once per group.
+template <int KIND, int NT, bool TILES, bool SHALLOW, bool GROUPS>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ Params p) {
   using C = MmaCfg<KIND, TILES, SHALLOW>;
   constexpr int NW = kMmaThreads / 32;
@@ -427,6 +431,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   const int split = cta % p.splits;
   cta /= p.splits;
   const int h = cta % p.nkv;
+  const int qh = GROUPS ? h * NW + warp : h;  // the query-head group of this thread's heads
   const int r = p.total_q - 1 - cta / p.nkv;
   const bool block_sel = p.blocks != nullptr;
   const bool latent = p.comp != nullptr;
@@ -446,7 +451,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   for (int nt = 0; nt < NT; ++nt) {
     const int head = nt * 8 + gid;
     const bool live = head < p.group;
-    const unsigned char* qrow = p.q + (((int64_t)r * p.nq + (int64_t)h * p.group + (live ? head : 0)) * C::D) * C::ELEM;
+    const unsigned char* qrow = p.q + (((int64_t)r * p.nq + (int64_t)qh * p.group + (live ? head : 0)) * C::D) * C::ELEM;
 #pragma unroll
     for (int ks = 0; ks < C::KSTEPS; ++ks) {
       // bf16: k-step of 16 elements, thread pair (2 tig, 2 tig + 1) and +8
@@ -675,13 +680,16 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     }
 
     const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
-    const int kA = t * C::TILE + warp * 16 + gid, kB = kA + 8;
+#pragma unroll 1
+    for (int sl = 0; sl < (GROUPS ? NW : 1); ++sl) {
+    const int kw = GROUPS ? sl : warp;  // the 16-key slice of the tile this warp scores
+    const int kA = t * C::TILE + kw * 16 + gid, kB = kA + 8;
     const bool vA = kA < band_keys && s_off[kA] != kInvalidOff;
     const bool vB = kB < band_keys && s_off[kB] != kInvalidOff;
     if (!__any_sync(0xffffffffu, vA || vB)) continue;
     constexpr uint32_t RS = TILES ? 128u : (uint32_t)C::SROW;  // row stride of a stage half
-    const uint32_t krow = smem_addr(sb) + (uint32_t)(warp * 16 + a_row) * RS;
-    const uint32_t vrow = smem_addr(sb + C::KV_BYTES) + (uint32_t)(warp * 16 + t_row) * RS;
+    const uint32_t krow = smem_addr(sb) + (uint32_t)(kw * 16 + a_row) * RS;
+    const uint32_t vrow = smem_addr(sb + C::KV_BYTES) + (uint32_t)(kw * 16 + t_row) * RS;
 
     // S^T = K Q^T over head_dim
     float s[NT][4];
@@ -776,10 +784,42 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
         }
       }
     }
+    }  // slices
   }
   if (timed_out) atomicOr(p.status, QSA_STATUS_TIMEOUT);
   cp_async_wait<0>();
   __syncthreads();  // the ring is drained; its shared memory now holds the warp states
+
+  if constexpr (GROUPS) {
+    // this warp holds the whole softmax state of its group's heads: sums
+    // across its key lanes, then the output straight from registers
+    const int64_t ob = ((int64_t)r * p.nq + (int64_t)qh * p.group) * C::D;
+    float inv[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        float l = l_run[nt][c];
+        l += __shfl_xor_sync(0xffffffffu, l, 4);
+        l += __shfl_xor_sync(0xffffffffu, l, 8);
+        l += __shfl_xor_sync(0xffffffffu, l, 16);
+        const int head = nt * 8 + 2 * tig + c;
+        const float M = m_run[nt][c];
+        const bool live = row_ok && head < p.group && M != -CUDART_INF_F;
+        inv[nt][c] = live ? 1.f / (l + sink_term(p, qh * p.group + head, M)) : 0.f;
+      }
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int head = nt * 8 + 2 * tig + (c & 1);
+          const int d = KIND == kBF16 ? mt * 16 + gid + (c >> 1) * 8 : mt * 16 + 2 * gid + (c >> 1);
+          if (head < p.group) store_out(p, ob + (int64_t)head * C::D + d, o[mt][nt][c] * inv[nt][c & 1]);
+        }
+    return;
+  }
 
   float* sm_o = reinterpret_cast<float*>(smem);  // [NW][GP][D]
   float* sm_m = sm_o + NW * GP * C::D;
@@ -818,14 +858,14 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   finish_unit_mma<NW>(p, r, h, split, row_ok, sm_m, sm_l, sm_o, GP, scratch, part, s_e);
 }
 
-template <int KIND, int NT, bool TILES, bool SHALLOW>
+template <int KIND, int NT, bool TILES, bool SHALLOW, bool GROUPS = false>
 cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
   using C = MmaCfg<KIND, TILES, SHALLOW>;
   static int configured_mask = 0;  // one bit per device (up to 32)
   int dev = 0;
   cudaGetDevice(&dev);
   if (!(configured_mask & (1 << (dev & 31)))) {
-    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, SHALLOW>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     configured_mask |= 1 << (dev & 31);
   }
@@ -845,14 +885,18 @@ cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES, SHALLOW>, p);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS>, p);
   }
-  mma_kernel<KIND, NT, TILES, SHALLOW><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
+  mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
   return cudaGetLastError();
 }
 template <int KIND, int NT>
 cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
-  if (!p.tma) return launch_mma_t<KIND, NT, false, false>(p, s);
+  if (!p.tma) {
+    if constexpr (NT == 2)
+      if (p.groups) return launch_mma_t<KIND, NT, false, false, true>(p, s);
+    return launch_mma_t<KIND, NT, false, false>(p, s);
+  }
   // (groups of up to 8 heads: with two N tiles the registers allow two CTAs anyway)
   if constexpr (KIND == kBF16 && NT == 1)
     if (p.shallow) return launch_mma_t<KIND, NT, true, true>(p, s);
@@ -864,7 +908,7 @@ cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
 template <int KIND, int NT, bool TILES>
 int mma_max_clusters_nt(int splits) {
   using C = MmaCfg<KIND, TILES>;
-  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)splits);
@@ -878,7 +922,7 @@ int mma_max_clusters_nt(int splits) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES, false, false>, &cfg) != cudaSuccess) {
     cudaGetLastError();  // a refused query is not a launch error
     return 0;
   }
@@ -894,8 +938,8 @@ template <int KIND, int NT, bool TILES>
 int mma_occupancy_nt() {
   using C = MmaCfg<KIND, TILES>;
   int n = 0;
-  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES, false>, kMmaThreads, C::SMEM);
+  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES, false, false>, kMmaThreads, C::SMEM);
   return n > 0 ? n : 1;
 }
 template <int KIND>

@@ -54,6 +54,18 @@ def test_small_latent_matches_oracle(name, launch):
     assert B.qsa_read_device_status(clear=True) == 0
 
 
+@pytest.mark.parametrize("num_heads", [64, 128])
+def test_head_groups_in_fours(num_heads):
+    """64 or 128 query heads (4 or 8 groups of 16): with one band a CTA serves
+    four groups of a row, one warp per group over every key; with three bands
+    each group is its own unit again.  Both match the oracle."""
+    x = dataclasses.replace(SMALL["latent_bf16_prefill_small"], num_heads=num_heads).build()
+    ref = oracle.latent_attention(x)
+    for kw in (dict(), dict(splits=1), dict(splits=3)):
+        assert_close(run_gpu(x, **kw), ref, x.dtype, f"{num_heads} heads {kw}")
+        assert B.qsa_read_device_status(clear=True) == 0
+
+
 def test_without_sinks_and_single_sources():
     spec = SMALL["latent_bf16_prefill_small"]
     x = spec.build()
