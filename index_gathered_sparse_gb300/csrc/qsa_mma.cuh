@@ -30,6 +30,9 @@
 //     16-byte copies into the same layout.
 // The bands of a unit merge through distributed shared memory when they form
 // one thread-block cluster (2 to 8 bands), else through a workspace ticket.
+// BF16 tile copies on grids of many waves use two stages (three CTAs per SM);
+// latent rows whose 16-head groups come in fours run one CTA for four groups,
+// a warp per group over every key (each key gathered once per row).
 #pragma once
 
 #include <cuda_bf16.h>
