@@ -562,6 +562,9 @@ def main():
         cfg = workload_config(x)
         cfg.update({"kernel": plan["kernel"], "splits": plan["splits"], "ctas": plan["ctas"],
                     "parallelism": f"replicas x{world}"})
+        if latent and plan["splits"] == 1 and (x.num_heads // min(x.num_heads, 16)) % 4 == 0:
+            # the launch serves four 16-head groups of a row per CTA (qsa_plan counts one per group)
+            cfg["ctas"] = plan["ctas"] // 4
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
