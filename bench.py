@@ -3,18 +3,22 @@
 
 A step is one call of the whole hot path (row -> sequence lookup, selection
 read, page translation, K/V gather, online softmax, split-K combine, output)
-over one batch of the bf16 decode workload: 64 sequences with one new token
-each, cache lengths U[1024, 8192], 32 query heads on 8 kv heads, head_dim 128,
-page 128, 4 layers (layer 2), selection width 2048.  Inputs are synthetic and
-seeded.  The cache is 4.8 GB and each step gathers ~0.52 GB of random rows;
-L2 is flushed before every timed step: a 2x-L2 buffer is written, then a
-second 2x-L2 buffer is read, so neither the workload nor dirty flush lines
-sit in L2 when the timed call starts.
+over one batch of the bf16 chunked-prefill workload: 4 sequences with
+[512, 1024, 256, 2048] new rows on cached lengths [0, 4096, 16384, 8192], 64
+query heads on 8 kv heads, head_dim 128, page 64, selection width 2048 (the
+64 positions nearest each row plus distinct uniform picks of the rest).
+Inputs are synthetic and seeded.  Each step attends 55.6 M (key, kv head)
+pairs, 28.6 GB of algorithmic K/V bytes over a 133 MB cache, so most gathers
+are L2 hits; the roofline line is therefore the tensor (flop) bound, with the
+DRAM fraction beside it.  L2 is flushed before every timed step: a 2x-L2
+buffer is written, then a second 2x-L2 buffer is read, so neither the
+workload nor dirty flush lines sit in L2 when the timed call starts.
+``--workload`` picks any other workload (bf16_decode, fp8_mixed, ...).
 
 One JSON line on stdout (rank 0).  ``--impl reference`` times the float64 CPU
-oracle on a bounded sample of the same workload instead.  Under torchrun each
-rank runs its own replica (the op shards with no exchange), timings are
-max-reduced and ``value`` is the aggregate over ranks.
+oracle on a bounded sample of the same workload instead, on every host core.
+Under torchrun each rank runs its own replica (the op shards with no
+exchange), timings are max-reduced and ``value`` is the aggregate over ranks.
 """
 from __future__ import annotations
 
@@ -33,6 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "sparse attn query-tokens/s per layer; effective HBM GB/s (% of GB300 peak)"
 UNIT = "query-tokens/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -42,11 +48,13 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="bf16_decode")
+    ap.add_argument("--workload", default="bf16_chunked_prefill")
     ap.add_argument("--kernel", type=int, default=0, help="force 1 CUDA-core / 2 tensor-core kernel")
     ap.add_argument("--splits", type=int, default=0, help="kernel 2: force CTAs per (row, kv head)")
     ap.add_argument("--ctas", type=int, default=0, help="kernel 3: force the persistent grid size")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle time budget of the CPU baseline")
+    ap.add_argument("--heads-per-unit", type=int, default=0, help="kernel 3: force the kv heads per unit")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of the CPU baseline")
+    ap.add_argument("--cpu-threads", type=int, default=0, help="oracle threads (0: every core this process may use)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--min-warmup-s", type=float, default=1.0,
@@ -59,13 +67,62 @@ def dist_env():
     return int(os.environ.get("RANK", "0")), ws, int(os.environ.get("LOCAL_RANK", "0"))
 
 
-def measured_peaks():
+def measured_peaks() -> dict:
+    """Roofline denominators: MEASURED_PEAKS.json (measured copy
+    bandwidth and cuBLAS bf16 rates) when present, else the fallbacks."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             pk = json.load(f)
-        return float(pk["hbm_gbs"]), "measured"
+        return {"hbm_gbs": float(pk["hbm_gbs"]), "bf16_tflops": float(pk["bf16_tflops"]),
+                "bf16_tflops_sustained": float(pk["bf16_tflops_sustained"]), "source": "measured"}
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": FALLBACK_BF16_TFLOPS_SUSTAINED, "source": "fallback"}
+
+
+def host_cores() -> int:
+    """Cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def roofline(x, ms: float, kernel: str, traffic) -> dict:
+    """The roofline entry of the dominant kernel.
+
+    Algorithmic bytes: every attended K and V row once per (row, kv head),
+    plus q, output, indices and counts.  Algorithmic flops: 4 * group *
+    head_dim per attended (key, kv head) pair (q.K and p.V).  When the
+    attended K/V bytes exceed twice the distinct K/V bytes the selections
+    name, the repeats are L2 hits and HBM does not bound the call: the line
+    is then the tensor bound (bf16 sustained rate; FP8 runs q.K at twice that
+    rate and p.V at the f16 rate, so 4/3 of it), with the DRAM fraction (from
+    the recorded traffic) beside it.  Otherwise it is the HBM bound."""
+    pk = measured_peaks()
+    t = ms / 1e3
+    alg = x.algorithmic_bytes()
+    eff_gbs = alg / t / 1e9
+    dram = None
+    if traffic:
+        dram = {"achieved": traffic / t / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": traffic / t / 1e9 / pk["hbm_gbs"], "traffic": traffic}
+    pairs = x.attended_pairs()
+    kv_alg = pairs * 2 * x.head_dim * (1 if x.dtype == "e4m3" else 2 if x.dtype == "bf16" else 4)
+    distinct = x.distinct_kv_bytes()
+    reuse = kv_alg / distinct if distinct else 1.0
+    common = {"kernel": kernel, "traffic": traffic, "algorithmic_bytes_per_launch": alg,
+              "l2_reuse": reuse, "effective_gbs": eff_gbs, "dram": dram}
+    if reuse >= 2.0 and x.dtype in ("bf16", "e4m3"):
+        flops = 4 * x.group * x.head_dim * pairs
+        peak = pk["bf16_tflops_sustained"] * (4.0 / 3.0 if x.dtype == "e4m3" else 1.0)
+        ach = flops / t / 1e12
+        return {"bound": "tensor", "achieved": ach, "peak": peak, "unit": "TFLOP/s", "frac": ach / peak,
+                "peak_source": f"{pk['source']} (MEASURED_PEAKS bf16_tflops_sustained"
+                               f"{' x 4/3: fp8 q.K at 2x, p.V at 1x' if x.dtype == 'e4m3' else ''})",
+                "flops_per_launch": flops, **common}
+    return {"bound": "hbm", "achieved": eff_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": eff_gbs / pk["hbm_gbs"],
+            "peak_source": f"{pk['source']} (MEASURED_PEAKS hbm_gbs copy)", **common}
 
 
 def _code_only(text: str) -> str:
@@ -210,23 +267,51 @@ def oracle_fn(x):
     return oracle.msa_attention if is_block_sparse(x) else oracle.sparse_attention
 
 
-def cpu_oracle_rate(x, seconds: float, rows_per_call: int = 1):
-    """Rows per second of the float64 oracle on this host, one thread."""
+def cpu_oracle_rate(x, seconds: float, threads: int = 1):
+    """Rows per second of the float64 oracle on this host: ``threads``
+    threads each take the next sampled row until ``seconds`` have passed
+    (the C oracle runs outside the interpreter lock, so the threads run on
+    separate cores).  Returns (rate, rows done, elapsed seconds)."""
+    import itertools
+    from concurrent.futures import ThreadPoolExecutor
+
     run = oracle_fn(x)
     rows = sample_rows(x.total_q)
-    done, t0 = 0, time.perf_counter()
-    while True:
-        sel = rows[done % rows.size: done % rows.size + rows_per_call]
-        run(x, sel)
-        done += sel.size
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            return done / el, done, el
+    ticket = itertools.count()
+    t0 = time.perf_counter()
+    stop = t0 + seconds
+
+    def worker():
+        done = 0
+        while time.perf_counter() < stop:
+            k = next(ticket) % rows.size
+            run(x, rows[k:k + 1])
+            done += 1
+        return done
+
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = [ex.submit(worker) for _ in range(threads)]
+        done = sum(f.result() for f in futs)
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def cpu_baseline(x, seconds: float, threads: int) -> dict:
+    """The oracle timed on the host cores: every core (the reported value)
+    and one thread beside it, on sampled rows of the same workload."""
+    one_s = max(1.0, seconds / 4)
+    r1, n1, e1 = cpu_oracle_rate(x, one_s, 1)
+    rn, nn, en = cpu_oracle_rate(x, max(1.0, seconds - one_s), threads)
+    return {"value": rn, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{nn} query rows of {x.name} (all heads, full selections) in {en:.1f}s on {threads} "
+                      f"threads; one thread: {n1} rows in {e1:.1f}s",
+            "one_thread": {"value": r1, "unit": UNIT, "cores": 1}}
 
 
 def run_reference(args, x, rank, world):
-    """The reference arm: the float64 CPU oracle timed on the host cores."""
+    """The reference arm: the float64 CPU oracle timed on every host core."""
     import numpy as np
+    from concurrent.futures import ThreadPoolExecutor
 
     import oracle
 
@@ -235,16 +320,19 @@ def run_reference(args, x, rank, world):
     oracle.build()
     run = oracle_fn(x)
     rows = sample_rows(x.total_q)
+    threads = args.cpu_threads or host_cores()
     t0 = time.perf_counter()
     run(x, rows[:1])
     per_row = time.perf_counter() - t0
-    rows_per_step = max(1, int(round(0.5 / max(per_row, 1e-6))))
+    # a step is about half a second of all-core work
+    rows_per_step = max(threads, int(round(0.5 * threads / max(per_row, 1e-6))))
     k = 0
+    ex = ThreadPoolExecutor(max_workers=threads)
 
     def step():
         nonlocal k
         sel = np.take(rows, np.arange(k, k + rows_per_step), mode="wrap")
-        run(x, sel)
+        list(ex.map(lambda r: run(x, sel[r:r + 1]), range(sel.size)))
         k += rows_per_step
 
     for _ in range(args.warmup):
@@ -253,14 +341,16 @@ def run_reference(args, x, rank, world):
     for _ in range(args.steps):
         step()
     el = time.perf_counter() - t0
+    ex.shutdown()
     value = rows_per_step * args.steps / el
-    sample = f"{rows_per_step} query row(s) of the {x.name} workload per step (all heads, full selections)"
+    sample = (f"{rows_per_step} query row(s) of the {x.name} workload per step (all heads, full selections), "
+              f"one row per oracle call on {threads} threads")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded numpy)", "config": workload_config(x),
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -352,7 +442,8 @@ def run_compress(args, spec, rank, world, local):
     ms = sum(per_step) / args.steps
     flags = B.qsa_read_device_status(clear=True)
     alg = x.algorithmic_bytes()
-    peak, peak_src = measured_peaks()
+    pk = measured_peaks()
+    peak, peak_src = pk["hbm_gbs"], pk["source"]
     achieved = alg / (ms / 1e3) / 1e9
     # end to end: counts and page table in from pinned memory, block keys back
     host = {k: d[k].cpu().pin_memory() for k in ("key_counts", "cache_lengths", "kv_lookup_table")}
@@ -441,7 +532,8 @@ def main():
     else:
         width = x.topk * x.kv_shape[3] if blocks else x.selection_width
         plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
-                          kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas, block_lists=blocks)
+                          kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas, block_lists=blocks,
+                          heads_per_unit=0 if blocks else args.heads_per_unit)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
@@ -465,7 +557,8 @@ def main():
         elif blocks:
             B.qsa_msa_attention_ragged_paged(**d, splits=args.splits)
         else:
-            B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas)
+            B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas,
+                                                heads_per_unit=args.heads_per_unit)
 
     def barrier():
         torch.cuda.synchronize()
@@ -541,27 +634,33 @@ def main():
         e2e = {"value": aggregate_rate(x.total_q, world, te / n_e2e), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e}
 
-    alg_bytes = x.algorithmic_bytes()
-    peak, peak_src = measured_peaks()
-    achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
-    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": recorded_traffic(x.name), "peak_source": f"{peak_src} (MEASURED_PEAKS hbm_gbs copy)",
-                "kernel": {1: "qsa simt_kernel", 2: "qsa mma_kernel", 3: "qsa stream_kernel"}[plan["kernel"]],
+    kname = {1: "qsa simt_kernel", 2: "qsa mma_kernel", 3: "qsa stream_kernel"}[plan["kernel"]]
+    if latent:
+        alg_bytes = x.algorithmic_bytes()
+        peak = measured_peaks()
+        achieved = alg_bytes / (ms_per_step / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peak["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peak["hbm_gbs"], "traffic": recorded_traffic(x.name),
+                "peak_source": f"{peak['source']} (MEASURED_PEAKS hbm_gbs copy)", "kernel": kname,
                 "algorithmic_bytes_per_launch": alg_bytes}
+    else:
+        roof = roofline(x, ms_per_step, kname, recorded_traffic(x.name))
+        alg_bytes = roof["algorithmic_bytes_per_launch"]
+        achieved = roof["effective_gbs"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
 
         oracle.build()
-        rate, rows, el = cpu_oracle_rate(x, args.cpu_seconds)
-        cpu = {"value": rate, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{rows} query rows of {x.name} (all heads, full selections) in {el:.1f}s, one thread"}
+        cpu = cpu_baseline(x, args.cpu_seconds, args.cpu_threads or host_cores())
 
     if rank == 0:
         cfg = workload_config(x)
         cfg.update({"kernel": plan["kernel"], "splits": plan["splits"], "ctas": plan["ctas"],
                     "parallelism": f"replicas x{world}"})
+        if args.heads_per_unit:
+            cfg["heads_per_unit"] = args.heads_per_unit
         if latent and plan["splits"] == 1 and (x.num_heads // min(x.num_heads, 16)) % 4 == 0:
             # the launch serves four 16-head groups of a row per CTA (qsa_plan counts one per group)
             cfg["ctas"] = plan["ctas"] // 4
@@ -571,7 +670,7 @@ def main():
             "vs_baseline": None, "dtype": x.dtype, "data": "synthetic (seeded numpy)", "config": cfg,
             "ms_per_step_median": sorted(per_step)[len(per_step) // 2], "ms_per_step_min": min(per_step),
             "effective_gbs": achieved, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": args.steps,
             "clocks": clocks, "device_status": flags,
         }
         print(json.dumps(line), flush=True)

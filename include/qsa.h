@@ -154,7 +154,16 @@ typedef struct qsa_options {
   int32_t block_lists; /* qsa_plan only: nonzero plans a qsa_msa_attention_ragged_paged
                           call (block lists run kernel 2's variant with tile copies,
                           whose occupancy differs); other entry points ignore it */
-  int32_t reserved[4];
+  int32_t heads_per_unit; /* kernel 3: 0 auto, else the adjacent kv heads one unit gathers
+                             together (1, 2, 4 or 8, dividing num_kv_heads; 8 needs group <= 8) */
+  int32_t test_stall;  /* tests only: nonzero makes kernel 3's producers issue no K/V
+                          copies and every wait give up after a few thousand polls, so
+                          the call ends early with QSA_STATUS_TIMEOUT and an undefined
+                          output; no copy is in flight when a CTA gives up */
+  int32_t tcgen05;     /* kernel 2: 0 auto, 1 the tcgen05 consumer (BF16: scores and output
+                          accumulate in tensor memory; the stage layout of tile copies),
+                          -1 the mma.sync consumer */
+  int32_t reserved[1];
 } qsa_options;
 
 /* Same as qsa_sparse_attention_ragged_paged, with explicit launch controls
@@ -343,8 +352,11 @@ QSA_API qsa_status qsa_read_device_status(void* stream, int32_t clear, uint32_t*
  *
  * Set-up: the first call on a device (with that device current) looks up the
  * scratch array's device address once and keeps it; make that first call
- * before any stream capture begins.  Each call then enqueues a clear of the
- * tickets and the kernel on `stream`.
+ * before any stream capture begins.  qsa_release_device_state forgets the
+ * address (a device reset drops it), and the call after it looks it up again,
+ * so that call too must come before any capture.  Each call then enqueues a
+ * clear of the tickets and the kernel on `stream`.  Argument errors are
+ * reported before any CUDA call.
  *
  * Every call on a device uses the same scratch, which keeps what the last
  * call left there: calls whose GPU work overlaps (different streams, or

@@ -22,7 +22,7 @@ QSA_F32, QSA_BF16, QSA_F8E4M3, QSA_U32, QSA_I32 = range(5)
 QSA_OK = 0
 STATUS_NAMES = {0: "QSA_OK", 1: "QSA_ERR_NULL", 2: "QSA_ERR_SHAPE", 3: "QSA_ERR_DTYPE",
                 4: "QSA_ERR_UNSUPPORTED", 5: "QSA_ERR_ARG", 6: "QSA_ERR_CUDA"}
-QSA_STATUS_BAD_INDEX, QSA_STATUS_BAD_PAGE, QSA_STATUS_BAD_ROW = 1, 2, 4
+QSA_STATUS_BAD_INDEX, QSA_STATUS_BAD_PAGE, QSA_STATUS_BAD_ROW, QSA_STATUS_TIMEOUT = 1, 2, 4, 8
 
 
 class qsa_tensor(ctypes.Structure):
@@ -32,7 +32,8 @@ class qsa_tensor(ctypes.Structure):
 
 class qsa_options(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int32), ("splits", ctypes.c_int32), ("ctas", ctypes.c_int32),
-                ("block_lists", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("block_lists", ctypes.c_int32), ("heads_per_unit", ctypes.c_int32), ("test_stall", ctypes.c_int32),
+                ("tcgen05", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 class LibraryMissing(RuntimeError):
@@ -159,11 +160,13 @@ def _kv_desc(kv: torch.Tensor, page_stride: int) -> qsa_tensor:
 def qsa_sparse_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
                                       kv_lookup_table, max_prompt_length, max_cache_length, layer_idx,
                                       token_indices, counts, scale, group, stream=None, *, kernel: int = 0,
-                                      splits: int = 0, ctas: int = 0) -> None:
+                                      splits: int = 0, ctas: int = 0, heads_per_unit: int = 0,
+                                      test_stall: int = 0, tcgen05: int = 0) -> None:
     """One layer of QSA sparse attention on the GPU (asynchronous on
-    ``stream``, default: PyTorch's current stream).  Raises QSAError on a
-    non-OK status.  ``kernel`` / ``splits`` / ``ctas`` force a launch choice
-    (tests and sweeps; see qsa_options)."""
+    ``stream``, default: PyTorch's current stream), with ``q``'s device
+    current.  Raises QSAError on a non-OK status.  ``kernel`` / ``splits`` /
+    ``ctas`` / ``heads_per_unit`` / ``tcgen05`` force a launch choice and
+    ``test_stall`` drives the give-up path (tests and sweeps; see qsa_options)."""
     lib = load_library()
     if stream is None:
         stream = torch.cuda.current_stream(q.device).cuda_stream
@@ -175,16 +178,19 @@ def qsa_sparse_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, p
         int(max_cache_length), int(layer_idx), _contig(token_indices, "token_indices"), _contig(counts, "counts"),
         float(scale), int(group), ctypes.c_void_p(stream),
     ]
-    if kernel or splits or ctas:
-        opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas)
-        _check(lib.qsa_sparse_attention_ragged_paged_ex(*args, ctypes.byref(opt)))
-    else:
-        _check(lib.qsa_sparse_attention_ragged_paged(*args))
+    with torch.cuda.device(q.device):  # the library resolves everything on the current device
+        if kernel or splits or ctas or heads_per_unit or test_stall or tcgen05:
+            opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas, heads_per_unit=heads_per_unit,
+                              test_stall=test_stall, tcgen05=tcgen05)
+            _check(lib.qsa_sparse_attention_ragged_paged_ex(*args, ctypes.byref(opt)))
+        else:
+            _check(lib.qsa_sparse_attention_ragged_paged(*args))
 
 
 def qsa_msa_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths,
                                    kv_lookup_table, max_prompt_length, max_cache_length, layer_idx, d_indices,
-                                   scale, group, stream=None, *, kernel: int = 0, splits: int = 0) -> None:
+                                   scale, group, stream=None, *, kernel: int = 0, splits: int = 0,
+                                   tcgen05: int = 0) -> None:
     """Block-sparse attention on the GPU: ``d_indices`` [num_kv_heads, total_q,
     topk] int32 lists whole blocks (pages) per (kv head, row); see qsa.h."""
     lib = load_library()
@@ -194,12 +200,13 @@ def qsa_msa_attention_ragged_paged(output, q, input_row_offsets, kv_blocks, page
         stream = stream.cuda_stream
     if d_indices.dtype != torch.int32:
         raise TypeError("d_indices must be int32")
-    opt = qsa_options(kernel=kernel, splits=splits, ctas=0)
-    _check(lib.qsa_msa_attention_ragged_paged(
-        _contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets), _kv_desc(kv_blocks, int(page_stride)),
-        int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length),
-        int(max_cache_length), int(layer_idx), _contig(d_indices, "d_indices"), float(scale), int(group),
-        ctypes.c_void_p(stream), ctypes.byref(opt)))
+    opt = qsa_options(kernel=kernel, splits=splits, ctas=0, tcgen05=tcgen05)
+    args = (_contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets), _kv_desc(kv_blocks, int(page_stride)),
+            int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length),
+            int(max_cache_length), int(layer_idx), _contig(d_indices, "d_indices"), float(scale), int(group),
+            ctypes.c_void_p(stream), ctypes.byref(opt))
+    with torch.cuda.device(q.device):
+        _check(lib.qsa_msa_attention_ragged_paged(*args))
 
 
 def qsa_compress_keys_paged(block_keys, gamma, freqs_cis, key_counts, kv_blocks, page_stride, cache_lengths,
@@ -214,11 +221,12 @@ def qsa_compress_keys_paged(block_keys, gamma, freqs_cis, key_counts, kv_blocks,
         stream = stream.cuda_stream
     if key_counts.dtype != torch.int32:
         raise TypeError("key_counts must be int32")
-    _check(lib.qsa_compress_keys_paged(
-        _contig(block_keys, "block_keys"), _contig(gamma, "gamma"), _contig(freqs_cis, "freqs_cis"),
-        _contig(key_counts, "key_counts"), _kv_desc(kv_blocks, int(page_stride)), int(page_stride),
-        _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length), int(max_cache_length), int(layer_idx),
-        int(ratio), int(rotary_dim), float(eps), ctypes.c_void_p(stream)))
+    args = (_contig(block_keys, "block_keys"), _contig(gamma, "gamma"), _contig(freqs_cis, "freqs_cis"),
+            _contig(key_counts, "key_counts"), _kv_desc(kv_blocks, int(page_stride)), int(page_stride),
+            _u32(cache_lengths), _u32(kv_lookup_table), int(max_prompt_length), int(max_cache_length), int(layer_idx),
+            int(ratio), int(rotary_dim), float(eps), ctypes.c_void_p(stream))
+    with torch.cuda.device(kv_blocks.device):
+        _check(lib.qsa_compress_keys_paged(*args))
 
 
 def qsa_latent_attention_ragged_paged(output, q, input_row_offsets, swa_blocks, swa_page_stride, swa_cache_lengths,
@@ -246,20 +254,24 @@ def qsa_latent_attention_ragged_paged(output, q, input_row_offsets, swa_blocks, 
         raise ValueError("comp_indices must have total_q rows and attn_sink num_heads entries")
     opt = qsa_options(kernel=0, splits=splits, ctas=0)
     ptr = lambda t: ctypes.c_void_p(t.data_ptr() if t.numel() else None)
-    _check(lib.qsa_latent_attention_ragged_paged(
-        _contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets), _kv_desc(swa_blocks, int(swa_page_stride)),
-        int(swa_page_stride), _u32(swa_cache_lengths), _u32(swa_lookup_table), _kv_desc(comp_blocks, int(comp_page_stride)),
-        int(comp_page_stride), ptr(comp_cache_lengths), ptr(comp_lookup_table), int(comp_lookup_table.shape[1]),
-        int(layer_idx), ptr(comp_indices), int(comp_indices.shape[1]), ptr(attn_sink), int(window), float(scale),
-        ctypes.c_void_p(stream), ctypes.byref(opt)))
+    args = (_contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets), _kv_desc(swa_blocks, int(swa_page_stride)),
+            int(swa_page_stride), _u32(swa_cache_lengths), _u32(swa_lookup_table),
+            _kv_desc(comp_blocks, int(comp_page_stride)), int(comp_page_stride), ptr(comp_cache_lengths),
+            ptr(comp_lookup_table), int(comp_lookup_table.shape[1]), int(layer_idx), ptr(comp_indices),
+            int(comp_indices.shape[1]), ptr(attn_sink), int(window), float(scale), ctypes.c_void_p(stream),
+            ctypes.byref(opt))
+    with torch.cuda.device(q.device):
+        _check(lib.qsa_latent_attention_ragged_paged(*args))
 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,
-             kernel: int = 0, splits: int = 0, ctas: int = 0, block_lists: bool = False) -> dict:
+             kernel: int = 0, splits: int = 0, ctas: int = 0, block_lists: bool = False,
+             heads_per_unit: int = 0, tcgen05: int = 0) -> dict:
     lib = load_library()
     k, s = ctypes.c_int32(), ctypes.c_int32()
     c, w = ctypes.c_int64(), ctypes.c_size_t()
-    opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas, block_lists=int(bool(block_lists)))
+    opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas, block_lists=int(bool(block_lists)),
+                      heads_per_unit=heads_per_unit, tcgen05=tcgen05)
     _check(lib.qsa_plan(dtype, total_q, num_kv_heads, head_dim, selection_width, group, ctypes.byref(opt),
                         ctypes.byref(k), ctypes.byref(s), ctypes.byref(c), ctypes.byref(w)))
     return {"kernel": k.value, "splits": s.value, "ctas": c.value, "workspace_bytes": w.value}
@@ -323,7 +335,9 @@ def qsa_sparse_attention_ragged_paged_noalloc(output, q, input_row_offsets, kv_b
                 or status_flags.numel() < 1 or not status_flags.is_cuda:
             raise ValueError("status_flags must be a CUDA tensor of at least one 32-bit integer")
         flags = status_flags.data_ptr()
-    _check(fn(_contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets),
-              _kv_desc(kv_blocks, int(page_stride)), int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table),
-              int(max_prompt_length), int(max_cache_length), int(layer_idx), _contig(token_indices, "token_indices"),
-              _contig(counts, "counts"), float(scale), int(group), ctypes.c_void_p(stream), ctypes.c_void_p(flags)))
+    args = (_contig(output, "output"), _contig(q, "q"), _u32(input_row_offsets),
+            _kv_desc(kv_blocks, int(page_stride)), int(page_stride), _u32(cache_lengths), _u32(kv_lookup_table),
+            int(max_prompt_length), int(max_cache_length), int(layer_idx), _contig(token_indices, "token_indices"),
+            _contig(counts, "counts"), float(scale), int(group), ctypes.c_void_p(stream), ctypes.c_void_p(flags))
+    with torch.cuda.device(q.device):  # the scratch address is looked up on the current device: q's
+        _check(fn(*args))

@@ -24,6 +24,10 @@ using qsa::Params;
 
 thread_local std::string g_last_error;
 
+// Drops the cached device address of the allocation-free entry point's
+// scratch for one device (defined with that entry point below).
+void noalloc_forget_device(int dev);
+
 qsa_status fail(qsa_status s, const std::string& msg) {
   g_last_error = msg;
   return s;
@@ -67,7 +71,9 @@ struct Resolved {
   int splits = 1;
   int cluster = 0;  // kernel 2: the bands of a unit merge inside one thread-block cluster
   int tiles = 0;    // kernel 2: the variant with tile copies (block lists)
+  int umma = 0;     // kernel 2: the tcgen05 consumer (implies the tile-copy layout)
   int groups = 0;   // kernel 2, latent mode: a CTA serves four head groups of a row
+  int stall = 0;    // kernel 3, tests only: no K/V copies, early give-up (qsa_options.test_stall)
   int band = 0;
   int64_t ctas = 0;
   size_t ws_partial_bytes = 0, ws_bytes = 0;
@@ -82,12 +88,26 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // then spreads over many CTAs whose short ranges cannot hide the dependent
 // prologue, and the per-(row, kv head) kernel with split-K, several CTAs per
 // SM, is faster.
-bool few_stream_units(const Resolved& R) {
-  const int64_t hpu = R.nkv % 4 == 0 ? 4 : R.nkv % 2 == 0 ? 2 : 1;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return false;
-  return R.total_q * (R.nkv / hpu) * 4 < sms;
+int device_sms();
+
+// Kv heads per unit of the persistent kernel: the forced value, else eight
+// when num_kv_heads and group allow and the units still outnumber the SMs
+// (prefill-like grids, whose gathers mostly hit L2: a 2 KB BF16 row per key
+// moves about 1.5x the L2 bandwidth of a 1 KB one), else the largest of 4,
+// 2, 1 that divides num_kv_heads (decode-like grids keep more, smaller units).
+int64_t stream_heads_per_unit(const Resolved& R, const qsa_options* opt, int32_t group) {
+  if (opt && opt->heads_per_unit > 0) return opt->heads_per_unit;
+  if (R.nkv % 8 == 0 && group <= 8) {
+    const int sms = device_sms();
+    if (sms > 0 && R.total_q * (R.nkv / 8) > sms) return 8;
+  }
+  return R.nkv % 4 == 0 ? 4 : R.nkv % 2 == 0 ? 2 : 1;
+}
+
+bool few_stream_units(const Resolved& R, const qsa_options* opt, int32_t group) {
+  const int64_t hpu = stream_heads_per_unit(R, opt, group);
+  const int sms = device_sms();
+  return sms > 0 && R.total_q * (R.nkv / hpu) * 4 < sms;
 }
 
 // Picks the kernel for a resolved call: for BF16 and FP8 with head_dim 128
@@ -106,7 +126,7 @@ qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
     R.kernel = 1;
   } else if (want == 0) {
     R.kernel = mma_ok ? 3 : 1;
-    if (R.kernel == 3 && few_stream_units(R)) R.kernel = 2;
+    if (R.kernel == 3 && few_stream_units(R, opt, group)) R.kernel = 2;
     if (R.kernel == 1 && !simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
   } else {
     return fail(QSA_ERR_ARG, "options.kernel must be 0, 1, 2 or 3");
@@ -114,6 +134,14 @@ qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
   if (opt && (opt->splits < 0 || opt->ctas < 0)) return fail(QSA_ERR_ARG, "options.splits and options.ctas must be >= 0");
   if (R.kernel != 2 && opt && opt->splits > 1) return fail(QSA_ERR_UNSUPPORTED, "only kernel 2 takes options.splits");
   if (R.kernel != 3 && opt && opt->ctas > 0) return fail(QSA_ERR_UNSUPPORTED, "only kernel 3 takes options.ctas");
+  if (opt && opt->heads_per_unit != 0) {
+    const int h = opt->heads_per_unit;
+    if (h != 1 && h != 2 && h != 4 && h != 8) return fail(QSA_ERR_ARG, "options.heads_per_unit must be 0, 1, 2, 4 or 8");
+    if (R.kernel != 3) return fail(QSA_ERR_UNSUPPORTED, "only kernel 3 takes options.heads_per_unit");
+    if (R.nkv % h) return fail(QSA_ERR_ARG, "options.heads_per_unit must divide num_kv_heads");
+    if (h == 8 && group > 8) return fail(QSA_ERR_UNSUPPORTED, "units of eight kv heads need group <= 8");
+  }
+  if (opt && opt->test_stall && R.kernel != 3) return fail(QSA_ERR_UNSUPPORTED, "only kernel 3 takes options.test_stall");
   return QSA_OK;
 }
 
@@ -229,26 +257,60 @@ struct DeviceState {
   uint32_t* status = nullptr;
   std::map<void*, Workspace> workspaces;  // keyed by stream
   int sms = 0;
-  int occ[2][2][2] = {};  // [bf16, e4m3][nt - 1][tile copies]
+  int occ[2][2][2][2] = {};  // [bf16, e4m3][nt - 1][tile copies][tcgen05 consumer]
   // resident clusters of s CTAs of the tensor-core kernel ([bf16, e4m3][nt - 1][tile copies][s]; -1 unknown)
-  int clusters[2][2][2][qsa::kMaxClusterSplits + 1];
+  int clusters[2][2][2][2][qsa::kMaxClusterSplits + 1];
   DeviceState() {
     for (auto& a : clusters)
       for (auto& b : a)
         for (auto& c : b)
-          for (int& d : c) d = -1;
+          for (auto& u : c)
+            for (int& d : u) d = -1;
   }
 };
 
 std::mutex g_mu;
 std::map<int, DeviceState> g_dev;
 
+// SM count of the current device (cached per device); 0 when unknown.
+int device_sms() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceState& st = g_dev[dev];
+  if (!st.sms && cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    st.sms = 0;
+  }
+  return st.sms;
+}
+
 qsa_status cuda_fail(cudaError_t e, const char* what) {
   return fail(QSA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
 }
 
+// Kernel 2's consumer: the tcgen05 one (scores and output in tensor memory,
+// BF16, the tile-copy stage layout) when forced with options.tcgen05 = 1,
+// the mma.sync one when forced with -1 or left to choose.
+qsa_status choose_consumer(Resolved& R, const qsa_options* opt) {
+  const int want = opt ? opt->tcgen05 : 0;
+  if (want < -1 || want > 1) return fail(QSA_ERR_ARG, "options.tcgen05 must be -1, 0 or 1");
+  R.umma = 0;
+  if (want == 1) {
+    if (R.kernel != 2) return fail(QSA_ERR_UNSUPPORTED, "only kernel 2 takes options.tcgen05");
+    if (R.elem != qsa::kBF16) return fail(QSA_ERR_UNSUPPORTED, "the tcgen05 consumer reads BF16 caches");
+    R.umma = 1;
+    R.tiles = 1;
+  }
+  return QSA_OK;
+}
+
 // Launch plan of the tensor-core kernel: CTAs per (row, kv head).
 qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int dev) {
+  {
+    const qsa_status s = choose_consumer(R, opt);
+    if (s != QSA_OK) return s;
+  }
   R.splits = 1;
   R.band = qsa::kMmaTile;
   if (R.kernel == 1) {
@@ -260,7 +322,7 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
     // Persistent stream-K: units of HPU adjacent kv heads, TILE keys per
     // 32 KB stage, one CTA per SM over equal ranges of virtual tiles.
     qsa::StreamPlan& sp = R.sp;
-    sp.HPU = R.nkv % 4 == 0 ? 4 : R.nkv % 2 == 0 ? 2 : 1;
+    sp.HPU = (int32_t)stream_heads_per_unit(R, opt, group);
     sp.NG = (int32_t)(R.nkv / sp.HPU);
     const int64_t tile = qsa::stream_tile(R.elem == qsa::kBF16 ? 2 : 1, sp.HPU);
     sp.VT = (int32_t)std::max<int64_t>(1, (R.W + tile - 1) / tile);
@@ -303,9 +365,10 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   // resident clusters of s bands (s <= kMaxClusterSplits), queried once per device
   auto clusters_of = [&](int64_t s) -> int {
     std::lock_guard<std::mutex> lk(g_mu);
-    int& c = g_dev[dev].clusters[kk][knt][R.tiles][s];
+    int& c = g_dev[dev].clusters[kk][knt][R.tiles][R.umma][s];
     if (c < 0)
-      c = kk == 0 ? qsa::mma_max_clusters_bf16(group, (int)s, R.tiles != 0) : qsa::mma_max_clusters_e4m3(group, (int)s, R.tiles != 0);
+      c = kk == 0 ? qsa::mma_max_clusters_bf16(group, (int)s, R.tiles != 0, R.umma != 0)
+                  : qsa::mma_max_clusters_e4m3(group, (int)s, R.tiles != 0, R.umma != 0);
     return c;
   };
   if (!(opt && opt->splits > 0)) {
@@ -317,10 +380,12 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
         const cudaError_t e = cudaDeviceGetAttribute(&st.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
       }
-      int& o = st.occ[kk][knt][R.tiles];
-      if (!o) o = kk == 0 ? qsa::mma_ctas_per_sm_bf16(group, R.tiles != 0) : qsa::mma_ctas_per_sm_e4m3(group, R.tiles != 0);
+      int& o = st.occ[kk][knt][R.tiles][R.umma];
+      if (!o)
+        o = kk == 0 ? qsa::mma_ctas_per_sm_bf16(group, R.tiles != 0, R.umma != 0)
+                    : qsa::mma_ctas_per_sm_e4m3(group, R.tiles != 0, R.umma != 0);
       sms = st.sms;
-      occ = st.occ[kk][knt][R.tiles];
+      occ = st.occ[kk][knt][R.tiles][R.umma];
     }
     const int64_t units = R.total_q * R.nkv;
     // Wave model: a CTA costs about (kPrologueKeys + keys it gathers); the
@@ -546,6 +611,8 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
   p.splits = R.splits;
   p.cluster = R.cluster;
   p.groups = R.groups;
+  p.stall = R.stall;
+  p.umma = R.umma;
   p.band = R.band;
   if (lat) {
     p.comp = lat->comp;
@@ -578,7 +645,7 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
       std::lock_guard<std::mutex> lk(g_mu);
       sms = g_dev[dev].sms;
     }
-    p.shallow = R.elem == qsa::kBF16 && sms > 0 && R.ctas >= 8 * (int64_t)sms ? 1 : 0;
+    p.shallow = !R.umma && R.elem == qsa::kBF16 && sms > 0 && R.ctas >= 8 * (int64_t)sms ? 1 : 0;
   }
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -615,6 +682,7 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   s = plan_launch(R, group, options, dev);
   if (s != QSA_OK) return s;
+  R.stall = options && options->test_stall ? 1 : 0;
 
   return launch_planned(R, output, q, input_row_offsets, kv_blocks, cache_lengths, kv_lookup_table, layer_idx,
                         static_cast<const int32_t*>(token_indices.data), static_cast<const int32_t*>(counts.data),
@@ -765,6 +833,8 @@ qsa_status qsa_latent_attention_ragged_paged(qsa_tensor output, qsa_tensor q, qs
   if (options) opt = *options;
   if (opt.kernel != 0 && opt.kernel != 2) return fail(QSA_ERR_UNSUPPORTED, "latent attention runs on kernel 2");
   if (opt.ctas != 0 || opt.splits < 0) return fail(QSA_ERR_ARG, "only options.splits applies");
+  if (opt.tcgen05 == 1) return fail(QSA_ERR_UNSUPPORTED, "latent attention runs on the mma.sync consumer");
+  opt.tcgen05 = -1;
   opt.kernel = 2;
   R.kernel = 2;
   if (R.total_q == 0) return QSA_OK;
@@ -949,6 +1019,7 @@ qsa_status qsa_release_device_state(void) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  noalloc_forget_device(dev);  // the allocation-free entry point looks its scratch address up again
   std::lock_guard<std::mutex> lk(g_mu);
   auto it = g_dev.find(dev);
   if (it == g_dev.end()) return QSA_OK;
@@ -1029,6 +1100,8 @@ void* g_noalloc_base[kNoallocMaxDevices];  // device address of g_noalloc_scratc
 // address.  In host code the name g_noalloc_scratch is only a stand-in for
 // the symbol, so the address has to be asked for.
 qsa_status noalloc_base(int dev, unsigned char** out) {
+  // (a device reset drops the image and its symbols: qsa_release_device_state
+  // forgets the address, and the next call looks it up again)
   if (dev < 0 || dev >= kNoallocMaxDevices)
     return fail(QSA_ERR_UNSUPPORTED, "qsa_sparse_attention_ragged_paged_noalloc: device ordinal above 63");
   std::lock_guard<std::mutex> lk(g_noalloc_mu);
@@ -1044,6 +1117,16 @@ qsa_status noalloc_base(int dev, unsigned char** out) {
 
 }  // namespace
 
+namespace {
+
+void noalloc_forget_device(int dev) {
+  if (dev < 0 || dev >= kNoallocMaxDevices) return;
+  std::lock_guard<std::mutex> lk(g_noalloc_mu);
+  g_noalloc_base[dev] = nullptr;
+}
+
+}  // namespace
+
 extern "C" qsa_status qsa_sparse_attention_ragged_paged_noalloc(
     qsa_tensor output, qsa_tensor q, qsa_tensor input_row_offsets, qsa_tensor kv_blocks, int64_t page_stride,
     qsa_tensor cache_lengths, qsa_tensor kv_lookup_table, uint32_t max_prompt_length, uint32_t max_cache_length,
@@ -1051,24 +1134,25 @@ extern "C" qsa_status qsa_sparse_attention_ragged_paged_noalloc(
     uint32_t* status_flags) {
   (void)max_prompt_length;
   (void)max_cache_length;
+  // argument errors first, before any CUDA call
   if (reinterpret_cast<uintptr_t>(status_flags) & 3u)
     return fail(QSA_ERR_ARG, "qsa_sparse_attention_ragged_paged_noalloc: status_flags must be 4-byte aligned");
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  unsigned char* base = nullptr;
-  qsa_status s = noalloc_base(dev, &base);
-  if (s != QSA_OK) return s;
-
   qsa_options opt;
   std::memset(&opt, 0, sizeof(opt));
   opt.kernel = 3;
   Resolved R;
-  s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table, layer_idx,
-                 token_indices, counts, group, &opt, R);
+  qsa_status s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table,
+                            layer_idx, token_indices, counts, group, &opt, R);
   if (s != QSA_OK) return s;
   if (R.total_q == 0) return QSA_OK;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   s = plan_launch(R, group, &opt, dev);
+  if (s != QSA_OK) return s;
+  unsigned char* base = nullptr;
+  s = noalloc_base(dev, &base);
   if (s != QSA_OK) return s;
 
   // scratch layout: status word | partial records | tickets

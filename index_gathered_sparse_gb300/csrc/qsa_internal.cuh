@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "qsa.h"
 
 namespace qsa {
@@ -67,6 +69,8 @@ struct Params {
   int32_t tma, tma_plane_k, tma_plane_v;
   int32_t shallow;  // BF16 tile copies, group <= 8: the two-stage variant (three CTAs per SM)
   int32_t groups;   // latent mode, one band, group 16: a CTA serves four head groups (nkv = groups / 4)
+  int32_t stall;    // kernel 3, tests only: producers issue no K/V copies and waits give up early
+  int32_t umma;     // kernel 2: the tcgen05 consumer (BF16, tile-copy layout; tile copies where tma)
   CUtensorMap tmap;
 };
 
@@ -85,9 +89,10 @@ struct StreamPlan {
 };
 
 // Keys per stage of the stream-K kernel for head_dim 128: 64 KB of K+V when
-// each consumer warp owns a head (HPU == 4), else 32 KB.
+// units have four or eight kv heads (eight consumer warps, no epilogue
+// buffer competing for shared memory), else 32 KB.
 __host__ __device__ constexpr int stream_tile(int elem_bytes, int hpu) {
-  return (hpu == 4 ? 65536 : 32768) / (2 * hpu * 128 * elem_bytes);
+  return (hpu >= 4 ? 65536 : 32768) / (2 * hpu * 128 * elem_bytes);
 }
 
 // Element type tags.
@@ -118,17 +123,35 @@ cudaError_t launch_stream_e4m3(const Params& p, const StreamPlan& sp, cudaStream
 cudaError_t launch_stream_bf16_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_e4m3_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 // CTAs of the tensor-core kernel that fit on one SM (for the split planner).
-// (`tiles`: the variant with tile copies, used for block lists.)
-int mma_ctas_per_sm_bf16(int group, bool tiles);
-int mma_ctas_per_sm_e4m3(int group, bool tiles);
+// (`tiles`: the variant with tile copies, used for block lists; `umma`: its
+// tcgen05 consumer.)
+int mma_ctas_per_sm_bf16(int group, bool tiles, bool umma);
+int mma_ctas_per_sm_e4m3(int group, bool tiles, bool umma);
 // Clusters of `splits` CTAs of the tensor-core kernel resident at once (0: none fit).
-int mma_max_clusters_bf16(int group, int splits, bool tiles);
-int mma_max_clusters_e4m3(int group, int splits, bool tiles);
+int mma_max_clusters_bf16(int group, int splits, bool tiles, bool umma);
+int mma_max_clusters_e4m3(int group, int splits, bool tiles, bool umma);
 
 // Floats of one split-K partial: o[group][D], m[group], l[group], padded to a
 // multiple of 4 so every partial starts 16-byte aligned.
 __host__ __device__ inline int64_t partial_stride(int64_t group, int64_t D) {
   return (group * (D + 2) + 3) / 4 * 4;
+}
+
+// Raises a kernel's dynamic shared-memory limit once per device.  `done` holds
+// one flag per device ordinal, read and set atomically (host threads may race
+// to set the attribute; setting it twice is harmless); ordinals past its end
+// set the attribute on every launch.
+constexpr int kMaxTrackedDevices = 256;
+template <typename Kernel>
+cudaError_t ensure_dynamic_smem(std::atomic<unsigned char> (&done)[kMaxTrackedDevices], Kernel kernel, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const bool tracked = dev >= 0 && dev < kMaxTrackedDevices;
+  if (tracked && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && tracked) done[dev].store(1, std::memory_order_release);
+  return e;
 }
 
 // Tensor-core kernel limits.

@@ -40,6 +40,7 @@
 #include <cuda_fp8.h>
 
 #include "qsa_device.cuh"
+#include "qsa_umma.cuh"
 
 namespace qsa {
 
@@ -49,7 +50,7 @@ namespace qsa {
 // loop, which measurably slows the per-row path).  SHALLOW (BF16 tile copies
 // only): two stages instead of three, so three CTAs fit on an SM, for grids
 // of many waves whose gathers mostly hit L2.
-template <int KIND, bool TILES, bool SHALLOW = false>
+template <int KIND, bool TILES, bool SHALLOW = false, bool UMMA = false>
 struct MmaCfg {
   static constexpr int D = 128;
   static constexpr int ELEM = KIND == kBF16 ? 2 : 1;
@@ -68,7 +69,15 @@ struct MmaCfg {
   // ring (1024-byte aligned with tile copies: the 128-byte swizzle repeats
   // every 8 lines), band offsets, and with tile copies one barrier per stage
   // and the tile-copy coordinates
-  static constexpr int SMEM = TILES ? 1024 + RING + kMmaMaxBand * 4 + STAGES * 8 + MAXT * 8 : RING + kMmaMaxBand * 4;
+  // tcgen05 consumer (UMMA, tile-copy layout only): the query heads as a
+  // 128-byte-swizzled K-major tile (16 rows x 128 elements), right after the
+  // ring, and a small block after the tile records (reductions, barriers,
+  // the tensor-memory address)
+  static constexpr int QBYTES = UMMA ? 16 * 128 * ELEM : 0;
+  static constexpr int UMISC = UMMA ? 1024 : 0;
+  static constexpr int SMEM = TILES ? 1024 + RING + QBYTES + kMmaMaxBand * 4 + STAGES * 8 + MAXT * 8 + UMISC
+                                    : RING + kMmaMaxBand * 4;
+  static_assert(!UMMA || (TILES && KIND == kBF16), "the tcgen05 consumer reads the BF16 tile-copy layout");
 };
 
 // Shared-memory layout of a stage's K (or V) half: line x of key k's row
@@ -125,8 +134,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // (each poll may block for a while in hardware), which never happens unless a
 // copy was lost.
 constexpr int kSpinLimit = 1 << 20;
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < kSpinLimit; ++i)
+// The poll limit of a test-only call whose producers issue no copies: its
+// waits give up quickly instead of after kSpinLimit polls.
+constexpr int kStallSpins = 4096;
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int limit = kSpinLimit) {
+  for (int i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -406,16 +418,33 @@ __device__ __forceinline__ void finish_unit_mma(const Params& p, int r, int h, i
 // row that read the same keys; warp w owns group w over every key of a tile
 // (all NW 16-key slices) and writes its heads from registers, so each key is
 // gathered once per row instead of once per group.
-template <int KIND, int NT, bool TILES, bool SHALLOW, bool GROUPS>
+//
+// UMMA (BF16, tile-copy layout): the scores and the output accumulate in
+// tensor memory through tcgen05 MMAs issued by one thread, on the stage bytes
+// as the copies left them (the 128-byte-swizzled layout is the tensor cores'
+// K-major layout for K and, read transposed, their MN-major layout for V^T):
+//     S^T[64 keys x GP]  = K[64 x 128] . Q^T      (M = 64, one lane per key)
+//     O^T[128 x 16]     += V^T[128 x 64] . P^T    (M = 128, one lane per channel)
+// The four warps turn S^T into P^T (one key per lane); the running maximum is
+// one reference per head for the whole CTA, moved only when a tile's maximum
+// passes it by more than 8 (base 2), and O^T is rescaled in tensor memory
+// then.  P^T goes into the stage's first 2 KB, whose K rows q.K has consumed.
+template <int KIND, int NT, bool TILES, bool SHALLOW, bool GROUPS, bool UMMA = false>
 __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_constant__ Params p) {
-  using C = MmaCfg<KIND, TILES, SHALLOW>;
+  using C = MmaCfg<KIND, TILES, SHALLOW, UMMA>;
   constexpr int NW = kMmaThreads / 32;
   constexpr int GP = 8 * NT;  // padded query heads
+  static_assert(!UMMA || !GROUPS, "the tcgen05 consumer serves one head group per CTA");
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = TILES ? smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u) : smem_raw;  // the stage ring
-  uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + C::RING);
+  unsigned char* q_tile = smem + C::RING;  // UMMA: the query heads, K-major, 128-byte swizzle (1024-byte aligned)
+  uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + C::RING + C::QBYTES);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(s_off + kMmaMaxBand);  // TILES: one barrier per stage
   int2* s_tile = reinterpret_cast<int2*>(s_full + C::STAGES);           // TILES: tile copy (page, first slot) or (-1, 0)
+  // UMMA: per-warp maxima and sums [NW][16], the q.K and p.V barriers, the tensor-memory base
+  float* u_red = reinterpret_cast<float*>(s_tile + C::MAXT);
+  uint64_t* u_bar = reinterpret_cast<uint64_t*>(u_red + NW * 16);
+  uint32_t* u_tmem = reinterpret_cast<uint32_t*>(u_bar + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -423,7 +452,18 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     // a stage's barrier completes a phase when a tile copy into it landed
     // (16-byte copies complete through per-thread cp.async groups instead)
     for (int k = 0; k < C::STAGES; ++k) mbar_init(smem_addr(&s_full[k]), 1);
+    if (UMMA) {  // one tcgen05 commit per tile on each
+      mbar_init(smem_addr(&u_bar[0]), 1);
+      mbar_init(smem_addr(&u_bar[1]), 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if constexpr (UMMA) {
+    // 32 tensor-memory columns: S^T in [0, GP), O^T in [16, 32)
+    if (warp == 0) {
+      tmem_alloc(smem_addr(u_tmem), 32);
+      tmem_relinquish();
+    }
   }
 
   // CTA -> (split, kv head, row): the bands of one unit are adjacent in the
@@ -448,10 +488,22 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
 
   // ---- trip 1 ----
   const int cnt = block_sel || latent ? p.W : __ldg(p.counts + r);
-  // Q^T fragments (the MMA B operand), zero for padded heads
+  if constexpr (UMMA) {
+    // the group's query heads as rows of a K-major 128-byte-swizzled tile
+    // (rows past the group zero): the B operand of q.K
+    for (int i = tid; i < 16 * 16; i += kMmaThreads) {
+      const int n = i >> 4, c = i & 15;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (n < p.group)
+        v = __ldg(reinterpret_cast<const uint4*>(p.q + (((int64_t)r * p.nq + (int64_t)qh * p.group + n) * C::D + c * 8) * C::ELEM));
+      *reinterpret_cast<uint4*>(q_tile + (c >> 3) * (16 * 128) + (n >> 3) * 1024 + (n & 7) * 128 + (((c & 7) ^ (n & 7)) << 4)) = v;
+    }
+  }
+  // Q^T fragments (the mma.sync B operand), zero for padded heads
   uint32_t qf[NT][C::KSTEPS][2];
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
+    if constexpr (UMMA) break;
     const int head = nt * 8 + gid;
     const bool live = head < p.group;
     const unsigned char* qrow = p.q + (((int64_t)r * p.nq + (int64_t)qh * p.group + (live ? head : 0)) * C::D) * C::ELEM;
@@ -671,9 +723,34 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   bool timed_out = false;
   uint32_t tma_phase = 0;  // bit s: parity of the next tile-copy phase of stage s
 
+  // UMMA state: the tensor-memory base, each head's reference maximum (the
+  // same in every thread) and this thread's key's share of each head's sum
+  uint32_t tmem = 0;
+  float m_ref[GP], l_part[GP];
+  if constexpr (UMMA) {
+    tc_fence_after();  // the allocation's address, published by the translation's barriers
+    tmem = *u_tmem;
+#pragma unroll
+    for (int n = 0; n < GP; ++n) {
+      m_ref[n] = -CUDART_INF_F;
+      l_part[n] = 0.f;
+    }
+  }
+
   for (int t = 0; t < ntiles; ++t) {
     cp_async_wait<C::STAGES - 2>();  // this thread's 16-byte copies of tile t
-    __syncthreads();  // everyone's copies of tile t landed; every warp is done with tile t - 1
+    if constexpr (UMMA) {
+      // this thread's copies into tile t visible to the tensor cores; p.V of
+      // tile t - 1 done (its stage is refilled below, O^T may be rescaled)
+      fence_proxy_async_smem();
+      const bool lost = t > 0 && !mbar_wait_asm(smem_addr(&u_bar[1]), (uint32_t)((t - 1) & 1));
+      if (__syncthreads_or(lost || timed_out)) {  // every thread takes the same decision
+        timed_out = true;
+        break;
+      }
+    } else {
+      __syncthreads();  // everyone's copies of tile t landed; every warp is done with tile t - 1
+    }
     if (t + C::STAGES - 1 < ntiles) issue(t + C::STAGES - 1);
     cp_async_commit();
     if (TILES && (tma_mask >> t & 1u)) {
@@ -683,6 +760,98 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     }
 
     const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
+    if constexpr (UMMA) {
+      const uint32_t kb = smem_addr(sb), vb = kb + (uint32_t)C::KV_BYTES;
+      // q.K: 8 K steps of 16 channels (4 per 128-byte line block), scores of
+      // key k in lane (k / 16) * 32 + k % 16, columns [0, GP)
+      if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < C::KSTEPS; ++ks)
+          umma_f16(tmem,
+                   smem_desc(kb + (uint32_t)((ks >> 2) * C::LINE_BYTES + (ks & 3) * 32), 16, 1024, kSwizzle128),
+                   smem_desc(smem_addr(q_tile) + (uint32_t)((ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, kSwizzle128),
+                   instr_desc(64, GP, 1, 0, 0), ks > 0);
+        umma_commit(smem_addr(&u_bar[0]));
+      }
+      if (!mbar_wait_asm(smem_addr(&u_bar[0]), (uint32_t)(t & 1))) timed_out = true;
+      tc_fence_after();
+      float sv[GP];
+      if constexpr (GP == 8) tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16), sv);
+      else tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), sv);
+      // this lane's key (lanes 16..31 hold no row of the 64-row product)
+      const int kk = t * C::TILE + warp * 16 + (lane & 15);
+      const bool valid = lane < 16 && kk < band_keys && s_off[kk] != kInvalidOff;
+#pragma unroll
+      for (int n = 0; n < GP; ++n) sv[n] = valid && n < p.group ? sv[n] * p.scale_log2 : -CUDART_INF_F;
+#pragma unroll
+      for (int n = 0; n < GP; ++n) {
+        float mx = sv[n];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        if (lane == 0) u_red[warp * 16 + n] = mx;
+      }
+      __syncthreads();
+      // the tile's maximum per head; the reference moves when the tile passes
+      // it by more than 8, so every term 2^(s - ref) stays <= 256 (every thread
+      // computes the same decision from the same values)
+      float alpha[GP];
+      bool moved = false;
+#pragma unroll
+      for (int n = 0; n < GP; ++n) {
+        const float mt = fmaxf(fmaxf(u_red[n], u_red[16 + n]), fmaxf(u_red[32 + n], u_red[48 + n]));
+        alpha[n] = 1.f;
+        if (mt > m_ref[n] + 8.f) {
+          alpha[n] = m_ref[n] == -CUDART_INF_F ? 0.f : exp2f(m_ref[n] - mt);
+          m_ref[n] = mt;
+          moved = true;
+        }
+      }
+      if (moved && t > 0) {
+        // O^T (this warp's 32 channels, 16 head columns) to the new references
+        float ov[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16u, ov);
+#pragma unroll
+        for (int n = 0; n < GP; ++n) ov[n] *= alpha[n];
+        tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + 16u, ov);
+        tmem_wait_st();
+      }
+#pragma unroll
+      for (int n = 0; n < GP; ++n) {
+        const float pn = exp2_fast(sv[n] - (m_ref[n] == -CUDART_INF_F ? 0.f : m_ref[n]));
+        l_part[n] = l_part[n] * alpha[n] + pn;
+        sv[n] = pn;
+      }
+      // P^T, MN-major without swizzle: key k's 16 head values at
+      // (k / 8) * 256 + (k % 8) * 16 (heads 0..7) and +128 (heads 8..15)
+      if (lane < 16) {
+        const int k = warp * 16 + lane;
+        unsigned char* pr = const_cast<unsigned char*>(sb) + (k >> 3) * 256 + (k & 7) * 16;
+        *reinterpret_cast<uint4*>(pr) =
+            make_uint4(pack_bf16(sv[0], sv[1]), pack_bf16(sv[2], sv[3]), pack_bf16(sv[4], sv[5]), pack_bf16(sv[6], sv[7]));
+        uint4 hi = make_uint4(0u, 0u, 0u, 0u);
+        if constexpr (GP == 16)
+          hi = make_uint4(pack_bf16(sv[8], sv[9]), pack_bf16(sv[10], sv[11]), pack_bf16(sv[12], sv[13]),
+                          pack_bf16(sv[14], sv[15]));
+        *reinterpret_cast<uint4*>(pr + 128) = hi;
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      // p.V: 4 K steps of 16 keys; O^T in columns [16, 32), lane = channel
+      if (tid == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int ks = 0; ks < C::TILE / 16; ++ks)
+          umma_f16(tmem + 16u, smem_desc(vb + (uint32_t)(ks * 2048), (uint32_t)C::LINE_BYTES, 1024, kSwizzle128),
+                   smem_desc(kb + (uint32_t)(ks * 512), 256, 128, kSwizzleNone), instr_desc(128, 16, 1, 1, 1),
+                   t > 0 || ks > 0);
+        umma_commit(smem_addr(&u_bar[1]));
+      }
+      continue;
+    }
 #pragma unroll 1
     for (int sl = 0; sl < (GROUPS ? NW : 1); ++sl) {
     const int kw = GROUPS ? sl : warp;  // the 16-key slice of the tile this warp scores
@@ -789,6 +958,33 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     }
     }  // slices
   }
+  float u_o[16];  // UMMA: O^T of this thread's channel (tid), one value per head column
+  if constexpr (UMMA) {
+    // p.V of the last tile done; then every head's sum over all key lanes,
+    // and the tensor memory handed back
+    if (!timed_out && ntiles > 0 && !mbar_wait_asm(smem_addr(&u_bar[1]), (uint32_t)((ntiles - 1) & 1)))
+      timed_out = true;
+    tc_fence_after();
+    if (ntiles > 0) {
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16u, u_o);
+    } else {
+#pragma unroll
+      for (int n = 0; n < 16; ++n) u_o[n] = 0.f;
+    }
+#pragma unroll
+    for (int n = 0; n < GP; ++n) {
+      float l = l_part[n];
+      l += __shfl_xor_sync(0xffffffffu, l, 1);
+      l += __shfl_xor_sync(0xffffffffu, l, 2);
+      l += __shfl_xor_sync(0xffffffffu, l, 4);
+      l += __shfl_xor_sync(0xffffffffu, l, 8);
+      l += __shfl_xor_sync(0xffffffffu, l, 16);
+      if (lane == 0) u_red[warp * 16 + n] = l;
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, 32);
+  }
   if (timed_out) atomicOr(p.status, QSA_STATUS_TIMEOUT);
   cp_async_wait<0>();
   __syncthreads();  // the ring is drained; its shared memory now holds the warp states
@@ -833,6 +1029,28 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   static_assert((NW * GP * C::D + 2 * NW * GP + 2 * kMaxSplits * GP + GP * (C::D + 2) + NW * GP + 2 * GP) * 4 <=
                     C::STAGES * C::STAGE_BYTES,
                 "epilogue buffers must fit in the drained ring");
+  if constexpr (UMMA) {
+    // one softmax state (the CTA's), as warp state 0 beside three empty ones
+    static_assert(kMmaThreads == C::D, "one thread per channel");
+#pragma unroll
+    for (int w = 0; w < NW; ++w)
+#pragma unroll
+      for (int n = 0; n < GP; ++n) sm_o[(w * GP + n) * C::D + tid] = w == 0 ? u_o[n] : 0.f;
+    if (tid == 0)
+#pragma unroll
+      for (int n = 0; n < GP; ++n) {
+        sm_m[n] = m_ref[n];
+        sm_l[n] = u_red[n] + u_red[16 + n] + u_red[32 + n] + u_red[48 + n];
+#pragma unroll
+        for (int w = 1; w < NW; ++w) {
+          sm_m[w * GP + n] = -CUDART_INF_F;
+          sm_l[w * GP + n] = 0.f;
+        }
+      }
+    __syncthreads();
+    finish_unit_mma<NW>(p, r, h, split, row_ok, sm_m, sm_l, sm_o, GP, scratch, part, s_e);
+    return;
+  }
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
@@ -861,17 +1079,12 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   finish_unit_mma<NW>(p, r, h, split, row_ok, sm_m, sm_l, sm_o, GP, scratch, part, s_e);
 }
 
-template <int KIND, int NT, bool TILES, bool SHALLOW, bool GROUPS = false>
+template <int KIND, int NT, bool TILES, bool SHALLOW, bool GROUPS = false, bool UMMA = false>
 cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
-  using C = MmaCfg<KIND, TILES, SHALLOW>;
-  static int configured_mask = 0;  // one bit per device (up to 32)
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured_mask & (1 << (dev & 31)))) {
-    const cudaError_t e = cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured_mask |= 1 << (dev & 31);
-  }
+  using C = MmaCfg<KIND, TILES, SHALLOW, UMMA>;
+  static std::atomic<unsigned char> configured[kMaxTrackedDevices] = {};
+  const cudaError_t e = ensure_dynamic_smem(configured, mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS, UMMA>, C::SMEM);
+  if (e != cudaSuccess) return e;
   const int64_t ctas = (int64_t)p.total_q * p.nkv * p.splits;
   if (ctas == 0) return cudaSuccess;
   if (p.cluster) {
@@ -888,13 +1101,17 @@ cudaError_t launch_mma_t(const Params& p, cudaStream_t s) {
     at[0].val.clusterDim.z = 1;
     cfg.attrs = at;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS>, p);
+    return cudaLaunchKernelEx(&cfg, mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS, UMMA>, p);
   }
-  mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
+  mma_kernel<KIND, NT, TILES, SHALLOW, GROUPS, UMMA><<<(unsigned)ctas, kMmaThreads, C::SMEM, s>>>(p);
   return cudaGetLastError();
 }
 template <int KIND, int NT>
 cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
+  if (p.umma) {  // the tcgen05 consumer: BF16, the tile-copy layout (tile copies where p.tma)
+    if constexpr (KIND == kBF16) return launch_mma_t<KIND, NT, true, false, false, true>(p, s);
+    return cudaErrorInvalidValue;
+  }
   if (!p.tma) {
     if constexpr (NT == 2)
       if (p.groups) return launch_mma_t<KIND, NT, false, false, true>(p, s);
@@ -908,10 +1125,10 @@ cudaError_t launch_mma_nt(const Params& p, cudaStream_t s) {
 
 // Clusters of `splits` CTAs of the tensor-core kernel that can be resident
 // at once on the device (0 when such a cluster cannot be placed).
-template <int KIND, int NT, bool TILES>
+template <int KIND, int NT, bool TILES, bool UMMA = false>
 int mma_max_clusters_nt(int splits) {
-  using C = MmaCfg<KIND, TILES>;
-  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+  using C = MmaCfg<KIND, TILES, false, UMMA>;
+  if (cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false, false, UMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)splits);
@@ -925,28 +1142,32 @@ int mma_max_clusters_nt(int splits) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES, false, false>, &cfg) != cudaSuccess) {
+  if (cudaOccupancyMaxActiveClusters(&n, mma_kernel<KIND, NT, TILES, false, false, UMMA>, &cfg) != cudaSuccess) {
     cudaGetLastError();  // a refused query is not a launch error
     return 0;
   }
   return n;
 }
 template <int KIND>
-int mma_max_clusters(int group, int splits, bool tiles) {
+int mma_max_clusters(int group, int splits, bool tiles, bool umma = false) {
+  if constexpr (KIND == kBF16)
+    if (umma) return group <= 8 ? mma_max_clusters_nt<KIND, 1, true, true>(splits) : mma_max_clusters_nt<KIND, 2, true, true>(splits);
   if (tiles) return group <= 8 ? mma_max_clusters_nt<KIND, 1, true>(splits) : mma_max_clusters_nt<KIND, 2, true>(splits);
   return group <= 8 ? mma_max_clusters_nt<KIND, 1, false>(splits) : mma_max_clusters_nt<KIND, 2, false>(splits);
 }
 
-template <int KIND, int NT, bool TILES>
+template <int KIND, int NT, bool TILES, bool UMMA = false>
 int mma_occupancy_nt() {
-  using C = MmaCfg<KIND, TILES>;
+  using C = MmaCfg<KIND, TILES, false, UMMA>;
   int n = 0;
-  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES, false, false>, kMmaThreads, C::SMEM);
+  cudaFuncSetAttribute(mma_kernel<KIND, NT, TILES, false, false, UMMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, mma_kernel<KIND, NT, TILES, false, false, UMMA>, kMmaThreads, C::SMEM);
   return n > 0 ? n : 1;
 }
 template <int KIND>
-int mma_occupancy(int group, bool tiles) {
+int mma_occupancy(int group, bool tiles, bool umma = false) {
+  if constexpr (KIND == kBF16)
+    if (umma) return group <= 8 ? mma_occupancy_nt<KIND, 1, true, true>() : mma_occupancy_nt<KIND, 2, true, true>();
   if (tiles) return group <= 8 ? mma_occupancy_nt<KIND, 1, true>() : mma_occupancy_nt<KIND, 2, true>();
   return group <= 8 ? mma_occupancy_nt<KIND, 1, false>() : mma_occupancy_nt<KIND, 2, false>();
 }

@@ -48,15 +48,16 @@ struct StreamCfg {
   static constexpr int ROWB = D * ELEM;             // one head's K (or V) row
   static constexpr int KEYB = HPU * ROWB;           // a unit's K (or V) bytes per key, contiguous
   static constexpr int SROW = KEYB + 16;            // padded shared-memory row (conflict-free ldmatrix)
-  // Consumer warps: eight (two per kv head, splitting each tile's keys) for
-  // units of four heads with one 8-head N tile, so that two dependent
-  // MMA/softmax chains share each SM sub-partition; else four.
-  static constexpr int NC = (NT == 1 && HPU == 4) ? 8 : 4;
+  // Consumer warps: eight for units of four heads with one 8-head N tile (two
+  // per kv head, splitting each tile's keys, so that two dependent
+  // MMA/softmax chains share each SM sub-partition) or of eight heads (one per
+  // head); else four.
+  static constexpr int NC = (NT == 1 && HPU >= 4) ? 8 : 4;
   static constexpr int CT = NC * 32;                // consumer threads
   static constexpr int WPH = NC / HPU;              // warps per head
   // two warps per head merge their softmax states pairwise through shared
   // memory (half of head_dim at a time) into the first warp's registers
-  static constexpr bool PAIR = NC == 8;
+  static constexpr bool PAIR = NC == 8 && WPH == 2;
   // keys per stage: 64 KB of K+V when each warp owns a head (no epilogue
   // buffer competes for shared memory), else 32 KB
   static constexpr int TILE = stream_tile(ELEM, HPU);
@@ -99,6 +100,8 @@ struct StreamCfg {
   static_assert(3 * H + 1 + STAGES + H + 2 < MR, "unit-meta ring too small");
   static_assert(SMEM <= 232448, "shared memory");
   static_assert(STAGES >= 3, "stage ring");
+  static_assert(WPH >= 1 && NC % HPU == 0, "every head has whole consumer warps");
+  static_assert(HPU < 8 || NT == 1, "eight-head units take one 8-head N tile");
 };
 
 // Barrier over the `n` threads of one role (id 1: producers, id 2: consumers).
@@ -507,9 +510,10 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     // producer barrier); false after a give-up.
     auto stage_free = [&](const TileCursor& c) -> bool {
       if (tid != 0 || c.o < S) return true;
-      return mbar_wait(smem_addr(&s_empty[c.o % S]), (uint32_t)((c.o / S - 1) & 1));
+      return mbar_wait(smem_addr(&s_empty[c.o % S]), (uint32_t)((c.o / S - 1) & 1), p.stall ? kStallSpins : kSpinLimit);
     };
     auto kv_hop = [&](const TileCursor& c) {
+      if (p.stall) return;  // (tests) no copy and no arrival: the consumers' waits give up
       const int kt = keys_in(c.n, c.j), slot = (c.o & (RT - 1)) * TILE, st = c.o % S;
       const uint32_t bar = smem_addr(&s_full[st]);
       if constexpr (C::BULK) {
@@ -1020,7 +1024,7 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
   int u = u_first, j = jlo_first, n = 0, jl = 0, ord = 0;
   bool entered = false, row_ok = false, aborted = false;
   while (true) {
-    const bool ok = mbar_wait(smem_addr(&s_full[ord % S]), (uint32_t)((ord / S) & 1));
+    const bool ok = mbar_wait(smem_addr(&s_full[ord % S]), (uint32_t)((ord / S) & 1), p.stall ? kStallSpins : kSpinLimit);
     if (role_any(2, C::CT, !ok)) {  // a give-up by any consumer is every consumer's decision
       aborted = true;
       break;
@@ -1053,7 +1057,21 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
     if (u + 1 <= u_last) load_q(u + 1, SCAN ? s_meta[mslot(u + 1) + 4] : p.total_q - 1 - (u + 1) / sp.NG, qn);
   }
   if (aborted) {
-    if (ctid == 0) atomicOr(p.status, QSA_STATUS_TIMEOUT);
+    // A give-up still arrives on the ticket of every shared unit this CTA
+    // contributes to and has not arrived on yet, so that each ticket reads
+    // zero again after its last arrival; a ticket this CTA takes last is
+    // re-armed without a merge (the call reports QSA_STATUS_TIMEOUT and its
+    // output is undefined).
+    if (ctid == 0) {
+      atomicOr(p.status, QSA_STATUS_TIMEOUT);
+      if (contributors(u_first) > 1) {
+        const uint32_t t = first_ticket != 0xFFFFFFFFu ? first_ticket : atomicAdd(p.ws_ticket + u_first, 1u);
+        if (t == (uint32_t)(contributors(u_first) - 1)) p.ws_ticket[u_first] = 0u;
+      }
+      if (u_last != u_first && contributors(u_last) > 1 &&
+          atomicAdd(p.ws_ticket + u_last, 1u) == (uint32_t)(contributors(u_last) - 1))
+        p.ws_ticket[u_last] = 0u;
+    }
     return;
   }
 
@@ -1125,15 +1143,9 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
 template <int KIND, int NT, int HPU, bool SCAN>
 cudaError_t launch_stream_t(const Params& p, const StreamPlan& sp, cudaStream_t s) {
   using C = StreamCfg<KIND, NT, HPU>;
-  static int configured_mask = 0;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (!(configured_mask & (1 << (dev & 31)))) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(stream_kernel<KIND, NT, HPU, SCAN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    configured_mask |= 1 << (dev & 31);
-  }
+  static std::atomic<unsigned char> configured[kMaxTrackedDevices] = {};
+  const cudaError_t e = ensure_dynamic_smem(configured, stream_kernel<KIND, NT, HPU, SCAN>, C::SMEM);
+  if (e != cudaSuccess) return e;
   if (sp.G == 0) return cudaSuccess;
   stream_kernel<KIND, NT, HPU, SCAN><<<sp.G, C::THREADS, C::SMEM, s>>>(p, sp);
   return cudaGetLastError();
@@ -1145,6 +1157,7 @@ template <int KIND, bool SCAN>
 cudaError_t launch_stream_kind(const Params& p, const StreamPlan& sp, cudaStream_t s) {
   const bool nt2 = p.group > 8;
   switch (sp.HPU) {
+    case 8: return nt2 ? cudaErrorInvalidValue : launch_stream_t<KIND, 1, 8, SCAN>(p, sp, s);
     case 4: return nt2 ? launch_stream_t<KIND, 2, 4, SCAN>(p, sp, s) : launch_stream_t<KIND, 1, 4, SCAN>(p, sp, s);
     case 2: return nt2 ? launch_stream_t<KIND, 2, 2, SCAN>(p, sp, s) : launch_stream_t<KIND, 1, 2, SCAN>(p, sp, s);
     default: return nt2 ? launch_stream_t<KIND, 2, 1, SCAN>(p, sp, s) : launch_stream_t<KIND, 1, 1, SCAN>(p, sp, s);

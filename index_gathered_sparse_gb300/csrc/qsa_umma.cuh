@@ -1,0 +1,116 @@
+// Fifth-generation tensor-core (tcgen05) primitives for sm_103a: tensor-memory
+// allocation, shared-memory matrix descriptors, the MMA issue and commit, and
+// tensor-memory loads and stores, as inline PTX.
+//
+// Conventions, checked on the GPU against a float64 product before any kernel
+// used them:
+//   - A shared-memory matrix descriptor holds the start address, the leading-
+//     and stride-dimension byte offsets (all >> 4), the fixed version bits 46..48
+//     = 0b001 and the swizzle mode in bits 61..63 (0 none, 2 128-byte).
+//   - K-major 128-byte-swizzled operand (rows of 128 bytes, chunk c of row r at
+//     chunk c ^ (r & 7), 8-row groups `sbo` bytes apart): the leading offset is
+//     unused; one 16-element (bf16) K step advances the start address by 32 B
+//     inside the 128-byte row, the next 64 elements are a separate block.
+//   - MN-major 128-byte-swizzled operand (the same bytes read transposed: 64
+//     M elements per 128-byte row, one row per K index): leading offset =
+//     stride between 64-element M blocks, stride offset = stride between
+//     8-row K groups.
+//   - MN-major operand without swizzle (core matrices of 8 K rows x 16 bytes):
+//     leading offset = stride between 8-row K groups, stride offset = stride
+//     between 8-element N groups.
+//   - Accumulator rows in tensor memory: M = 128 puts row i in lane i; M = 64
+//     puts row i in lane (i / 16) * 32 + i % 16 (lanes 0..15 of each warp's
+//     32-lane quarter).  A warp reads only its own quarter of the lanes.
+#pragma once
+
+#include <stdint.h>
+
+namespace qsa {
+
+// Allocates `ncols` (a power of two >= 32) tensor-memory columns for this CTA
+// and writes their base address to the shared-memory word `dst`.  One full
+// warp executes it.
+__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst), "r"(ncols) : "memory");
+}
+// Lets other CTAs on the SM allocate; after this the CTA allocates no more.
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols) : "memory");
+}
+// Ordering of tensor-core work across a thread barrier.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)swizzle << 61;
+  return d;
+}
+constexpr uint32_t kSwizzleNone = 0, kSwizzle128 = 2;
+
+// Instruction descriptor: f32 accumulator, A and B of element kind `ab`
+// (kind::f16: 0 f16, 1 bf16; kind::f8f6f4: 0 e4m3), A / B MN-major when
+// a_mn / b_mn, shape M x N.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, int ab, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)ab << 7) | ((uint32_t)ab << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] x B[smem], 16-bit inputs; issued by one thread.
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.u32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
+// Arrives once on the mbarrier when every MMA this thread issued before has completed.
+__device__ __forceinline__ void umma_commit(uint32_t mbar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(mbar) : "memory");
+}
+
+// 32 lanes x N columns of 32 bits: thread t of the warp receives lane
+// (quarter base + t), columns col .. col + N - 1.  The load and its wait are
+// one asm statement, so no output register is read before it has arrived.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(
+          taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
+}  // namespace qsa

@@ -154,6 +154,35 @@ class QSAInputs:
             + self.total_q * 4
         )
 
+    def attended_pairs(self) -> int:
+        """(key, kv head) pairs the method attends: every valid entry of every
+        row, once per kv head."""
+        return int(self.valid_counts().sum()) * self.num_kv_heads
+
+    def algorithmic_flops(self) -> int:
+        """Flops of the two contractions: per attended (key, kv head) pair,
+        ``group`` query heads x head_dim multiply-adds for q.K and as many
+        for p.V (2 flops each)."""
+        return 4 * self.group * self.head_dim * self.attended_pairs()
+
+    def distinct_kv_bytes(self) -> int:
+        """K and V bytes of the distinct cache positions the selections name,
+        counted once per sequence (all kv heads): what a gather must bring
+        from DRAM at least once when every repeat hits in L2."""
+        n = self.valid_counts()
+        seq = self.row_sequence()
+        kv_len = self.cache_lengths.astype(np.int64) + np.diff(self.input_row_offsets.astype(np.int64))
+        distinct = 0
+        for b in range(self.batch):
+            rows = np.nonzero(seq == b)[0]
+            if rows.size == 0:
+                continue
+            w = int(n[rows].max())
+            sel = self.token_indices[rows, :w].astype(np.int64)
+            keep = (np.arange(w)[None, :] < n[rows][:, None]) & (sel >= 0) & (sel < kv_len[b])
+            distinct += int(np.unique(sel[keep]).size)
+        return distinct * self.num_kv_heads * 2 * self.head_dim * ELEM_BYTES[self.dtype]
+
 
 # ----------------------------------------------------------------------------
 # selection recipes (per row); each returns the valid prefix as int64
@@ -552,6 +581,22 @@ class MSAInputs(QSAInputs):
         return (n * 2 * D * ekv + self.total_q * self.num_q_heads * D * (ekv + eo)
                 + self.d_indices.size * 4)
 
+    def attended_pairs(self) -> int:
+        return int(self.attended_keys().sum())
+
+    def distinct_kv_bytes(self) -> int:
+        """K and V bytes of the distinct blocks listed per (sequence, kv head),
+        each counted whole."""
+        P = int(self.kv_shape[3])
+        seq = self.row_sequence()
+        blocks = 0
+        for b in range(self.batch):
+            rows = np.nonzero(seq == b)[0]
+            for h in range(self.num_kv_heads):
+                ids = self.d_indices[h, rows].reshape(-1)
+                blocks += int(np.unique(ids[ids >= 0]).size)
+        return blocks * P * 2 * self.head_dim * ELEM_BYTES[self.dtype]
+
 
 @dataclasses.dataclass
 class MSASpec:
@@ -654,6 +699,11 @@ def msa_small_variants() -> dict:
         "msa_bf16_decode_small": msa_bf16_decode(seed=16, batch=5, cache_range=(70, 900), topk=6),
         "msa_bf16_prefill_small": msa_bf16_prefill(seed=17, rows=(20, 7, 33), cache=(0, 130, 300), topk=5),
         "msa_fp8_decode_small": msa_fp8_decode(seed=18, batch=4, cache_range=(100, 1200), topk=4),
+        # speculative-decode shape: 2, 3 and 4 new rows per sequence on cached
+        # context, the last one straddling a block boundary (positions 255..258
+        # with blocks of 64), so rows of one sequence differ in their causal block
+        "msa_bf16_specdec_small": msa_bf16_prefill(seed=19, rows=(2, 3, 4), cache=(150, 700, 255), topk=6,
+                                                   name="msa_bf16_specdec"),
     }
 
 

@@ -23,6 +23,7 @@ int main(void) {
   F(qsa_tensor, data); F(qsa_tensor, dtype); F(qsa_tensor, ndim); F(qsa_tensor, shape);
   printf("qsa_options size %zu\n", sizeof(qsa_options));
   F(qsa_options, kernel); F(qsa_options, splits); F(qsa_options, ctas); F(qsa_options, block_lists);
+  F(qsa_options, heads_per_unit); F(qsa_options, test_stall); F(qsa_options, tcgen05);
   F(qsa_options, reserved);
   return 0;
 }

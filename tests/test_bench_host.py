@@ -58,3 +58,37 @@ def test_committed_traffic_matches_the_sources():
         rec = json.load(f)
     h = bench.kernel_source_hash()
     assert rec and all(e["kernel_hash"] == h for e in rec.values())
+
+
+def test_roofline_bound_follows_l2_reuse():
+    """Selections whose repeats are L2 hits (prefill rows of one sequence)
+    take the tensor bound, with flops = 4 * group * head_dim per attended
+    (key, kv head) pair; one row per sequence (decode) takes the HBM bound."""
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    small = wl.small_variants()
+    pre = small["bf16_prefill_small"].build()
+    r = bench.roofline(pre, 2.0, "k", 1000)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["l2_reuse"] > 2
+    flops = 4 * pre.group * pre.head_dim * int(pre.valid_counts().sum()) * pre.num_kv_heads
+    assert r["flops_per_launch"] == flops
+    assert abs(r["achieved"] - flops / 2e-3 / 1e12) < 1e-9 and abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12
+    assert r["dram"]["traffic"] == 1000 and abs(r["dram"]["achieved"] - 1000 / 2e-3 / 1e9) < 1e-9
+    dec = small["bf16_decode_small"].build()
+    r = bench.roofline(dec, 2.0, "k", None)
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["dram"] is None
+    assert abs(r["achieved"] - dec.algorithmic_bytes() / 2e-3 / 1e9) < 1e-6
+    fp8 = small["fp8_mixed_small"].build()
+    r = bench.roofline(fp8, 2.0, "k", None)
+    if r["bound"] == "tensor":  # fp8: q.K at twice the bf16 rate, p.V at the f16 rate
+        assert abs(r["peak"] - bench.measured_peaks()["bf16_tflops_sustained"] * 4 / 3) < 1e-9
+
+
+def test_cpu_baseline_reports_threads_and_one_thread():
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    x = wl.tiny_ragged().build()
+    cpu = bench.cpu_baseline(x, 1.0, 2)
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 2 and cpu["value"] > 0
+    assert cpu["one_thread"]["cores"] == 1 and cpu["one_thread"]["value"] > 0
+    assert bench.host_cores() >= 1

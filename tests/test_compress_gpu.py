@@ -60,10 +60,21 @@ def test_ratios_and_rotary_widths(ratio, rotary):
 
 
 def test_key_without_page_zeroes_its_block_and_flags():
+    """The first page of sequence 1 names no page of the kv_blocks
+    descriptor: its blocks are zero and flagged.  The descriptor ends one
+    page before the allocation and the entry names that last allocated
+    (NaN-filled) page, so even a regressed check could not read outside the
+    cache."""
     x = SMALL["compress_f32_small"].build()
     tab = x.cache.kv_lookup_table.copy()
-    tab[1, 0] = x.cache.kv_shape[0] + 3  # the first page of sequence 1 names no page
-    got = run_gpu(dataclasses.replace(x, cache=dataclasses.replace(x.cache, kv_lookup_table=tab)))
+    assert x.cache.poison_page == x.cache.kv_shape[0] - 1
+    tab[1, 0] = x.cache.poison_page
+    y = dataclasses.replace(x, cache=dataclasses.replace(x.cache, kv_lookup_table=tab))
+    d = wl.to_torch_compress(y, "cuda")
+    d["kv_blocks"] = d["kv_blocks"][: x.cache.poison_page]  # the descriptor's pages stop before the poison page
+    B.qsa_compress_keys_paged(**d)
+    torch.cuda.synchronize()
+    got = d["block_keys"].float().cpu().double().numpy()
     assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_PAGE
     ref = oracle.compress_keys(x)
     P = x.cache.kv_shape[3]

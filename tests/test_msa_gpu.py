@@ -88,13 +88,22 @@ def test_block_list_edge_cases():
 
 
 def test_missing_page_is_skipped_and_flagged():
+    """A listed block whose table entry names no page of the kv_blocks
+    descriptor is skipped and flagged.  The descriptor ends one page before
+    the allocation and the entry names that last allocated (NaN-filled)
+    page, so even a regressed check could not read outside the cache."""
     x = SMALL["msa_bf16_decode_small"].build()
     seq = x.row_sequence()
     b, blk = int(seq[1]), int(x.d_indices[0, 1, 0])
     tab = x.kv_lookup_table.copy()
-    tab[b, blk] = x.kv_shape[0] + 7  # names no page of kv_blocks
+    assert x.poison_page == x.kv_shape[0] - 1
+    tab[b, blk] = x.poison_page
     bad = dataclasses.replace(x, kv_lookup_table=tab)
-    got = run_gpu(bad)
+    d = wl.to_torch_msa(bad, "cuda")
+    d["kv_blocks"] = d["kv_blocks"][: x.poison_page]  # the descriptor's pages stop before the poison page
+    B.qsa_msa_attention_ragged_paged(**d)
+    torch.cuda.synchronize()
+    got = d["output"].float().cpu().double().numpy()
     assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_PAGE
     d = x.d_indices.copy()  # the expected result: that block unlisted wherever this sequence lists it
     rows = np.nonzero(seq == b)[0]

@@ -76,6 +76,21 @@ def _launches(dtype):
 
 CASES = [(n, i) for n in sorted(SMALL) for i in range(len(_launches(SMALL[n].dtype)))]
 
+# units of the persistent kernel with a forced number of kv heads: eight (2 KB
+# of K per key for BF16, one consumer warp per head) where num_kv_heads and
+# group allow, one and two everywhere, each on split and unsplit grids
+HPU_CASES = []
+for _n in sorted(SMALL):
+    _s = SMALL[_n]
+    if _s.dtype == "f32":
+        continue
+    _g = _s.num_q_heads // _s.num_kv_heads
+    for _h in (1, 2, 8):
+        if _s.num_kv_heads % _h or (_h == 8 and _g > 8):
+            continue
+        for _c in (0, 7, 1000):
+            HPU_CASES.append((_n, _h, _c))
+
 
 @pytest.mark.parametrize("name,launch", CASES)
 def test_small_workloads_match_oracle(name, launch):
@@ -85,6 +100,32 @@ def test_small_workloads_match_oracle(name, launch):
     ref = oracle.sparse_attention(x)
     assert_close(got, ref, x.dtype, f"{name} {kw}")
     assert status_clean()
+
+
+@pytest.mark.parametrize("name,hpu,ctas", HPU_CASES)
+def test_heads_per_unit_match_oracle(name, hpu, ctas):
+    x = SMALL[name].build()
+    kw = dict(kernel=3, heads_per_unit=hpu, ctas=ctas)
+    assert_close(run_gpu(x, **kw), oracle.sparse_attention(x), x.dtype, f"{name} {kw}")
+    assert status_clean()
+
+
+def test_give_up_path_reports_timeout_and_keeps_the_stream_usable():
+    """A test-only launch makes the persistent kernel's producers issue no K/V
+    copies, so every consumer wait gives up after a few thousand polls (no
+    copy is in flight when a CTA leaves) and the call reports
+    QSA_STATUS_TIMEOUT.  The CTAs still arrive on the tickets of the units
+    they share, so the next calls on the same stream, with the same grid and
+    workspace, match the oracle again."""
+    x = SMALL["bf16_decode_small"].build()
+    ref = oracle.sparse_attention(x)
+    for ctas in (7, 64):  # more units than CTAs (scanned split), then units spread over several CTAs
+        B.qsa_read_device_status(clear=True)
+        run_gpu(x, kernel=3, ctas=ctas, test_stall=1)
+        assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_TIMEOUT
+        for _ in range(2):
+            assert_close(run_gpu(x, kernel=3, ctas=ctas), ref, "bf16", f"after a give-up, ctas {ctas}")
+            assert status_clean()
 
 
 def test_worked_example_on_gpu():
@@ -264,12 +305,24 @@ def test_zero_width_selection():
 
 
 def test_out_of_range_positions_are_skipped_and_reported():
+    """Positions inside counts but at or past the sequence's length are
+    skipped and flagged.  The bad values lie in [kv_len, max_pages * page_size):
+    their table entries name the sequence's last page (slots past kv_len)
+    or the poison page, both allocated and NaN-filled, so even a kernel whose
+    range check regressed could only read NaN inside the cache, never outside
+    any tensor.  (No negative value has that property, so negative positions
+    are left to the same comparison, pos < 0 || pos >= kv_len.)"""
     x = SMALL["bf16_decode_small"].build()
     n = x.valid_counts()
-    bad_rows = [0, 2, 5]
+    P, max_pages = x.kv_shape[3], x.kv_lookup_table.shape[1]
+    seq = x.row_sequence()
+    kv_len = x.cache_lengths.astype(np.int64) + np.diff(x.input_row_offsets.astype(np.int64))
+    bad_rows = [r for r in range(x.total_q) if kv_len[seq[r]] + P < max_pages * P and n[r] >= 3][:3]
+    assert len(bad_rows) == 3
     for r in bad_rows:
-        x.token_indices[r, 1] = 10**7          # past the sequence
-        x.token_indices[r, n[r] - 1] = -3      # negative
+        x.token_indices[r, 1] = kv_len[seq[r]]          # the first position past the sequence
+        x.token_indices[r, n[r] - 1] = kv_len[seq[r]] + P - 1  # a later page of the table row
+    assert (x.token_indices[bad_rows][:, [1]] < max_pages * P).all()
     # expected: the same rows with those entries removed
     y = SMALL["bf16_decode_small"].build()
     for r in bad_rows:
@@ -278,7 +331,8 @@ def test_out_of_range_positions_are_skipped_and_reported():
         y.token_indices[r, : len(sel)] = sel
         y.counts[r] = len(sel)
     ref = oracle.sparse_attention(y)
-    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=3), dict(kernel=3, ctas=4)):
+    for launch in (dict(), dict(kernel=1), dict(kernel=2, splits=3), dict(kernel=3, ctas=4),
+                   dict(kernel=3, heads_per_unit=8)):
         B.qsa_read_device_status(clear=True)
         got = run_gpu(x, **launch)
         assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_INDEX
@@ -286,17 +340,33 @@ def test_out_of_range_positions_are_skipped_and_reported():
 
 
 def test_bad_page_table_entry_is_skipped_and_reported():
+    """A table entry naming no page of the kv_blocks descriptor is skipped and
+    flagged.  The descriptor ends one page before the allocation and the bad
+    entry names that last allocated (NaN-filled) page, so even a regressed
+    check could not read outside the cache."""
     x = SMALL["bf16_decode_small"].build()
     r = 1
     b = x.row_sequence()[r]
     p = int(x.token_indices[r, 0])
     lp = p // x.kv_shape[3]
-    x.kv_lookup_table[b, lp] = 0xFFFFFFF0  # names no page
-    for launch in (dict(), dict(kernel=2), dict(kernel=1)):
+    assert x.poison_page == x.kv_shape[0] - 1
+    x.kv_lookup_table[b, lp] = x.poison_page
+    # expected: row r's keys on that page removed (no other row of sequence b exists in this decode batch)
+    assert (x.row_sequence() == b).sum() == 1
+    y = SMALL["bf16_decode_small"].build()
+    sel = [int(v) for v in y.token_indices[r, : y.counts[r]] if int(v) // x.kv_shape[3] != lp]
+    y.token_indices[r, : len(sel)] = sel
+    y.counts[r] = len(sel)
+    ref = oracle.sparse_attention(y)
+    for launch in (dict(), dict(kernel=2), dict(kernel=1), dict(kernel=3, heads_per_unit=8)):
+        d = wl.to_torch(x, "cuda")
+        d["kv_blocks"] = d["kv_blocks"][: x.poison_page]  # the descriptor's pages stop before the poison page
         B.qsa_read_device_status(clear=True)
-        got = run_gpu(x, **launch)
+        B.qsa_sparse_attention_ragged_paged(**d, **launch)
+        torch.cuda.synchronize()
+        got = d["output"].float().cpu().double().numpy()
         assert B.qsa_read_device_status(clear=True) & B.QSA_STATUS_BAD_PAGE
-        assert np.isfinite(got).all()
+        assert_close(got, ref, "bf16", f"bad page {launch}")
 
 
 def test_rows_outside_every_sequence_are_zero_and_reported():
