@@ -53,6 +53,7 @@ def parse():
     ap.add_argument("--splits", type=int, default=0, help="kernel 2: force CTAs per (row, kv head)")
     ap.add_argument("--ctas", type=int, default=0, help="kernel 3: force the persistent grid size")
     ap.add_argument("--heads-per-unit", type=int, default=0, help="kernel 3: force the kv heads per unit")
+    ap.add_argument("--tcgen05", type=int, default=0, help="kernel 2: 1 the tcgen05 consumer, -1 mma.sync")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle time budget of the CPU baseline")
     ap.add_argument("--cpu-threads", type=int, default=0, help="oracle threads (0: every core this process may use)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -533,7 +534,7 @@ def main():
         width = x.topk * x.kv_shape[3] if blocks else x.selection_width
         plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
                           kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas, block_lists=blocks,
-                          heads_per_unit=0 if blocks else args.heads_per_unit)
+                          heads_per_unit=0 if blocks else args.heads_per_unit, tcgen05=args.tcgen05)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
@@ -555,10 +556,10 @@ def main():
         if latent:
             B.qsa_latent_attention_ragged_paged(**d, splits=args.splits)
         elif blocks:
-            B.qsa_msa_attention_ragged_paged(**d, splits=args.splits)
+            B.qsa_msa_attention_ragged_paged(**d, splits=args.splits, tcgen05=args.tcgen05)
         else:
             B.qsa_sparse_attention_ragged_paged(**d, kernel=args.kernel, splits=args.splits, ctas=args.ctas,
-                                                heads_per_unit=args.heads_per_unit)
+                                                heads_per_unit=args.heads_per_unit, tcgen05=args.tcgen05)
 
     def barrier():
         torch.cuda.synchronize()
@@ -661,6 +662,8 @@ def main():
                     "parallelism": f"replicas x{world}"})
         if args.heads_per_unit:
             cfg["heads_per_unit"] = args.heads_per_unit
+        if args.tcgen05:
+            cfg["tcgen05"] = args.tcgen05
         if latent and plan["splits"] == 1 and (x.num_heads // min(x.num_heads, 16)) % 4 == 0:
             # the launch serves four 16-head groups of a row per CTA (qsa_plan counts one per group)
             cfg["ctas"] = plan["ctas"] // 4

@@ -441,10 +441,11 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   uint32_t* s_off = reinterpret_cast<uint32_t*>(smem + C::RING + C::QBYTES);
   uint64_t* s_full = reinterpret_cast<uint64_t*>(s_off + kMmaMaxBand);  // TILES: one barrier per stage
   int2* s_tile = reinterpret_cast<int2*>(s_full + C::STAGES);           // TILES: tile copy (page, first slot) or (-1, 0)
-  // UMMA: per-warp maxima and sums [NW][16], the q.K and p.V barriers, the tensor-memory base
+  // UMMA: per-warp maxima and sums [NW][16], the barriers of q.K (two S^T
+  // buffers) and p.V, the tensor-memory base
   float* u_red = reinterpret_cast<float*>(s_tile + C::MAXT);
   uint64_t* u_bar = reinterpret_cast<uint64_t*>(u_red + NW * 16);
-  uint32_t* u_tmem = reinterpret_cast<uint32_t*>(u_bar + 2);
+  uint32_t* u_tmem = reinterpret_cast<uint32_t*>(u_bar + 3);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -452,17 +453,19 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     // a stage's barrier completes a phase when a tile copy into it landed
     // (16-byte copies complete through per-thread cp.async groups instead)
     for (int k = 0; k < C::STAGES; ++k) mbar_init(smem_addr(&s_full[k]), 1);
-    if (UMMA) {  // one tcgen05 commit per tile on each
+    if (UMMA) {  // q.K of even and of odd tiles, p.V: one tcgen05 commit per phase
       mbar_init(smem_addr(&u_bar[0]), 1);
       mbar_init(smem_addr(&u_bar[1]), 1);
+      mbar_init(smem_addr(&u_bar[2]), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if constexpr (UMMA) {
-    // 32 tensor-memory columns: S^T in [0, GP), O^T in [16, 32)
+    // 64 tensor-memory columns: two S^T buffers at 0 and 16, O^T in [32, 48)
     if (warp == 0) {
-      tmem_alloc(smem_addr(u_tmem), 32);
+      tmem_alloc(smem_addr(u_tmem), 64);
       tmem_relinquish();
+      tc_fence_before();  // the address is read after the translation's barriers
     }
   }
 
@@ -660,10 +663,15 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   }
 
   const int hc = p.head_bytes ? h : 0;  // the unit's head in the cache (the latent cache has one)
+  // stages that received a tile copy, and the parity of each stage's next
+  // tile-copy phase (identical in every thread): a give-up drains them
+  uint32_t tma_used = 0, tma_next = 0;
   auto issue = [&](int t) {
     unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
     const uint32_t bar = smem_addr(&s_full[t % C::STAGES]);
     if (TILES && (tma_mask >> t & 1u)) {
+      tma_used |= 1u << (t % C::STAGES);
+      tma_next ^= 1u << (t % C::STAGES);
       if (tid == 0) {
         const int2 tc = s_tile[t];
         tile_fence_proxy_async();  // earlier generic accesses of the stage before the async-proxy writes
@@ -726,6 +734,7 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   // UMMA state: the tensor-memory base, each head's reference maximum (the
   // same in every thread) and this thread's key's share of each head's sum
   uint32_t tmem = 0;
+  int issued = 0, issued_qk = 0;  // tiles whose p.V / q.K were issued (the same in every thread)
   float m_ref[GP], l_part[GP];
   if constexpr (UMMA) {
     tc_fence_after();  // the allocation's address, published by the translation's barriers
@@ -737,95 +746,130 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     }
   }
 
-  for (int t = 0; t < ntiles; ++t) {
-    cp_async_wait<C::STAGES - 2>();  // this thread's 16-byte copies of tile t
-    if constexpr (UMMA) {
-      // this thread's copies into tile t visible to the tensor cores; p.V of
-      // tile t - 1 done (its stage is refilled below, O^T may be rescaled)
+  if constexpr (UMMA) {
+    // Pipeline, per tile t (every thread, uniform control flow):
+    //   A  tile t + 1's bytes landed -> q.K(t + 1) into the other S^T buffer
+    //      (the tensor cores run it during this tile's softmax)
+    //   B  S^T(t) read; p.V(t - 1) done (O^T stable, its stage free)
+    //   D  tile t + 2 copied into the stage tile t - 1 used
+    //   B' when a key passes its head's reference by more than 8, the exact
+    //      tile maxima move the references and O^T is rescaled; P^T(t) written
+    //   C  p.V(t)
+    // S^T buffer b (tiles of parity b) has its own barrier, so no wait can
+    // see a later phase of it; p.V's barrier is waited for tile t - 1 before
+    // p.V(t) is issued.  Ring of three stages: the copies of tile t + 1 are
+    // the newest when step A waits for them.
+    static_assert(C::STAGES == 3, "the pipeline's copy waits assume three stages");
+    constexpr uint32_t kO = 32;  // O^T columns; S^T buffers at 0 and 16
+    auto wait_tile = [&](int t) -> bool {  // this thread's copies of tile t, visible to the tensor cores
+      cp_async_wait<0>();
       fence_proxy_async_smem();
-      const bool lost = t > 0 && !mbar_wait_asm(smem_addr(&u_bar[1]), (uint32_t)((t - 1) & 1));
-      if (__syncthreads_or(lost || timed_out)) {  // every thread takes the same decision
-        timed_out = true;
-        break;
+      bool ok = true;
+      if (TILES && (tma_mask >> t & 1u)) {
+        const int st = t % C::STAGES;
+        ok = mbar_wait_asm(smem_addr(&s_full[st]), (tma_phase >> st) & 1u) != 0;
+        tma_phase ^= 1u << st;
       }
-    } else {
-      __syncthreads();  // everyone's copies of tile t landed; every warp is done with tile t - 1
-    }
-    if (t + C::STAGES - 1 < ntiles) issue(t + C::STAGES - 1);
-    cp_async_commit();
-    if (TILES && (tma_mask >> t & 1u)) {
-      const int st = t % C::STAGES;
-      if (!mbar_wait_asm(smem_addr(&s_full[st]), (tma_phase >> st) & 1u)) timed_out = true;
-      tma_phase ^= 1u << st;
-    }
-
-    const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
-    if constexpr (UMMA) {
-      const uint32_t kb = smem_addr(sb), vb = kb + (uint32_t)C::KV_BYTES;
-      // q.K: 8 K steps of 16 channels (4 per 128-byte line block), scores of
-      // key k in lane (k / 16) * 32 + k % 16, columns [0, GP)
-      if (tid == 0) {
-        tc_fence_after();
+      return ok;
+    };
+    auto issue_qk = [&](int t) {  // thread 0
+      const uint32_t kb = smem_addr(smem + (t % C::STAGES) * C::STAGE_BYTES);
+      tc_fence_after();
 #pragma unroll
-        for (int ks = 0; ks < C::KSTEPS; ++ks)
-          umma_f16(tmem,
-                   smem_desc(kb + (uint32_t)((ks >> 2) * C::LINE_BYTES + (ks & 3) * 32), 16, 1024, kSwizzle128),
-                   smem_desc(smem_addr(q_tile) + (uint32_t)((ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, kSwizzle128),
-                   instr_desc(64, GP, 1, 0, 0), ks > 0);
-        umma_commit(smem_addr(&u_bar[0]));
+      for (int ks = 0; ks < C::KSTEPS; ++ks)
+        umma_f16(tmem + (uint32_t)((t & 1) * 16),
+                 smem_desc(kb + (uint32_t)((ks >> 2) * C::LINE_BYTES + (ks & 3) * 32), 16, 1024, kSwizzle128),
+                 smem_desc(smem_addr(q_tile) + (uint32_t)((ks >> 2) * 2048 + (ks & 3) * 32), 16, 1024, kSwizzle128),
+                 instr_desc(64, GP, 1, 0, 0), ks > 0);
+      umma_commit(smem_addr(&u_bar[t & 1]));
+    };
+    if (ntiles > 0) {
+      if (__syncthreads_or(!wait_tile(0))) {
+        timed_out = true;
+      } else {
+        if (tid == 0) issue_qk(0);
+        issued_qk = 1;
       }
-      if (!mbar_wait_asm(smem_addr(&u_bar[0]), (uint32_t)(t & 1))) timed_out = true;
+    }
+    for (int t = 0; t < ntiles && !timed_out; ++t) {
+      const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
+      const uint32_t kb = smem_addr(sb), vb = kb + (uint32_t)C::KV_BYTES;
+      // A
+      if (t + 1 < ntiles) {
+        if (__syncthreads_or(!wait_tile(t + 1))) {
+          timed_out = true;
+          break;
+        }
+        if (tid == 0) issue_qk(t + 1);
+        ++issued_qk;
+      }
+      // B: scores of key k in lane (k / 16) * 32 + k % 16
+      bool lost = !mbar_wait_asm(smem_addr(&u_bar[t & 1]), (uint32_t)((t >> 1) & 1));
       tc_fence_after();
       float sv[GP];
-      if constexpr (GP == 8) tmem_ld8(tmem + ((uint32_t)(warp * 32) << 16), sv);
-      else tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), sv);
-      // this lane's key (lanes 16..31 hold no row of the 64-row product)
+      const uint32_t srow = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)((t & 1) * 16);
+      if constexpr (GP == 8) tmem_ld8(srow, sv);
+      else tmem_ld16(srow, sv);
+      if (t > 0) lost |= !mbar_wait_asm(smem_addr(&u_bar[2]), (uint32_t)((t - 1) & 1));
+      // D: the stage of tile t - 1 (its p.V is done) takes tile t + 2, whose
+      // copies then overlap this tile's softmax and p.V (after a give-up it
+      // is left alone: the stage may still be read)
+      if (t + C::STAGES - 1 < ntiles && !lost) issue(t + C::STAGES - 1);
+      cp_async_commit();
       const int kk = t * C::TILE + warp * 16 + (lane & 15);
       const bool valid = lane < 16 && kk < band_keys && s_off[kk] != kInvalidOff;
-#pragma unroll
-      for (int n = 0; n < GP; ++n) sv[n] = valid && n < p.group ? sv[n] * p.scale_log2 : -CUDART_INF_F;
+      bool want = false;
 #pragma unroll
       for (int n = 0; n < GP; ++n) {
-        float mx = sv[n];
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        if (lane == 0) u_red[warp * 16 + n] = mx;
+        sv[n] = valid && n < p.group ? sv[n] * p.scale_log2 : -CUDART_INF_F;
+        want |= sv[n] > m_ref[n] + 8.f;
       }
-      __syncthreads();
-      // the tile's maximum per head; the reference moves when the tile passes
-      // it by more than 8, so every term 2^(s - ref) stays <= 256 (every thread
-      // computes the same decision from the same values)
-      float alpha[GP];
-      bool moved = false;
+      if (__syncthreads_or(want || lost)) {
+        // the tile's maxima per head, across the warps; every thread moves the
+        // references it passes by more than 8 the same way
 #pragma unroll
-      for (int n = 0; n < GP; ++n) {
-        const float mt = fmaxf(fmaxf(u_red[n], u_red[16 + n]), fmaxf(u_red[32 + n], u_red[48 + n]));
-        alpha[n] = 1.f;
-        if (mt > m_ref[n] + 8.f) {
-          alpha[n] = m_ref[n] == -CUDART_INF_F ? 0.f : exp2f(m_ref[n] - mt);
-          m_ref[n] = mt;
-          moved = true;
+        for (int n = 0; n < GP; ++n) {
+          float mx = sv[n];
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          if (lane == 0) u_red[warp * 16 + n] = mx;
         }
-      }
-      if (moved && t > 0) {
-        // O^T (this warp's 32 channels, 16 head columns) to the new references
-        float ov[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16u, ov);
+        __syncthreads();
+        float alpha[GP];
+        bool moved = false;
 #pragma unroll
-        for (int n = 0; n < GP; ++n) ov[n] *= alpha[n];
-        tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + 16u, ov);
-        tmem_wait_st();
+        for (int n = 0; n < GP; ++n) {
+          const float mt = fmaxf(fmaxf(u_red[n], u_red[16 + n]), fmaxf(u_red[32 + n], u_red[48 + n]));
+          alpha[n] = 1.f;
+          if (mt > m_ref[n] + 8.f) {
+            alpha[n] = m_ref[n] == -CUDART_INF_F ? 0.f : exp2f(m_ref[n] - mt);
+            m_ref[n] = mt;
+            moved = true;
+          }
+          l_part[n] *= alpha[n];
+        }
+        if (moved && t > 0) {
+          // O^T (this warp's 32 channels, 16 head columns) to the new references
+          float ov[16];
+          tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + kO, ov);
+#pragma unroll
+          for (int n = 0; n < GP; ++n) ov[n] *= alpha[n];
+          tmem_st16(tmem + ((uint32_t)(warp * 32) << 16) + kO, ov);
+          tmem_wait_st();
+        }
+        __syncthreads();  // u_red is read by every thread before the next tile writes it
       }
 #pragma unroll
       for (int n = 0; n < GP; ++n) {
         const float pn = exp2_fast(sv[n] - (m_ref[n] == -CUDART_INF_F ? 0.f : m_ref[n]));
-        l_part[n] = l_part[n] * alpha[n] + pn;
+        l_part[n] += pn;
         sv[n] = pn;
       }
-      // P^T, MN-major without swizzle: key k's 16 head values at
-      // (k / 8) * 256 + (k % 8) * 16 (heads 0..7) and +128 (heads 8..15)
+      // P^T, MN-major without swizzle, over the stage's first 2 KB (q.K(t)
+      // has read those K rows): key k's 16 head values at (k / 8) * 256 +
+      // (k % 8) * 16 (heads 0..7) and +128 (heads 8..15)
       if (lane < 16) {
         const int k = warp * 16 + lane;
         unsigned char* pr = const_cast<unsigned char*>(sb) + (k >> 3) * 256 + (k & 7) * 16;
@@ -839,19 +883,35 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
       }
       fence_proxy_async_smem();
       tc_fence_before();
-      __syncthreads();
-      // p.V: 4 K steps of 16 keys; O^T in columns [16, 32), lane = channel
+      if (__syncthreads_or(lost)) {
+        timed_out = true;
+        break;
+      }
+      // C: p.V, 4 K steps of 16 keys; O^T in columns [32, 48), lane = channel
       if (tid == 0) {
         tc_fence_after();
 #pragma unroll
         for (int ks = 0; ks < C::TILE / 16; ++ks)
-          umma_f16(tmem + 16u, smem_desc(vb + (uint32_t)(ks * 2048), (uint32_t)C::LINE_BYTES, 1024, kSwizzle128),
+          umma_f16(tmem + kO, smem_desc(vb + (uint32_t)(ks * 2048), (uint32_t)C::LINE_BYTES, 1024, kSwizzle128),
                    smem_desc(kb + (uint32_t)(ks * 512), 256, 128, kSwizzleNone), instr_desc(128, 16, 1, 1, 1),
                    t > 0 || ks > 0);
-        umma_commit(smem_addr(&u_bar[1]));
+        umma_commit(smem_addr(&u_bar[2]));
       }
-      continue;
+      ++issued;
     }
+  } else
+  for (int t = 0; t < ntiles; ++t) {
+    cp_async_wait<C::STAGES - 2>();  // this thread's 16-byte copies of tile t
+    __syncthreads();  // everyone's copies of tile t landed; every warp is done with tile t - 1
+    if (t + C::STAGES - 1 < ntiles) issue(t + C::STAGES - 1);
+    cp_async_commit();
+    if (TILES && (tma_mask >> t & 1u)) {
+      const int st = t % C::STAGES;
+      if (!mbar_wait_asm(smem_addr(&s_full[st]), (tma_phase >> st) & 1u)) timed_out = true;
+      tma_phase ^= 1u << st;
+    }
+
+    const unsigned char* sb = smem + (t % C::STAGES) * C::STAGE_BYTES;
 #pragma unroll 1
     for (int sl = 0; sl < (GROUPS ? NW : 1); ++sl) {
     const int kw = GROUPS ? sl : warp;  // the 16-key slice of the tile this warp scores
@@ -960,13 +1020,16 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
   }
   float u_o[16];  // UMMA: O^T of this thread's channel (tid), one value per head column
   if constexpr (UMMA) {
-    // p.V of the last tile done; then every head's sum over all key lanes,
+    // p.V of the last tile done (its commit also covers every earlier MMA, so
+    // after a give-up nothing of ours is still running either, unless this
+    // bounded wait gives up too); then every head's sum over all key lanes,
     // and the tensor memory handed back
-    if (!timed_out && ntiles > 0 && !mbar_wait_asm(smem_addr(&u_bar[1]), (uint32_t)((ntiles - 1) & 1)))
-      timed_out = true;
+    if (issued > 0 && !mbar_wait_asm(smem_addr(&u_bar[2]), (uint32_t)((issued - 1) & 1))) timed_out = true;
+    if (timed_out && issued_qk > issued)  // a q.K issued after the last p.V
+      mbar_wait_asm(smem_addr(&u_bar[(issued_qk - 1) & 1]), (uint32_t)(((issued_qk - 1) >> 1) & 1));
     tc_fence_after();
-    if (ntiles > 0) {
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16u, u_o);
+    if (issued > 0) {
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 32u, u_o);
     } else {
 #pragma unroll
       for (int n = 0; n < 16; ++n) u_o[n] = 0.f;
@@ -983,9 +1046,16 @@ __global__ void __launch_bounds__(kMmaThreads, 2) mma_kernel(const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 32);
+    if (warp == 0) tmem_dealloc(tmem, 64);
   }
-  if (timed_out) atomicOr(p.status, QSA_STATUS_TIMEOUT);
+  if (timed_out) {
+    atomicOr(p.status, QSA_STATUS_TIMEOUT);
+    // a tile copy whose wait gave up may still be landing: wait again
+    // (bounded) for each stage's last tile-copy phase before the ring is reused
+    if (TILES && tid == 0)
+      for (int st = 0; st < C::STAGES; ++st)
+        if ((tma_used >> st) & 1u) mbar_wait_asm(smem_addr(&s_full[st]), ((tma_next >> st) & 1u) ^ 1u);
+  }
   cp_async_wait<0>();
   __syncthreads();  // the ring is drained; its shared memory now holds the warp states
 

@@ -2,10 +2,13 @@
 // "Gather-GQA over the token indices a QSA selection names").
 //
 // One CTA of 4 warps per (query row, kv head).  Warps take the row's selected
-// positions round-robin; for each one a warp reads the K row (each lane a
-// head_dim/32 slice), forms the `group` dot products with warp-shuffle sums,
-// updates a base-2 online softmax per query head and accumulates the V row.
-// The four warp states are merged in shared memory at the end.  This kernel
+// positions U at a time, round-robin (the page's `unroll`: gathered keys
+// loaded before any is consumed): lanes 0..U-1 translate one position each
+// (index, then page-table entry, all U in flight together), then every lane
+// loads its head_dim/32 slice of all U K and V rows before the first is
+// used.  Per key the warp forms the `group` dot products with warp-shuffle
+// sums, updates a base-2 online softmax per query head and accumulates the V
+// row.  The four warp states are merged in shared memory at the end.  This kernel
 // serves FP32 (whose 1e-4 tolerance rules out TF32 tensor cores) and every
 // (dtype, head_dim, group) the tensor-core kernel does not cover.
 #include <cuda_bf16.h>
@@ -99,34 +102,49 @@ __global__ void __launch_bounds__(128) simt_kernel(const Params p) {
 
   uint32_t bad = ri.ok ? 0u : QSA_STATUS_BAD_ROW;
   const int32_t* idx_row = p.indices + (int64_t)r * p.W;
-  for (int j = warp; j < ri.n; j += NW) {
-    const int32_t pos = __ldg(idx_row + j);
-    const int64_t lp = logical_page(p, ri.kv_len, pos, bad);
-    if (lp < 0) continue;
-    const uint32_t page = __ldg(p.table + (int64_t)ri.b * p.max_pages + lp);
-    const uint32_t off = k_row_offset16(p, page, pos, h, bad);
-    if (off == kInvalidOff) continue;
-    const unsigned char* krow = p.kv + (int64_t)off * 16;
-    float k[EPL], v[EPL];
-    load_slice<ELEM, EPL>(krow, lane, k);
-    load_slice<ELEM, EPL>(krow + p.v_minus_k_bytes, lane, v);
+  // keys in flight per warp: 8, or 4 when the group's accumulators are large
+  constexpr int U = G * EPL <= 32 ? 8 : 4;
+  for (int j0 = warp * U; j0 < ri.n; j0 += NW * U) {
+    // lane u < U translates key j0 + u (entries past counts are never read)
+    uint32_t off = kInvalidOff;
+    if (lane < U && j0 + lane < ri.n) {
+      const int32_t pos = __ldg(idx_row + j0 + lane);
+      const int64_t lp = logical_page(p, ri.kv_len, pos, bad);
+      if (lp >= 0) off = k_row_offset16(p, __ldg(p.table + (int64_t)ri.b * p.max_pages + lp), pos, h, bad);
+    }
+    uint32_t offs[U];
+    float k[U][EPL], v[U][EPL];
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      float dot = 0.f;
+    for (int u = 0; u < U; ++u) {
+      offs[u] = __shfl_sync(0xffffffffu, off, u);
+      if (offs[u] != kInvalidOff) {
+        const unsigned char* krow = p.kv + (int64_t)offs[u] * 16;
+        load_slice<ELEM, EPL>(krow, lane, k[u]);
+        load_slice<ELEM, EPL>(krow + p.v_minus_k_bytes, lane, v[u]);
+      }
+    }
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) dot = fmaf(qr[i][e], k[e], dot);
+    for (int u = 0; u < U; ++u) {
+      if (offs[u] == kInvalidOff) continue;  // (the same in every lane)
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      const float s = dot * p.scale_log2;
-      const float mn = fmaxf(m[i], s);
-      const float alpha = exp2f(m[i] - mn);
-      const float pe = exp2f(s - mn);
-      l[i] = l[i] * alpha + pe;
+      for (int i = 0; i < G; ++i) {
+        float dot = 0.f;
 #pragma unroll
-      for (int e = 0; e < EPL; ++e) acc[i][e] = fmaf(acc[i][e], alpha, pe * v[e]);
-      m[i] = mn;
+        for (int e = 0; e < EPL; ++e) dot = fmaf(qr[i][e], k[u][e], dot);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+        const float s = dot * p.scale_log2;
+        const float mn = fmaxf(m[i], s);
+        const float alpha = exp2f(m[i] - mn);
+        const float pe = exp2f(s - mn);
+        l[i] = l[i] * alpha + pe;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) acc[i][e] = fmaf(acc[i][e], alpha, pe * v[u][e]);
+        m[i] = mn;
+      }
     }
   }
+  bad = __reduce_or_sync(0xffffffffu, bad);  // the translating lanes' flags
   if (bad && lane == 0) atomicOr(p.status, bad);
 
 #pragma unroll

@@ -626,7 +626,16 @@ __global__ void __launch_bounds__(StreamCfg<KIND, NT, HPU>::THREADS, 1) stream_k
       hist[0] = meta_issued;
     }
     cp_async_wait_all();  // no copy of ours may land after we leave
-    if (aborted) bad |= QSA_STATUS_TIMEOUT;
+    if (aborted) {
+      bad |= QSA_STATUS_TIMEOUT;
+      // Bulk copies are not covered by the wait above: before leaving, wait
+      // (bounded again) for the last STAGES tiles' full barriers, whose phases
+      // complete when their bytes have landed (phases complete in order, so
+      // earlier uses of a stage are then done too).  A test stall issued none.
+      if (C::BULK && !p.stall && tid == 0)
+        for (int o = max(0, ckv.o - S); o < ckv.o; ++o)
+          if (!mbar_wait(smem_addr(&s_full[o % S]), (uint32_t)((o / S) & 1))) break;
+    }
     if (bad) atomicOr(p.status, bad);
     return;
   }
