@@ -40,6 +40,16 @@ FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
 NOMINAL_HBM_GBS = 8000.0
+# Fixed costs of one call of the per-(row, kv head) kernel, measured on a
+# GB300 with CUDA events and a per-CTA globaltimer trace of the long-context
+# decode launch: an empty kernel of the same grid, the three dependent trips
+# to memory before the first gathered byte (row search with counts and Q,
+# the band's list entries, the page-table entries), and the cluster merge of
+# split bands.  With the algorithmic bytes at the copy peak they give the
+# floor a call of that kernel cannot beat.
+EMPTY_LAUNCH_US = 4.1
+DEPENDENT_TRIPS_US = 4.3
+CLUSTER_MERGE_US = 1.0
 
 
 def parse():
@@ -124,6 +134,18 @@ def roofline(x, ms: float, kernel: str, traffic) -> dict:
                 "flops_per_launch": flops, **common}
     return {"bound": "hbm", "achieved": eff_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s", "frac": eff_gbs / pk["hbm_gbs"],
             "peak_source": f"{pk['source']} (MEASURED_PEAKS hbm_gbs copy)", **common}
+
+
+def latency_floor(x, ms: float, splits: int) -> dict:
+    """Floor of a per-(row, kv head) kernel call: launch + three dependent
+    trips + the algorithmic bytes at the measured copy peak (+ the merge when
+    bands are split), beside the measured time."""
+    pk = measured_peaks()
+    hbm_us = x.algorithmic_bytes() / (pk["hbm_gbs"] * 1e3)
+    fixed = EMPTY_LAUNCH_US + DEPENDENT_TRIPS_US + (CLUSTER_MERGE_US if splits > 1 else 0.0)
+    floor = fixed + hbm_us
+    return {"floor_us": floor, "fixed_us": fixed, "bytes_at_copy_peak_us": hbm_us, "time_us": ms * 1e3,
+            "frac_of_floor": floor / (ms * 1e3)}
 
 
 def _code_only(text: str) -> str:
@@ -664,6 +686,8 @@ def main():
             cfg["heads_per_unit"] = args.heads_per_unit
         if args.tcgen05:
             cfg["tcgen05"] = args.tcgen05
+        if plan["kernel"] == 2:
+            roof["floor"] = latency_floor(x, ms_per_step, plan["splits"])
         if latent and plan["splits"] == 1 and (x.num_heads // min(x.num_heads, 16)) % 4 == 0:
             # the launch serves four 16-head groups of a row per CTA (qsa_plan counts one per group)
             cfg["ctas"] = plan["ctas"] // 4
