@@ -126,3 +126,29 @@ def test_forced_kernel_limits(lib):
     opt = B.qsa_options(kernel=7)
     st = lib.qsa_sparse_attention_ragged_paged_ex(*[_args()[k] for k in order], ctypes.byref(opt))
     assert st == 5
+
+
+def test_launch_option_limits(lib):
+    """The launch controls added for tests and sweeps are checked with the
+    arguments, before anything is launched."""
+    order = ["output", "q", "input_row_offsets", "kv_blocks", "page_stride", "cache_lengths", "kv_lookup_table",
+             "max_prompt_length", "max_cache_length", "layer_idx", "token_indices", "counts", "scale", "group",
+             "stream"]
+
+    def ex(opt, **over):
+        return lib.qsa_sparse_attention_ragged_paged_ex(*[_args(**over)[k] for k in order], ctypes.byref(opt))
+
+    e4m3 = dict(q=_t((5, 8, 128), B.QSA_F8E4M3), kv_blocks=_t((10, 2, 3, 16, 2, 128), B.QSA_F8E4M3))
+    cases = [
+        (B.qsa_options(kernel=3, heads_per_unit=3), {}, 5),   # not 1, 2, 4 or 8
+        (B.qsa_options(kernel=3, heads_per_unit=4), {}, 5),   # does not divide 2 kv heads
+        (B.qsa_options(kernel=2, heads_per_unit=2), {}, 4),   # only the persistent kernel groups heads
+        (B.qsa_options(kernel=1, test_stall=1), {}, 4),       # only the persistent kernel stalls
+        (B.qsa_options(kernel=2, tcgen05=2), {}, 5),          # -1, 0 or 1
+        (B.qsa_options(kernel=3, tcgen05=1), {}, 4),          # only kernel 2 has the tcgen05 consumer
+        (B.qsa_options(kernel=2, tcgen05=1), e4m3, 4),        # which reads BF16 caches
+    ]
+    for opt, over, code in cases:
+        st = ex(opt, **over)
+        assert st == code, (opt.kernel, opt.heads_per_unit, opt.test_stall, opt.tcgen05, B.STATUS_NAMES.get(st),
+                            lib.qsa_last_error_message())
