@@ -402,3 +402,16 @@ def test_full_size_workload_sampled_rows(name):
     assert_close(got[rows], ref, x.dtype, name)
     assert np.isfinite(got).all()
     assert status_clean()
+
+
+@pytest.mark.parametrize("ctas", [0, 7, 1000])
+def test_fp8_eight_head_units_match_oracle(ctas):
+    """FP8 with 8 kv heads (1 KB of K per key for eight heads): the persistent
+    kernel's eight-head units, on split and unsplit grids."""
+    import dataclasses
+
+    spec = dataclasses.replace(wl.small_variants()["fp8_mixed_small"], num_q_heads=64, num_kv_heads=8)
+    x = spec.build()
+    kw = dict(kernel=3, heads_per_unit=8, ctas=ctas)
+    assert_close(run_gpu(x, **kw), oracle.sparse_attention(x), "e4m3", f"fp8 eight-head units {kw}")
+    assert status_clean()
