@@ -59,7 +59,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="bf16_chunked_prefill")
-    ap.add_argument("--kernel", type=int, default=0, help="force 1 CUDA-core / 2 tensor-core kernel")
+    ap.add_argument("--kernel", type=int, default=0, help="force 1 CUDA-core, 2 per-(row, kv head), 3 stream-K or 4 row-group kernel")
     ap.add_argument("--splits", type=int, default=0, help="kernel 2: force CTAs per (row, kv head)")
     ap.add_argument("--ctas", type=int, default=0, help="kernel 3: force the persistent grid size")
     ap.add_argument("--heads-per-unit", type=int, default=0, help="kernel 3: force the kv heads per unit")
@@ -554,9 +554,11 @@ def main():
                           kernel=2, splits=args.splits)
     else:
         width = x.topk * x.kv_shape[3] if blocks else x.selection_width
+        extents = {} if blocks else dict(batch=x.batch, page_size=x.kv_shape[3],
+                                         max_prompt_length=x.max_prompt_length, max_cache_length=x.max_cache_length)
         plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, width, x.group,
                           kernel=2 if blocks else args.kernel, splits=args.splits, ctas=args.ctas, block_lists=blocks,
-                          heads_per_unit=0 if blocks else args.heads_per_unit, tcgen05=args.tcgen05)
+                          heads_per_unit=0 if blocks else args.heads_per_unit, tcgen05=args.tcgen05, **extents)
     B.qsa_reserve_workspace(plan["workspace_bytes"])
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush_w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
@@ -687,7 +689,7 @@ def main():
                        "two buffer sets, with step i+1's upload and step i-1's read-back on their own streams "
                        "overlapping step i's call"}
 
-    kname = {1: "qsa simt_kernel", 2: "qsa mma_kernel", 3: "qsa stream_kernel"}[plan["kernel"]]
+    kname = {1: "qsa simt_kernel", 2: "qsa mma_kernel", 3: "qsa stream_kernel", 4: "qsa rg_kernel"}[plan["kernel"]]
     if latent:
         alg_bytes = x.algorithmic_bytes()
         peak = measured_peaks()

@@ -123,7 +123,21 @@ typedef enum qsa_status {
  * or, when its units (total_q * num_kv_heads / H, H = 4, 2 or 1, the largest
  * that divides num_kv_heads) are under a quarter of the SM count, on the
  * per-(row, kv head) tensor-core kernel with split-K; the rest on the
- * CUDA-core kernel (group 1..8 or 16).  Device pointers must be 16-byte aligned, and
+ * CUDA-core kernel (group 1..8 or 16).
+ *
+ * Prefill-like BF16 calls (head_dim 128, group 4, 8 or 16, a power-of-two
+ * page_size >= 8, on average at least R = 128 / group rows per sequence and
+ * max_cache_length + max_prompt_length <= R * selection_width) run on the
+ * row-group kernel: R consecutive rows of a sequence share one CTA per kv
+ * head, which loads the sequence's pages tile by tile once for all of them
+ * and masks each row to its own positions.  It reads K and V at positions
+ * some row of the group did not select (those scores are masked; those V
+ * rows are zeroed before use), so a non-finite K or V there does not reach
+ * the output.  Its workspace (one bitmap of max_cache_length +
+ * max_prompt_length bits and one flag per row) comes from the same
+ * per-stream workspace as split-K.  Rows that repeat a position, or whose
+ * sequence is longer than the hints say, are served exactly by that
+ * kernel's CUDA-core path.  Device pointers must be 16-byte aligned, and
  * page_stride * element size a multiple of 16 bytes.  kv_blocks may span up
  * to 64 GiB.
  *
@@ -148,7 +162,10 @@ QSA_API qsa_status qsa_sparse_attention_ragged_paged(
 typedef struct qsa_options {
   int32_t kernel;    /* 0 auto, 1 CUDA-core kernel, 2 tensor-core kernel with one
                         CTA per (row, kv head[, split]), 3 persistent stream-K
-                        tensor-core kernel (the default where it applies) */
+                        tensor-core kernel (the default where it applies), 4
+                        row-group kernel (see "Kernel coverage"; only the
+                        entry points that take max_prompt_length and
+                        max_cache_length, and qsa_plan_ex, can run it) */
   int32_t splits;    /* kernel 2: 0 auto, else CTAs per (row, kv head) */
   int32_t ctas;      /* kernel 3: 0 auto (one per SM), else the persistent grid size */
   int32_t block_lists; /* qsa_plan only: nonzero plans a qsa_msa_attention_ragged_paged
@@ -298,13 +315,24 @@ QSA_API qsa_status qsa_compress_keys_paged(
     int32_t rotary_dim, float eps, void* stream);
 
 /* Describes the launch a call with these extents would make, without
- * launching: kernel (1 CUDA-core, 2 tensor-core), CTAs per (row, kv head)
- * along the selection, total CTAs and split-K workspace bytes.  dtype is the
+ * launching: kernel (1 .. 4, as qsa_options.kernel), CTAs per (row, kv head)
+ * along the selection, total CTAs and workspace bytes.  dtype is the
  * q / kv_blocks element type.  Host only; reads no device memory (it queries
- * the current device's SM count and the kernel's occupancy). */
+ * the current device's SM count and the kernel's occupancy).  Without the
+ * batch, page size and length hints it never plans kernel 4: use qsa_plan_ex
+ * for the plan of a qsa_sparse_attention_ragged_paged call. */
 QSA_API qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
                     int64_t selection_width, int32_t group, const qsa_options* options, int32_t* kernel,
                     int32_t* splits, int64_t* ctas, size_t* workspace_bytes);
+
+/* qsa_plan with every host-known extent of a qsa_sparse_attention_ragged_paged
+ * call: batch (cache_lengths' extent, >= 1 when total_q > 0), page_size
+ * (kv_blocks' axis 3, >= 1) and the two length hints as the call passes them.
+ * Its kernel and workspace figure are those of that call. */
+QSA_API qsa_status qsa_plan_ex(int32_t dtype, int64_t total_q, int64_t batch, int64_t num_kv_heads,
+                    int64_t head_dim, int64_t page_size, int64_t selection_width, int32_t group,
+                    uint32_t max_prompt_length, uint32_t max_cache_length, const qsa_options* options,
+                    int32_t* kernel, int32_t* splits, int64_t* ctas, size_t* workspace_bytes);
 
 /* Makes sure the split-K workspace of (current device, stream) holds at least
  * `bytes` bytes (allocating and zeroing it if not).  Blocking; not for the

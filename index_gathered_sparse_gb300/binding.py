@@ -80,6 +80,10 @@ def load_library():
     lib.qsa_plan.argtypes = [i32, i64, i64, i64, i64, i32, ctypes.POINTER(qsa_options), ctypes.POINTER(i32),
                              ctypes.POINTER(i32), ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_size_t)]
     lib.qsa_plan.restype = ctypes.c_int
+    lib.qsa_plan_ex.argtypes = [i32, i64, i64, i64, i64, i64, i64, i32, u32, u32, ctypes.POINTER(qsa_options),
+                                ctypes.POINTER(i32), ctypes.POINTER(i32), ctypes.POINTER(i64),
+                                ctypes.POINTER(ctypes.c_size_t)]
+    lib.qsa_plan_ex.restype = ctypes.c_int
     lib.qsa_reserve_workspace.argtypes = [P, ctypes.c_size_t]
     lib.qsa_reserve_workspace.restype = ctypes.c_int
     lib.qsa_release_device_state.argtypes = []
@@ -266,14 +270,22 @@ def qsa_latent_attention_ragged_paged(output, q, input_row_offsets, swa_blocks, 
 
 def qsa_plan(dtype: int, total_q: int, num_kv_heads: int, head_dim: int, selection_width: int, group: int,
              kernel: int = 0, splits: int = 0, ctas: int = 0, block_lists: bool = False,
-             heads_per_unit: int = 0, tcgen05: int = 0) -> dict:
+             heads_per_unit: int = 0, tcgen05: int = 0, batch=None, page_size=None,
+             max_prompt_length=None, max_cache_length=None) -> dict:
+    """The launch a call with these extents would make.  With batch,
+    page_size and the two length hints (qsa_plan_ex) it is exactly the plan of
+    a qsa_sparse_attention_ragged_paged call with those arguments."""
     lib = load_library()
     k, s = ctypes.c_int32(), ctypes.c_int32()
     c, w = ctypes.c_int64(), ctypes.c_size_t()
     opt = qsa_options(kernel=kernel, splits=splits, ctas=ctas, block_lists=int(bool(block_lists)),
                       heads_per_unit=heads_per_unit, tcgen05=tcgen05)
-    _check(lib.qsa_plan(dtype, total_q, num_kv_heads, head_dim, selection_width, group, ctypes.byref(opt),
-                        ctypes.byref(k), ctypes.byref(s), ctypes.byref(c), ctypes.byref(w)))
+    outs = (ctypes.byref(k), ctypes.byref(s), ctypes.byref(c), ctypes.byref(w))
+    if batch is None:
+        _check(lib.qsa_plan(dtype, total_q, num_kv_heads, head_dim, selection_width, group, ctypes.byref(opt), *outs))
+    else:
+        _check(lib.qsa_plan_ex(dtype, total_q, int(batch), num_kv_heads, head_dim, int(page_size), selection_width,
+                               group, int(max_prompt_length), int(max_cache_length), ctypes.byref(opt), *outs))
     return {"kernel": k.value, "splits": s.value, "ctas": c.value, "workspace_bytes": w.value}
 
 

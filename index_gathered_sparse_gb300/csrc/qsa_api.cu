@@ -67,7 +67,12 @@ struct Resolved {
   int64_t total_q = 0, nq = 0, D = 0, num_pages = 0, L = 0, P = 0, nkv = 0, batch = 0, max_pages = 0, W = 0;
   int64_t pitch = 0;  // elements between pages
   int out_bf16 = 0;
-  int kernel = 0;  // 1 CUDA-core, 2 tensor-core
+  int kernel = 0;  // 1 CUDA-core, 2 per-(row, kv head) tensor-core, 3 persistent stream-K, 4 row groups
+  // max_cache_length + max_prompt_length as the caller passed them (-1: not
+  // given); only kernel 4 depends on them, to size its bitmaps
+  int64_t hint_ctx = -1;
+  int rg_rows = 0, rg_capw = 0, rg_box = 0;  // kernel 4: rows per group, bitmap words per row, slots per copy
+  int64_t rg_groups = 0;                     // kernel 4: most groups the call can have
   int splits = 1;
   int cluster = 0;  // kernel 2: the bands of a unit merge inside one thread-block cluster
   int tiles = 0;    // kernel 2: the variant with tile copies (block lists)
@@ -110,15 +115,52 @@ bool few_stream_units(const Resolved& R, const qsa_options* opt, int32_t group) 
   return sms > 0 && R.total_q * (R.nkv / hpu) * 4 < sms;
 }
 
+// Positions kernel 4's bitmaps cover: the hinted longest sequence rounded up
+// to whole 128-position tiles.
+int64_t rowgroup_positions(const Resolved& R) { return (R.hint_ctx + 127) / 128 * 128; }
+
+// Why kernel 4 cannot run this call (nullptr: it can).  It serves BF16
+// caches with head_dim 128, group 4, 8 or 16 (128 / group rows fill the
+// tensor-core tile), pages of a power-of-two number of slots, at least 8 (a
+// tile copy then starts on a 1024-byte swizzle boundary), and needs the
+// length hints to size its bitmaps (at most kRgMaxCapWords words per row).
+const char* rowgroup_unfit(const Resolved& R, int32_t group) {
+  if (R.hint_ctx < 0)
+    return "kernel 4 needs page_size, max_cache_length and max_prompt_length (this entry point has none; "
+           "qsa_plan_ex takes them)";
+  if (R.elem != qsa::kBF16 || R.D != 128) return "kernel 4 needs BF16 with head_dim 128";
+  if (group != 4 && group != 8 && group != 16) return "kernel 4 needs group 4, 8 or 16";
+  if (R.P < 8 || (R.P & (R.P - 1))) return "kernel 4 needs a power-of-two page_size of at least 8";
+  if (rowgroup_positions(R) / 32 > qsa::kRgMaxCapWords)
+    return "kernel 4 covers sequences of at most 1 Mi positions (max_cache_length + max_prompt_length)";
+  return nullptr;
+}
+
+// Kernel 4 pays when the rows of a sequence are many (prefill) and their
+// sequences short enough that walking every position in tiles costs no more
+// than the rows' own selections: on average at least 128 / group rows per
+// sequence, and a hinted longest sequence of at most (128 / group) x
+// selection_width positions.  Hints of zero read as "not given" (every
+// sequence would then take the kernel's slow exact path).
+bool rowgroup_pays(const Resolved& R, int32_t group) {
+  const int64_t rows = 128 / group;
+  return R.hint_ctx > 0 && R.total_q >= rows * R.batch && R.hint_ctx <= rows * R.W;
+}
+
 // Picks the kernel for a resolved call: for BF16 and FP8 with head_dim 128
 // the persistent tensor-core kernel, or the per-(row, kv head) one when the
-// persistent kernel would get few units; the CUDA-core kernel otherwise (or
-// as forced).
+// persistent kernel would get few units, or the row-group kernel for
+// prefill-like BF16 calls it serves; the CUDA-core kernel otherwise (or as
+// forced).
 qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
   const bool mma_ok = (R.elem == qsa::kBF16 || R.elem == qsa::kE4M3) && R.D == 128;
   const bool simt_ok = group <= 8 || group == 16;
   const int want = opt ? opt->kernel : 0;
-  if (want == 2 || want == 3) {
+  if (want == 4) {
+    const char* why = rowgroup_unfit(R, group);
+    if (why) return fail(QSA_ERR_UNSUPPORTED, why);
+    R.kernel = 4;
+  } else if (want == 2 || want == 3) {
     if (!mma_ok) return fail(QSA_ERR_UNSUPPORTED, "tensor-core kernels need BF16 or F8E4M3 with head_dim 128");
     R.kernel = want;
   } else if (want == 1) {
@@ -127,9 +169,12 @@ qsa_status choose_kernel(Resolved& R, int32_t group, const qsa_options* opt) {
   } else if (want == 0) {
     R.kernel = mma_ok ? 3 : 1;
     if (R.kernel == 3 && few_stream_units(R, opt, group)) R.kernel = 2;
+    if (R.kernel == 3 && !(opt && (opt->ctas > 0 || opt->heads_per_unit != 0 || opt->test_stall)) &&
+        !rowgroup_unfit(R, group) && rowgroup_pays(R, group))
+      R.kernel = 4;
     if (R.kernel == 1 && !simt_ok) return fail(QSA_ERR_UNSUPPORTED, "CUDA-core kernel runs groups 1..8 and 16");
   } else {
-    return fail(QSA_ERR_ARG, "options.kernel must be 0, 1, 2 or 3");
+    return fail(QSA_ERR_ARG, "options.kernel must be 0, 1, 2, 3 or 4");
   }
   if (opt && (opt->splits < 0 || opt->ctas < 0)) return fail(QSA_ERR_ARG, "options.splits and options.ctas must be >= 0");
   if (R.kernel != 2 && opt && opt->splits > 1) return fail(QSA_ERR_UNSUPPORTED, "only kernel 2 takes options.splits");
@@ -244,7 +289,14 @@ qsa_status check_args(const qsa_tensor& output, const qsa_tensor& q, const qsa_t
     return fail(QSA_ERR_UNSUPPORTED, "an extent exceeds 2^31 - 1");
   if (R.nq * R.D * R.total_q > ((int64_t)1 << 40)) return fail(QSA_ERR_UNSUPPORTED, "q larger than 2^40 elements");
 
-  return choose_kernel(R, group, opt);
+  const qsa_status s = choose_kernel(R, group, opt);
+  if (s == QSA_OK && R.kernel == 4 && R.num_pages == 0) {
+    // kernel 4 copies whole pages: with no page at all, every position is bad
+    // and kernel 3 reports them
+    if (opt && opt->kernel == 4) return fail(QSA_ERR_UNSUPPORTED, "kernel 4 needs a cache of at least one page");
+    R.kernel = 3;
+  }
+  return s;
 }
 
 // Split-K scratch of one (device, stream): f32 partials (contents never need
@@ -318,6 +370,21 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   }
   R.splits = 1;
   R.band = qsa::kMmaTile;
+  if (R.kernel == 4) {
+    // Row groups: 128 / group rows of a sequence per CTA and kv head; the
+    // sequences' groups number at most ceil(total_q / rows) + batch.  The
+    // workspace holds each row's bitmap and its flags.
+    R.rg_rows = 128 / group;
+    R.rg_capw = (int)(rowgroup_positions(R) / 32);
+    R.rg_box = (int)std::min<int64_t>(R.P, 128);
+    R.rg_groups = (R.total_q + R.rg_rows - 1) / R.rg_rows + std::min(R.batch, R.total_q);
+    R.ctas = R.rg_groups * R.nkv;
+    if (R.ctas > 0x7FFFFFFF) return fail(QSA_ERR_UNSUPPORTED, "kernel 4: more than 2^31 - 1 CTAs");
+    R.ws_partial_bytes = ((size_t)R.total_q * R.rg_capw * 4 + 255) / 256 * 256 + ((size_t)R.total_q * 4 + 255) / 256 * 256;
+    R.ws_tickets = 0;
+    R.ws_bytes = R.ws_partial_bytes;
+    return QSA_OK;
+  }
   if (R.kernel == 1) {
     R.ctas = R.total_q * R.nkv;
     R.ws_bytes = R.ws_partial_bytes = 0;
@@ -529,18 +596,19 @@ TensorMapEncode tensor_map_encoder() {
 // with qsa::Params::tmap (p.tma = 1), or leaves p.tma = 0 when a tile copy
 // cannot describe the layout (pages shorter than a tile, strides that are
 // not multiples of 16 bytes, ...): every tile then takes 16-byte copies.
-void encode_tile_map(Params& p, const void* kv, int elem, int64_t num_pages) {
+// Kernel 4 asks for boxes of min(page_size, 128) slots and needs the map.
+void encode_tile_map(Params& p, const void* kv, int elem, int64_t num_pages, int box_slots = qsa::kMmaTile) {
   p.tma = 0;
   const TensorMapEncode encode = tensor_map_encoder();
   const int64_t plane = (int64_t)p.P * p.slot_bytes;
-  if (!encode || elem == qsa::kF32 || p.P < qsa::kMmaTile || p.slot_bytes <= 0 || p.slot_bytes % 128 != 0 ||
+  if (!encode || elem == qsa::kF32 || p.P < box_slots || p.slot_bytes <= 0 || p.slot_bytes % 128 != 0 ||
       p.k_layer_bytes % plane != 0 || p.v_minus_k_bytes % plane != 0 || p.page_pitch_bytes % 16 != 0 ||
       (reinterpret_cast<uintptr_t>(kv) & 15u) != 0 || num_pages <= 0 || num_pages > 0xFFFFFFFFll)
     return;
   const cuuint64_t dims[5] = {elem == qsa::kBF16 ? 64u : 128u, (cuuint64_t)(p.slot_bytes / 128), (cuuint64_t)p.P,
                               (cuuint64_t)(2 * (p.v_minus_k_bytes / plane)), (cuuint64_t)num_pages};
   const cuuint64_t strides[4] = {128u, (cuuint64_t)p.slot_bytes, (cuuint64_t)plane, (cuuint64_t)p.page_pitch_bytes};
-  const cuuint32_t box[5] = {(cuuint32_t)dims[0], 1u, (cuuint32_t)qsa::kMmaTile, 1u, 1u};
+  const cuuint32_t box[5] = {(cuuint32_t)dims[0], 1u, (cuuint32_t)box_slots, 1u, 1u};
   const cuuint32_t estride[5] = {1u, 1u, 1u, 1u, 1u};
   const CUresult r = encode(&p.tmap, elem == qsa::kBF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8, 5,
                             const_cast<void*>(kv), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -662,8 +730,22 @@ qsa_status launch_planned(Resolved& R, const qsa_tensor& output, const qsa_tenso
     p.shallow = !R.umma && R.elem == qsa::kBF16 && sms > 0 && R.ctas >= 8 * (int64_t)sms ? 1 : 0;
   }
 
+  if (R.kernel == 4) {
+    p.rg_bits = reinterpret_cast<uint32_t*>(p.ws_partial);
+    p.rg_flags = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(p.ws_partial) +
+                                            ((size_t)R.total_q * R.rg_capw * 4 + 255) / 256 * 256);
+    p.rg_rows = R.rg_rows;
+    p.rg_capw = R.rg_capw;
+    p.rg_box = R.rg_box;
+    p.rg_groups = (int32_t)R.rg_groups;
+    encode_tile_map(p, kv_blocks.data, R.elem, R.num_pages, R.rg_box);
+    if (!p.tma) return fail(QSA_ERR_CUDA, "kernel 4: the cache's TMA tensor map could not be encoded");
+  }
+
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (R.kernel == 1)
+  if (R.kernel == 4)
+    e = qsa::launch_rowgroup(p, st);
+  else if (R.kernel == 1)
     e = qsa::launch_simt(p, R.elem, st);
   else if (R.kernel == 2)
     e = R.elem == qsa::kBF16 ? qsa::launch_mma_bf16(p, st) : qsa::launch_mma_e4m3(p, st);
@@ -683,9 +765,11 @@ qsa_status qsa_sparse_attention_ragged_paged_ex(qsa_tensor output, qsa_tensor q,
                                                 uint32_t max_cache_length, uint32_t layer_idx,
                                                 qsa_tensor token_indices, qsa_tensor counts, float scale,
                                                 int32_t group, void* stream, const qsa_options* options) {
-  (void)max_prompt_length;  // launch-sizing hints only: the plan uses host-known extents
-  (void)max_cache_length;
+  // Launch-sizing hints: kernel 4 sizes its bitmaps from them (a sequence
+  // longer than they say is still served exactly, by that kernel's CUDA-core
+  // path); the other kernels use host-known extents only.
   Resolved R;
+  R.hint_ctx = (int64_t)max_cache_length + (int64_t)max_prompt_length;
   qsa_status s = check_args(output, q, input_row_offsets, kv_blocks, page_stride, cache_lengths, kv_lookup_table,
                             layer_idx, token_indices, counts, group, options, R);
   if (s != QSA_OK) return s;
@@ -982,22 +1066,32 @@ qsa_status qsa_compress_keys_paged(qsa_tensor block_keys, qsa_tensor gamma, qsa_
   return QSA_OK;
 }
 
-qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
-                    int64_t selection_width, int32_t group, const qsa_options* options, int32_t* kernel,
-                    int32_t* splits, int64_t* ctas, size_t* workspace_bytes) {
+}  // extern "C"
+
+namespace {
+
+// qsa_plan and qsa_plan_ex: the plan of a call with these extents (batch 0,
+// page_size 0 and hint_ctx -1 when the caller does not give them).
+qsa_status plan_extents(int32_t dtype, int64_t total_q, int64_t batch, int64_t num_kv_heads, int64_t head_dim,
+                        int64_t page_size, int64_t selection_width, int32_t group, int64_t hint_ctx,
+                        const qsa_options* options, int32_t* kernel, int32_t* splits, int64_t* ctas,
+                        size_t* workspace_bytes) {
   Resolved R;
   if (dtype != QSA_F32 && dtype != QSA_BF16 && dtype != QSA_F8E4M3)
     return fail(QSA_ERR_DTYPE, "dtype must be F32, BF16 or F8E4M3");
-  if (total_q < 0 || num_kv_heads < 1 || selection_width < 0 || group < 1)
+  if (total_q < 0 || num_kv_heads < 1 || selection_width < 0 || group < 1 || batch < 0 || page_size < 0)
     return fail(QSA_ERR_SHAPE, "negative or empty extent");
   if (head_dim != 64 && head_dim != 128) return fail(QSA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (group > 16) return fail(QSA_ERR_UNSUPPORTED, "group must be <= 16");
   if (options && options->splits < 0) return fail(QSA_ERR_ARG, "options.splits must be >= 0");
   R.elem = dtype == QSA_F32 ? qsa::kF32 : dtype == QSA_BF16 ? qsa::kBF16 : qsa::kE4M3;
   R.total_q = total_q;
+  R.batch = batch;
   R.nkv = num_kv_heads;
   R.D = head_dim;
+  R.P = page_size;
   R.W = selection_width;
+  R.hint_ctx = hint_ctx;
   qsa_status s = choose_kernel(R, group, options);
   if (s != QSA_OK) return s;
   int dev = 0;
@@ -1011,6 +1105,28 @@ qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_
   if (ctas) *ctas = R.ctas;
   if (workspace_bytes) *workspace_bytes = R.ws_bytes;
   return QSA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+qsa_status qsa_plan(int32_t dtype, int64_t total_q, int64_t num_kv_heads, int64_t head_dim,
+                    int64_t selection_width, int32_t group, const qsa_options* options, int32_t* kernel,
+                    int32_t* splits, int64_t* ctas, size_t* workspace_bytes) {
+  return plan_extents(dtype, total_q, 0, num_kv_heads, head_dim, 0, selection_width, group, -1, options, kernel,
+                      splits, ctas, workspace_bytes);
+}
+
+qsa_status qsa_plan_ex(int32_t dtype, int64_t total_q, int64_t batch, int64_t num_kv_heads, int64_t head_dim,
+                       int64_t page_size, int64_t selection_width, int32_t group, uint32_t max_prompt_length,
+                       uint32_t max_cache_length, const qsa_options* options, int32_t* kernel, int32_t* splits,
+                       int64_t* ctas, size_t* workspace_bytes) {
+  if (total_q > 0 && batch < 1) return fail(QSA_ERR_SHAPE, "query rows without any sequence (batch == 0)");
+  if (page_size < 1) return fail(QSA_ERR_SHAPE, "page_size must be >= 1");
+  return plan_extents(dtype, total_q, batch, num_kv_heads, head_dim, page_size, selection_width, group,
+                      (int64_t)max_cache_length + (int64_t)max_prompt_length, options, kernel, splits, ctas,
+                      workspace_bytes);
 }
 
 qsa_status qsa_reserve_workspace(void* stream, size_t bytes) {

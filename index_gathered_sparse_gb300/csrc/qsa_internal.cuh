@@ -71,8 +71,23 @@ struct Params {
   int32_t groups;   // latent mode, one band, group 16: a CTA serves four head groups (nkv = groups / 4)
   int32_t stall;    // kernel 3, tests only: producers issue no K/V copies and waits give up early
   int32_t umma;     // kernel 2: the tcgen05 consumer (BF16, tile-copy layout; tile copies where tma)
+  // Kernel 4 (row groups over page tiles): a bitmap of each row's selected
+  // positions (bit pos % 32 of word pos / 32), written by its first kernel,
+  // and per-row flags (kRgDup, kRgOverflow).  tmap then holds a box of
+  // rg_box slots (min(page_size, 128)) instead of kernel 2's 64.
+  uint32_t* rg_bits;  // [total_q, rg_capw]
+  int32_t* rg_flags;  // [total_q]
+  int32_t rg_rows;    // query rows per group: 128 / group
+  int32_t rg_capw;    // bitmap words per row (the positions the bitmaps cover / 32)
+  int32_t rg_box;     // slots per tile copy
+  int32_t rg_groups;  // most groups the call can have (grid size / num_kv_heads)
   CUtensorMap tmap;
 };
+
+// Kernel 4's row flags: the row repeats a position, or its sequence has more
+// positions than the bitmaps cover.  A group with a flagged row takes the
+// kernel's exact CUDA-core path.
+constexpr int32_t kRgDup = 1, kRgOverflow = 2;
 
 // Launch plan of the persistent stream-K kernel (computed on the host).
 struct StreamPlan {
@@ -119,6 +134,10 @@ struct CompressParams {
 cudaError_t launch_compress(const CompressParams& p, int elem, int freq_elem, int head_dim, cudaStream_t stream);
 
 cudaError_t launch_stream_bf16(const Params& p, const StreamPlan& sp, cudaStream_t stream);
+// Kernel 4: the bitmap kernel, then the row-group kernel (BF16, head_dim 128).
+cudaError_t launch_rowgroup(const Params& p, cudaStream_t stream);
+// Shared memory of kernel 4's bitmap kernel for rg_capw words per row.
+constexpr int kRgMaxCapWords = 32768;  // 1 Mi positions, 128 KB
 cudaError_t launch_stream_e4m3(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_bf16_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);
 cudaError_t launch_stream_e4m3_scan(const Params& p, const StreamPlan& sp, cudaStream_t stream);

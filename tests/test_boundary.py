@@ -147,8 +147,34 @@ def test_launch_option_limits(lib):
         (B.qsa_options(kernel=2, tcgen05=2), {}, 5),          # -1, 0 or 1
         (B.qsa_options(kernel=3, tcgen05=1), {}, 4),          # only kernel 2 has the tcgen05 consumer
         (B.qsa_options(kernel=2, tcgen05=1), e4m3, 4),        # which reads BF16 caches
+        # the row-group kernel: BF16, head_dim 128, group 4, 8 or 16, a power-of-two page of >= 8 slots,
+        # bitmaps of at most 1 Mi positions; none of the other kernels' controls
+        (B.qsa_options(kernel=4), e4m3, 4),
+        (B.qsa_options(kernel=4), dict(q=_t((5, 4, 128), B.QSA_BF16), output=_t((5, 4, 128), B.QSA_BF16), group=2), 4),
+        (B.qsa_options(kernel=4), dict(kv_blocks=_t((10, 2, 3, 12, 2, 128), B.QSA_BF16)), 4),
+        (B.qsa_options(kernel=4), dict(kv_blocks=_t((10, 2, 3, 4, 2, 128), B.QSA_BF16)), 4),
+        (B.qsa_options(kernel=4), dict(max_cache_length=(1 << 20)), 4),
+        (B.qsa_options(kernel=4, splits=2), {}, 4),
+        (B.qsa_options(kernel=4, ctas=3), {}, 4),
+        (B.qsa_options(kernel=4, heads_per_unit=2), {}, 4),
+        (B.qsa_options(kernel=4, tcgen05=1), {}, 4),
+        (B.qsa_options(kernel=5), {}, 5),
     ]
     for opt, over, code in cases:
         st = ex(opt, **over)
         assert st == code, (opt.kernel, opt.heads_per_unit, opt.test_stall, opt.tcgen05, B.STATUS_NAMES.get(st),
                             lib.qsa_last_error_message())
+
+
+def test_plan_without_extents_never_plans_the_row_group_kernel(lib):
+    """qsa_plan has no page size or length hints: forcing kernel 4 there is
+    refused before any CUDA call; qsa_plan_ex checks its extra extents."""
+    opt = B.qsa_options(kernel=4)
+    k, s = ctypes.c_int32(), ctypes.c_int32()
+    c, w = ctypes.c_int64(), ctypes.c_size_t()
+    outs = (ctypes.byref(k), ctypes.byref(s), ctypes.byref(c), ctypes.byref(w))
+    assert lib.qsa_plan(B.QSA_BF16, 64, 8, 128, 256, 8, ctypes.byref(opt), *outs) == 4
+    assert b"qsa_plan_ex" in lib.qsa_last_error_message()
+    assert lib.qsa_plan_ex(B.QSA_BF16, 64, 0, 8, 128, 64, 256, 8, 16, 100, ctypes.byref(opt), *outs) == 2  # no batch
+    assert lib.qsa_plan_ex(B.QSA_BF16, 64, 2, 8, 128, 0, 256, 8, 16, 100, ctypes.byref(opt), *outs) == 2  # no page
+    assert lib.qsa_plan_ex(B.QSA_BF16, 64, 2, 8, 128, 48, 256, 8, 16, 100, ctypes.byref(opt), *outs) == 4

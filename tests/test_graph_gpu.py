@@ -4,8 +4,9 @@ workspace of the capturing stream is reserved (qsa_plan's figure) and one
 warm-up call has run on it, a call captured with torch.cuda.graph and
 replayed writes the same output bits as a direct call.  Cases cover each launch form: the persistent
 kernel, kernel 2 with bands merged inside a thread-block cluster
-(cudaLaunchKernelEx) and through the workspace tickets, and block lists
-with tile copies (a tensor map encoded on the host at capture time).
+(cudaLaunchKernelEx) and through the workspace tickets, block lists
+with tile copies (a tensor map encoded on the host at capture time), and
+the row-group kernel (two launches; its bitmaps in the workspace).
 """
 import numpy as np
 import pytest
@@ -32,6 +33,7 @@ CASES = {
     "cluster_bands": ("bf16_long_decode_small", dict(kernel=2, splits=6)),
     "ticket_bands": ("bf16_long_decode_small", dict(kernel=2, splits=12)),
     "block_tiles": ("msa_bf16_decode_small", dict(splits=3)),
+    "row_groups": ("bf16_prefill_small", dict(kernel=4)),
 }
 
 
@@ -58,7 +60,9 @@ def test_graph_replay_matches_direct_call(case):
                           kernel=2, splits=kw.get("splits", 0), block_lists=True)
     else:
         plan = B.qsa_plan(code, x.total_q, x.num_kv_heads, x.head_dim, x.selection_width, x.group,
-                          kernel=kw.get("kernel", 0), splits=kw.get("splits", 0))
+                          kernel=kw.get("kernel", 0), splits=kw.get("splits", 0), batch=x.batch,
+                          page_size=x.kv_shape[3], max_prompt_length=x.max_prompt_length,
+                          max_cache_length=x.max_cache_length)
     B.qsa_reserve_workspace(plan["workspace_bytes"], stream=s.cuda_stream)
     with torch.cuda.stream(s):
         fn(**d, **kw)  # warm-up on the capturing stream (status word, kernel attributes)
