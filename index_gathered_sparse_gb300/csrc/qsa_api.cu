@@ -139,8 +139,8 @@ const char* rowgroup_unfit(const Resolved& R, int32_t group) {
 // Kernel 4 pays when the rows of a sequence are many (prefill) and their
 // sequences short enough that walking every position in tiles costs no more
 // than the rows' own selections: on average at least 128 / group rows per
-// sequence, and a hinted longest sequence of at most (128 / group) x
-// selection_width positions.  Hints of zero read as "not given" (every
+// sequence (half the rows of one of its CTAs), and a hinted longest sequence
+// of at most (128 / group) x selection_width positions.  Hints of zero read as "not given" (every
 // sequence would then take the kernel's slow exact path).
 bool rowgroup_pays(const Resolved& R, int32_t group) {
   const int64_t rows = 128 / group;
@@ -371,10 +371,11 @@ qsa_status plan_launch(Resolved& R, int32_t group, const qsa_options* opt, int d
   R.splits = 1;
   R.band = qsa::kMmaTile;
   if (R.kernel == 4) {
-    // Row groups: 128 / group rows of a sequence per CTA and kv head; the
-    // sequences' groups number at most ceil(total_q / rows) + batch.  The
-    // workspace holds each row's bitmap and its flags.
-    R.rg_rows = 128 / group;
+    // Row groups: 256 / group rows of a sequence per CTA and kv head (two
+    // 128-row tensor-core tiles); the sequences' groups number at most
+    // ceil(total_q / rows) + batch.  The workspace holds each row's bitmap and
+    // its flags.
+    R.rg_rows = 256 / group;
     R.rg_capw = (int)(rowgroup_positions(R) / 32);
     R.rg_box = (int)std::min<int64_t>(R.P, 128);
     R.rg_groups = (R.total_q + R.rg_rows - 1) / R.rg_rows + std::min(R.batch, R.total_q);

@@ -5,13 +5,13 @@
 // page ("Gather-GQA over the token indices a QSA selection names"): for each
 // query row, kv head and query head of its group, softmax(scale q.K_sel) V_sel
 // over exactly the positions the row lists.  Rows of one prefill sequence list
-// heavily overlapping positions, so this kernel serves R = 128 / group
+// heavily overlapping positions, so this kernel serves R = 256 / group
 // consecutive rows of a sequence together: their R x group query heads of one
-// kv head are the 128 rows of a tensor-core tile, and the kernel walks the
-// sequence's positions in tiles of 128 (whole pages, loaded once by TMA),
-// skipping tiles no row of the group selects.  Scores of keys a row did not
-// list are masked out before the softmax, so every row still attends exactly
-// its own positions:
+// kv head are the rows of two 128-row tensor-core tiles, and the kernel walks
+// the sequence's positions in tiles of 128 keys (whole pages, loaded once by
+// TMA for both), skipping tiles no row of the group selects.  Scores of keys
+// a row did not list are masked out before the softmax, so every row still
+// attends exactly its own positions:
 //
 //   S = Q . K^T    (M = 128 query heads x rows, N = 128 keys, K = 128 channels)
 //   P = 2^(scale log2(e) S - m) on the row's own keys, 0 elsewhere
@@ -25,50 +25,61 @@
 // a repeated index is its own softmax term, which a bitmap cannot count, so a
 // group with such a row takes an exact CUDA-core path instead.
 //
-// CTA = (group of rows, kv head); 6 warps:
+// CTA = (group of rows, kv head): R = 256 / group rows, whose 256 query
+// heads form two 128-row accumulator tiles A (the first R / 2 rows) and B
+// sharing every K/V tile.  10 warps:
 //   warp 0      producer: the group's mask words of each tile from the bitmaps,
 //               empty tiles skipped, page-table lookups, TMA tile copies of K
 //               and V (page 0 stands in for pages past the sequence or named
-//               by no page: none of their keys is selected), three stages
-//   warp 1      one thread issues the MMAs: S(i) = Q.K(i)^T, then O += P(i-1).V(i-1)
-//   warps 2..5  softmax of the 128 accumulator rows (one thread per row), with
-//               a lazy running maximum: O is rescaled only when a row's maximum
-//               grows by more than 2^8; they also zero the V rows of keys no
-//               row of the group selects (so 0 x non-finite never reaches O)
-//               and write the output.
-// Tensor memory: S double-buffered (2 x 128 columns), O (128), P
-// double-buffered (2 x 64 columns of packed bf16 pairs) = 512 columns.
+//               by no page: none of their keys is selected), two stages with
+//               separate K and V arrivals; once a tile's V has landed it zeroes
+//               the V rows of keys no row of the group selects (so
+//               0 x non-finite never reaches O) before P.V may read them
+//   warp 1      one thread issues the MMAs in the order
+//               QK_A(i) QK_B(i) PV_A(i) QK_A(i+1) PV_B(i) QK_B(i+1) ...,
+//               so each softmax warpgroup works while the tensor cores serve
+//               the other tile
+//   warps 2..5  softmax of tile A (one thread per accumulator row), warps
+//   6..9        of tile B: a lazy running maximum (O is rescaled only when a
+//               row's maximum grows by more than 2^8), one read of S per
+//               tile, P written back over the scores it replaces (keys 2j,
+//               2j + 1 in column j), and the output.
+// Tensor memory: S_A, S_B (128 columns each, P_A / P_B in their first 64
+// columns as packed bf16 pairs), O_A, O_B (128 each) = 512 columns.  P_X(i)
+// overwrites S_X(i) after it is read, and QK_X(i+1) overwrites P_X(i) only
+// after PV_X(i), issued before it by the same thread (tensor-core operations
+// of one thread execute in issue order).
 #include "qsa_mma.cuh"
 
 namespace qsa {
 namespace {
 
-constexpr int kRgThreads = 192;
-constexpr int kRgStages = 3;
+constexpr int kRgThreads = 320;
+constexpr int kRgStages = 2;
 constexpr uint32_t kRgHalf = 16384;           // 64 channels (128 B) x 128 rows, 128-byte swizzle
-constexpr uint32_t kRgTileBytes = 2 * kRgHalf;  // Q, or one K or V tile
+constexpr uint32_t kRgTileBytes = 2 * kRgHalf;  // a Q tile, or one K or V tile
 constexpr uint32_t kRgStageBytes = 2 * kRgTileBytes;
-constexpr uint32_t kRgStageOff = kRgTileBytes;  // after Q
+constexpr uint32_t kRgStageOff = 2 * kRgTileBytes;  // after Q_A, Q_B
 
 struct TileHdr {
   int32_t pos0;          // first position of the tile
   int32_t end;           // 1: the unit has no more tiles
   int32_t pad[2];
   uint32_t any[4];       // keys some row of the group selects
-  uint32_t mask[32][4];  // per row of the group: the keys it selects
+  uint32_t mask[64][4];  // per row of the group (at most 64): the keys it selects
 };
 constexpr uint32_t kRgHdrOff = kRgStageOff + kRgStages * kRgStageBytes;
 constexpr uint32_t kRgBarOff = kRgHdrOff + kRgStages * (uint32_t)sizeof(TileHdr);
-// barriers: full[3], done[3], s_full[2], p_full[2], q_full -> 11 x 8 B, then misc words
-constexpr int kBarFull = 0, kBarDone = 3, kBarS = 6, kBarP = 8, kBarQ = 10;
+// barriers: full_k[2], full_v[2], kv_free[2], s_full[2], p_full[2], o_done[2], q_full, v_ready[2] -> 15 x 8 B
+constexpr int kBarK = 0, kBarV = 2, kBarFree = 4, kBarS = 6, kBarP = 8, kBarO = 10, kBarQ = 12, kBarVR = 13;
 constexpr uint32_t kRgMiscOff = kRgBarOff + 128;
 constexpr uint32_t kRgSmemBytes = kRgMiscOff + 32 * 4;
 constexpr uint32_t kRgSmemAlloc = kRgSmemBytes + 1024;  // the 1024-byte alignment of the swizzled tiles
 static_assert(kRgSmemAlloc <= 232448, "kernel 4's shared memory exceeds the per-CTA limit");
 static_assert(sizeof(TileHdr) % 16 == 0, "tile headers must stay 16-byte aligned");
 
-// TMEM columns
-constexpr uint32_t kColS = 0, kColO = 256, kColP = 384;
+// TMEM columns of tile X (0 = A, 1 = B)
+constexpr uint32_t kColS = 0, kColO = 256;
 
 // S = Q.K^T: A (Q) and B (K) K-major; O = P.V: A (P) in tensor memory, B (V) MN-major.
 constexpr uint32_t kIdescQK = instr_desc(128, 128, 1, 0, 0);
@@ -171,26 +182,29 @@ __global__ void __launch_bounds__(256) rg_bitmap_kernel(const Params p) {
   if (threadIdx.x == 0) p.rg_flags[r] = dup ? kRgDup : 0;
 }
 
-// The exact path of a group with a flagged row: warp w serves rows w, w + 6,
-// ... of the group, its `group` query heads on kv head h, walking the row's
-// list in order (repeats included) with an online softmax per head; lane l
-// holds channels 4l .. 4l + 3.
+// The exact path of a group with a flagged row: the warps take (row, up to 8
+// query heads on kv head h) items in turn, walking the row's list in order
+// (repeats included) with an online softmax per head; lane l holds channels
+// 4l .. 4l + 3.
 __device__ void rg_exact(const Params& p, const GroupInfo& gr, int h) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int G = p.group;
-  for (int rl = warp; rl < gr.nrows; rl += nw) {
+  // (row, chunk of up to 8 query heads) items, one per warp at a time
+  const int chunks = (G + 7) / 8;
+  for (int item = warp; item < gr.nrows * chunks; item += nw) {
+    const int rl = item / chunks, h0 = (item % chunks) * 8, hn = min(8, G - h0);
     const int r = gr.row0 + rl;
     const int n = min(max(__ldg(p.counts + r), 0), p.W);
-    float qv[16][4], acc[16][4], m[16], l[16];
+    float qv[8][4], acc[8][4], m[8], l[8];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < 8; ++i) {
       m[i] = -CUDART_INF_F;
       l[i] = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) qv[i][c] = acc[i][c] = 0.f;
-      if (i < G) {
-        const __nv_bfloat16* qp =
-            reinterpret_cast<const __nv_bfloat16*>(p.q) + ((int64_t)r * p.nq + (int64_t)h * G + i) * 128 + 4 * lane;
+      if (i < hn) {
+        const __nv_bfloat16* qp = reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                  ((int64_t)r * p.nq + (int64_t)h * G + h0 + i) * 128 + 4 * lane;
 #pragma unroll
         for (int c = 0; c < 4; ++c) qv[i][c] = __bfloat162float(qp[c]);
       }
@@ -217,8 +231,8 @@ __device__ void rg_exact(const Params& p, const GroupInfo& gr, int h) {
         vf[0] = __low2float(v01); vf[1] = __high2float(v01); vf[2] = __low2float(v23); vf[3] = __high2float(v23);
       }
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        if (i >= G) break;
+      for (int i = 0; i < 8; ++i) {
+        if (i >= hn) break;
         float d = qv[i][0] * kf[0] + qv[i][1] * kf[1] + qv[i][2] * kf[2] + qv[i][3] * kf[3];
 #pragma unroll
         for (int o = 16; o; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
@@ -234,10 +248,10 @@ __device__ void rg_exact(const Params& p, const GroupInfo& gr, int h) {
     }
     if (bad && lane == 0) atomicOr(p.status, bad);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      if (i >= G) break;
+    for (int i = 0; i < 8; ++i) {
+      if (i >= hn) break;
       const float inv = l[i] > 0.f ? 1.f / l[i] : 0.f;
-      const int64_t o = ((int64_t)r * p.nq + (int64_t)h * G + i) * 128 + 4 * lane;
+      const int64_t o = ((int64_t)r * p.nq + (int64_t)h * G + h0 + i) * 128 + 4 * lane;
 #pragma unroll
       for (int c = 0; c < 4; ++c) store_out(p, o + c, acc[i][c] * inv);
     }
@@ -255,6 +269,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&x);
 }
 
+// 320 threads, one CTA per SM (its shared memory).  Ten warps put three on
+// two of the SM's four sub-partitions, whose register files hold 16 Ki
+// registers each: at most 168 registers a thread.
 __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -262,7 +279,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
   const int R = p.rg_rows, G = p.group;
   const int h = (int)(blockIdx.x % (uint32_t)p.nkv), gi = (int)(blockIdx.x / (uint32_t)p.nkv);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kRgBarOff);
-  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kRgMiscOff);  // [0] tmem base, [8..] scratch
+  uint32_t* misc = reinterpret_cast<uint32_t*>(smem + kRgMiscOff);  // [0] tmem base, [1] abort, [8..] scratch
   TileHdr* hdr = reinterpret_cast<TileHdr*>(smem + kRgHdrOff);
   const uint32_t sQ = smem_addr(smem), sStage = sQ + kRgStageOff;
   auto bar = [&](int k) { return smem_addr(&bars[k]); };
@@ -277,15 +294,16 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
   }
 
   if (tid == 0) {
-    for (int k = 0; k < 3; ++k) {
-      mbar_init(bar(kBarFull + k), 1);
-      mbar_init(bar(kBarDone + k), 1);
-    }
     for (int k = 0; k < 2; ++k) {
+      mbar_init(bar(kBarK + k), 1);
+      mbar_init(bar(kBarV + k), 1);
+      mbar_init(bar(kBarFree + k), 1);
       mbar_init(bar(kBarS + k), 1);
       mbar_init(bar(kBarP + k), 128);
+      mbar_init(bar(kBarO + k), 1);
+      mbar_init(bar(kBarVR + k), 1);
     }
-    mbar_init(bar(kBarQ), 128);
+    mbar_init(bar(kBarQ), 256);
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 1) {
@@ -308,30 +326,60 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
     // ---------------------------------------------------------------- producer
     const int NT = (int)((gr.kv_len + 127) >> 7);
     const int words_valid = (int)((gr.kv_len + 31) >> 5);  // bitmap words the first kernel wrote
-    const int nw = R * 4;
+    const int nw = R * 4;                                    // mask words of a tile (at most 256)
     const uint32_t* bits = p.rg_bits + (int64_t)gr.row0 * p.rg_capw;
     const int BR = p.rg_box;  // slots per copy: min(P, 128)
     const int np = 128 / BR;  // copies per line of a tile
-    auto load_words = [&](int t, uint32_t (&wv)[4]) {
+    auto load_words = [&](int t, uint32_t (&wv)[8]) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const int w = lane + 32 * k, row = w >> 2, wi = t * 4 + (w & 3);
         wv[k] = 0u;
         if (w < nw && row < gr.nrows && wi < words_valid) wv[k] = __ldg(bits + (int64_t)row * p.rg_capw + wi);
       }
     };
-    uint32_t nxt[4] = {0u, 0u, 0u, 0u};
+    uint32_t nxt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
     if (NT > 0) load_words(0, nxt);
     int i = 0;
     bool ok = true;
-    for (int t = 0; t < NT && ok; ++t) {
-      uint32_t cur[4];
+    // Tile j's V has landed: zero the rows of keys no row of the group selects
+    // (lane l: keys l, l + 32, l + 64, l + 96), then let P.V read it.
+    auto finish_v = [&](int j) -> bool {
+      const int sj = j % kRgStages;
+      if (!warp_wait(bar(kBarV + sj), (uint32_t)((j / kRgStages) & 1))) return false;
+      const uint32_t vt = sStage + (uint32_t)sj * kRgStageBytes + kRgTileBytes;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int k = lane + 32 * c;
+        if ((hdr[sj].any[c] >> lane) & 1u) continue;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) cur[k] = nxt[k];
+        for (int x2 = 0; x2 < 2; ++x2)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + x2 * kRgHalf + (uint32_t)k * 128 + q * 16),
+                         "r"(0u)
+                         : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarVR + sj));
+      return true;
+    };
+    for (int t = 0; t < NT && ok; ++t) {
+      uint32_t cur[8], o = 0u;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        cur[k] = nxt[k];
+        o |= cur[k];
+      }
       if (t + 1 < NT) load_words(t + 1, nxt);
-      if (!__any_sync(0xffffffffu, (cur[0] | cur[1] | cur[2] | cur[3]) != 0u)) continue;
+      if (!__any_sync(0xffffffffu, o != 0u)) continue;
+      if (i > 0 && !finish_v(i - 1)) {
+        ok = false;
+        break;
+      }
       const int s = i % kRgStages;
-      if (i >= kRgStages && !warp_wait(bar(kBarDone + s), (uint32_t)((i / kRgStages - 1) & 1))) {
+      if (i >= kRgStages && !warp_wait(bar(kBarFree + s), (uint32_t)((i / kRgStages - 1) & 1))) {
         ok = false;
         break;
       }
@@ -366,7 +414,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         }
         bool had = false;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
           had |= (cur[k] & kill) != 0u;
           cur[k] &= ~kill;
         }
@@ -375,7 +423,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
       TileHdr& th = hdr[s];
       uint32_t any = 0u;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const int w = lane + 32 * k;
         if (w < nw) th.mask[w >> 2][w & 3] = cur[k];
         any |= cur[k];
@@ -389,85 +437,113 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         th.end = 0;
       }
       __syncwarp();
-      const uint32_t fb = bar(kBarFull + s);
+      const uint32_t kb = bar(kBarK + s), vb = bar(kBarV + s);
       if (lane == 0) {
         tile_fence_proxy_async();
-        mbar_arrive_expect_tx(fb, 2 * kRgTileBytes);
+        mbar_arrive_expect_tx(kb, kRgTileBytes);
+        mbar_arrive_expect_tx(vb, kRgTileBytes);
       }
       __syncwarp();
       if (lane < np) {
         const uint32_t dst = sStage + (uint32_t)s * kRgStageBytes + (uint32_t)(BR < 128 ? lane * BR * 128 : 0);
         const int slot = BR < 128 ? 0 : (int)(pos0 % p.P);
 #pragma unroll
-        for (int kv = 0; kv < 2; ++kv)
+        for (int x = 0; x < 2; ++x)
+          tma_load_5d(dst + x * kRgHalf, &p.tmap, 0, h * 2 + x, slot, p.tma_plane_k, phys, kb);
 #pragma unroll
-          for (int x = 0; x < 2; ++x)
-            tma_load_5d(dst + kv * kRgTileBytes + x * kRgHalf, &p.tmap, 0, h * 2 + x, slot,
-                        kv ? p.tma_plane_v : p.tma_plane_k, phys, fb);
+        for (int x = 0; x < 2; ++x)
+          tma_load_5d(dst + kRgTileBytes + x * kRgHalf, &p.tmap, 0, h * 2 + x, slot, p.tma_plane_v, phys, vb);
       }
       ++i;
     }
+    if (ok && i > 0 && !finish_v(i - 1)) ok = false;
     if (ok) {
-      // end of the unit
+      // end of the unit: a header with no copies, on the K barrier
       const int s = i % kRgStages;
-      if (i >= kRgStages && !warp_wait(bar(kBarDone + s), (uint32_t)((i / kRgStages - 1) & 1))) ok = false;
+      if (i >= kRgStages && !warp_wait(bar(kBarFree + s), (uint32_t)((i / kRgStages - 1) & 1))) ok = false;
       if (ok && lane == 0) {
         hdr[s].end = 1;
-        mbar_arrive(bar(kBarFull + s));
+        mbar_arrive(bar(kBarK + s));
       }
     }
     if (!ok) {
       if (lane == 0) give_up();
       // copies in flight land before the CTA leaves
-      for (int j = max(0, i - kRgStages); j < i; ++j)
-        if (!warp_wait(bar(kBarFull + j % kRgStages), (uint32_t)((j / kRgStages) & 1))) break;
+      for (int j = max(0, i - kRgStages); j < i; ++j) {
+        if (!warp_wait(bar(kBarK + j % kRgStages), (uint32_t)((j / kRgStages) & 1))) break;
+        if (!warp_wait(bar(kBarV + j % kRgStages), (uint32_t)((j / kRgStages) & 1))) break;
+      }
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
       uint32_t last_bar = 0, last_phase = 0;
-      bool ok = mbar_wait(bar(kBarQ), 0);
-      int i = 0;
-      auto pv = [&](int j) -> bool {
-        if (!mbar_wait(bar(kBarP + (j & 1)), (uint32_t)((j >> 1) & 1))) return false;
-        tc_fence_after();
-        const uint32_t vbase = sStage + (uint32_t)(j % kRgStages) * kRgStageBytes + kRgTileBytes;
-        const uint32_t pcol = tm + kColP + (uint32_t)(j & 1) * 64;
-#pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-          umma_f16_ts(tm + kColO, pcol + ks * 8, smem_desc(vbase + ks * 2048, kRgHalf, 1024, kSwizzle128), kIdescPV,
-                      j > 0 || ks > 0);
-        umma_commit(bar(kBarDone + j % kRgStages));
-        last_bar = bar(kBarDone + j % kRgStages);
-        last_phase = (uint32_t)((j / kRgStages) & 1);
-        return true;
-      };
-      while (ok) {
-        const int s = i % kRgStages;
-        if (!mbar_wait(bar(kBarFull + s), (uint32_t)((i / kRgStages) & 1))) {
-          ok = false;
-          break;
-        }
-        if (*reinterpret_cast<volatile int32_t*>(&hdr[s].end)) break;
-        tc_fence_after();
-        const uint32_t kbase = sStage + (uint32_t)s * kRgStageBytes;
-        const uint32_t sc = tm + kColS + (uint32_t)(i & 1) * 128;
+      auto qk = [&](int X, int i) {
+        const uint32_t kbase = sStage + (uint32_t)(i % kRgStages) * kRgStageBytes;
+        const uint32_t qbase = sQ + (uint32_t)X * kRgTileBytes;
+        const uint32_t sc = tm + kColS + (uint32_t)X * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (uint32_t)(ks >> 2) * kRgHalf + (uint32_t)(ks & 3) * 32;
-          umma_f16(sc, smem_desc(sQ + off, 16, 1024, kSwizzle128), smem_desc(kbase + off, 16, 1024, kSwizzle128),
+          umma_f16(sc, smem_desc(qbase + off, 16, 1024, kSwizzle128), smem_desc(kbase + off, 16, 1024, kSwizzle128),
                    kIdescQK, ks > 0);
         }
-        umma_commit(bar(kBarS + (i & 1)));
-        last_bar = bar(kBarS + (i & 1));
-        last_phase = (uint32_t)((i >> 1) & 1);
-        if (i > 0 && !pv(i - 1)) {
+        umma_commit(bar(kBarS + X));
+        last_bar = bar(kBarS + X);
+        last_phase = (uint32_t)(i & 1);
+      };
+      auto pv = [&](int X, int i) -> bool {
+        if (!mbar_wait(bar(kBarP + X), (uint32_t)(i & 1))) return false;
+        tc_fence_after();
+        const uint32_t vbase = sStage + (uint32_t)(i % kRgStages) * kRgStageBytes + kRgTileBytes;
+        const uint32_t pcol = tm + kColS + (uint32_t)X * 128;  // P_X over the first 64 columns of S_X
+        const uint32_t oc = tm + kColO + (uint32_t)X * 128;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_f16_ts(oc, pcol + ks * 8, smem_desc(vbase + ks * 2048, kRgHalf, 1024, kSwizzle128), kIdescPV,
+                      i > 0 || ks > 0);
+        umma_commit(bar(kBarO + X));
+        last_bar = bar(kBarO + X);
+        last_phase = (uint32_t)(i & 1);
+        return true;
+      };
+      // waits for tile i's K copy; false at the end of the unit (or on a give-up)
+      auto next_k = [&](int i, bool& ok) -> bool {
+        const int s = i % kRgStages;
+        if (!mbar_wait(bar(kBarK + s), (uint32_t)((i / kRgStages) & 1))) {
+          ok = false;
+          return false;
+        }
+        if (*reinterpret_cast<volatile int32_t*>(&hdr[s].end)) return false;
+        tc_fence_after();
+        return true;
+      };
+      bool ok = mbar_wait(bar(kBarQ), 0);
+      int i = 0;
+      bool more = ok && next_k(0, ok);
+      if (more) {
+        qk(0, 0);
+        qk(1, 0);
+      }
+      while (more && ok) {
+        const int s = i % kRgStages;
+        if (!mbar_wait(bar(kBarVR + s), (uint32_t)((i / kRgStages) & 1)) || !pv(0, i)) {
           ok = false;
           break;
         }
+        more = next_k(i + 1, ok);
+        if (!ok) break;
+        if (more) qk(0, i + 1);  // after PV_A(i), which reads P_A in these columns
+        if (!pv(1, i)) {
+          ok = false;
+          break;
+        }
+        umma_commit(bar(kBarFree + s));  // both P.V of tile i issued: its stage is free once they are done
+        last_bar = bar(kBarFree + s);
+        last_phase = (uint32_t)((i / kRgStages) & 1);
+        if (more) qk(1, i + 1);
         ++i;
       }
-      if (ok && i > 0) ok = pv(i - 1);
       if (!ok) {
         give_up();
         if (last_bar) mbar_wait(last_bar, last_phase);  // the tensor cores finish what was issued
@@ -476,71 +552,81 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax
-    const int quarter = warp & 3;
-    const int m = quarter * 32 + lane;  // accumulator row = TMEM lane
-    const int rl = m / G, hq = m % G;   // row of the group, query head of kv head h
+    // warp w serves accumulator rows 32 (w & 3) .. + 31 of tile X = (w - 2) / 4
+    // (the TMEM lanes its position in the warpgroup may access)
+    const int X = (warp - 2) >> 2, quarter = warp & 3;
+    const int m = quarter * 32 + lane;               // accumulator row = TMEM lane
+    const int rl = X * (R >> 1) + m / G, hq = m % G;  // row of the group, query head of kv head h
     const bool live = rl < gr.nrows;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t sc = tm + lane_off + kColS + (uint32_t)X * 128;
+    const uint32_t oc = tm + lane_off + kColO + (uint32_t)X * 128;
     {
-      // this row of Q, 128-byte-swizzled K-major (zeros past the group's rows)
+      // this row of Q into tile X, 128-byte-swizzled K-major (zeros past the group's rows)
       const uint4* src =
           live ? reinterpret_cast<const uint4*>(p.q + ((int64_t)(gr.row0 + rl) * p.nq + (int64_t)h * G + hq) * 256)
                : nullptr;
+      const uint32_t qb = sQ + (uint32_t)X * kRgTileBytes;
 #pragma unroll
       for (int c = 0; c < 16; ++c) {
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
         if (live) v = __ldg(src + c);
-        const uint32_t dst = sQ + (uint32_t)(c >> 3) * kRgHalf + (uint32_t)m * 128 + ((uint32_t)((c & 7) ^ (m & 7)) << 4);
+        if (p.scale_log2 < 0.f) {
+          v.x ^= 0x80008000u;
+          v.y ^= 0x80008000u;
+          v.z ^= 0x80008000u;
+          v.w ^= 0x80008000u;
+        }
+        const uint32_t dst = qb + (uint32_t)(c >> 3) * kRgHalf + (uint32_t)m * 128 + ((uint32_t)((c & 7) ^ (m & 7)) << 4);
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                      : "memory");
       }
       fence_proxy_async_smem();
       mbar_arrive(bar(kBarQ));
     }
+    // the softmax runs on raw scores times c = |scale log2(e)| (at least
+    // 1e-30, so a zero scale still gives -inf x c = -inf on masked keys); a
+    // negative scale is applied by negating Q, which is exact
+    const float c_log2 = fmaxf(fabsf(p.scale_log2), 1e-30f);
     float m_ref = -CUDART_INF_F, l = 0.f;
     int i = 0;
     bool ok = true;
     for (;;) {
       const int s = i % kRgStages;
-      if (!warp_wait(bar(kBarFull + s), (uint32_t)((i / kRgStages) & 1))) {
+      if (!warp_wait(bar(kBarK + s), (uint32_t)((i / kRgStages) & 1))) {
         ok = false;
         break;
       }
       if (*reinterpret_cast<volatile int32_t*>(&hdr[s].end)) break;
-      if (!warp_wait(bar(kBarS + (i & 1)), (uint32_t)((i >> 1) & 1))) {
+      if (!warp_wait(bar(kBarS + X), (uint32_t)(i & 1))) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float x[128];
-      const uint32_t sc = tm + lane_off + kColS + (uint32_t)(i & 1) * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(sc + c * 32, x + c * 32);
-      const uint4 mk = *reinterpret_cast<const uint4*>(&hdr[s].mask[rl < R ? rl : 0][0]);
+      const uint4 mk = *reinterpret_cast<const uint4*>(&hdr[s].mask[rl][0]);
       const uint32_t mw[4] = {mk.x, mk.y, mk.z, mk.w};
-      float mx = -CUDART_INF_F;
+      // One pass over S, half by half (keys 64 hf .. + 63): keys this row did
+      // not select read as -inf; the half's maximum over eight independent
+      // chains (raw scores; c >= 0); the reference moves when that maximum
+      // exceeds it by more than 2^8 (or there was none yet), rescaling O, the
+      // sum and, for the second half, the first half's P already in tensor
+      // memory; then p = 2^(c s - m) in one FFMA and one ex2 per key (masked
+      // keys: 0), written as bf16 pairs over columns 32 hf .. + 31 of S_X,
+      // which that half has read.
+      float sa[8];
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float v = ((mw[c] >> j) & 1u) ? x[c * 32 + j] * p.scale_log2 : -CUDART_INF_F;
-          x[c * 32 + j] = v;
-          mx = fmaxf(mx, v);
-        }
-      // lazy running maximum: move it only when this tile's maximum exceeds it by 2^8
-      const bool need = mx > m_ref + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float mnew = need ? mx : m_ref;
-        const float f = need ? (m_ref == -CUDART_INF_F ? 0.f : exp2_fast(m_ref - mnew)) : 1.f;
-        if (i > 0 && __any_sync(0xffffffffu, need && l > 0.f)) {
+      for (int k = 0; k < 8; ++k) sa[k] = 0.f;
+      auto move_ref = [&](float mxh, int hf) -> bool {
+        const bool need = mxh > m_ref + 8.f;
+        if (!__any_sync(0xffffffffu, need)) return true;
+        const bool seen = m_ref != -CUDART_INF_F;  // O holds nonzero terms only then
+        const float mnew = need ? mxh : m_ref;
+        const float f = need ? (seen ? exp2_fast(m_ref - mnew) : 0.f) : 1.f;
+        if (i > 0 && __any_sync(0xffffffffu, need && seen)) {
           // O holds every earlier tile once the previous P.V is done
-          if (!warp_wait(bar(kBarDone + (i - 1) % kRgStages), (uint32_t)(((i - 1) / kRgStages) & 1))) {
-            ok = false;
-            break;
-          }
+          if (!warp_wait(bar(kBarO + X), (uint32_t)((i - 1) & 1))) return false;
           tc_fence_after();
-          const uint32_t oc = tm + lane_off + kColO;
-#pragma unroll
+#pragma unroll 1
           for (int c = 0; c < 4; ++c) {
             float o[32];
             uint32_t w[32];
@@ -549,49 +635,68 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
             for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(o[j] * f);
             tmem_st32(oc + c * 32, w);
           }
-          tmem_wait_st();
         }
+        if (hf == 1 && __any_sync(0xffffffffu, need && seen)) {
+          // the first half's P was taken against the old reference
+          tmem_wait_st();
+          float pw[32];
+          uint32_t w[32];
+          tmem_ld32(sc, pw);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const uint32_t b = __float_as_uint(pw[j]);
+            w[j] = pack_bf16(__uint_as_float(b << 16) * f, __uint_as_float(b & 0xFFFF0000u) * f);
+          }
+          tmem_st32(sc, w);
+        }
+        tmem_wait_st();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sa[k] *= f;
         l *= f;
         m_ref = mnew;
-      }
-      const float mr = m_ref == -CUDART_INF_F ? 0.f : m_ref;
-      uint32_t pk[64];
-      float sum = 0.f;
+        return true;
+      };
+      auto half_pass = [&](int hf) -> bool {
+        const uint32_t w0 = mw[2 * hf], w1 = mw[2 * hf + 1];
+        float x[64];
+        tmem_ld64(sc + hf * 64, x);
+        float mxa[8];
 #pragma unroll
-      for (int j = 0; j < 64; ++j) {
-        const float p0 = exp2_fast(x[2 * j] - mr), p1 = exp2_fast(x[2 * j + 1] - mr);
-        sum += p0 + p1;
-        pk[j] = pack_bf16(p0, p1);
-      }
-      l += sum;
-      // P(i) goes where P(i - 2) was: that P.V must be done
-      if (i >= 2 && !warp_wait(bar(kBarDone + (i - 2) % kRgStages), (uint32_t)(((i - 2) / kRgStages) & 1))) {
+        for (int k = 0; k < 8; ++k) mxa[k] = -CUDART_INF_F;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          x[j] = (((j < 32 ? w0 : w1) >> (j & 31)) & 1u) ? x[j] : -CUDART_INF_F;
+          mxa[j & 7] = fmaxf(mxa[j & 7], x[j]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) mxa[k] = fmaxf(mxa[k], mxa[k + 4]);
+        const float mxr = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+        if (!move_ref(mxr == -CUDART_INF_F ? -CUDART_INF_F : mxr * c_log2, hf)) return false;
+        const float nm = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float p0 = exp2_fast(fmaf(x[2 * j], c_log2, nm)), p1 = exp2_fast(fmaf(x[2 * j + 1], c_log2, nm));
+          sa[(2 * j) & 7] += p0;
+          sa[(2 * j + 1) & 7] += p1;
+          pk[j] = pack_bf16(p0, p1);
+        }
+        tmem_st32(sc + hf * 32, pk);
+        return true;
+      };
+      if (!half_pass(0) || !half_pass(1)) {
         ok = false;
         break;
       }
-      const uint32_t pc = tm + lane_off + kColP + (uint32_t)(i & 1) * 64;
-      tmem_st32(pc, pk);
-      tmem_st32(pc + 32, pk + 32);
       tmem_wait_st();
-      // V rows of keys no row of the group selects (other positions, slots past
-      // the sequence) are zeroed, so 0 x non-finite never reaches O
-      if (!((hdr[s].any[m >> 5] >> (m & 31)) & 1u)) {
-        const uint32_t vrow = sStage + (uint32_t)s * kRgStageBytes + kRgTileBytes + (uint32_t)m * 128;
-#pragma unroll
-        for (int x2 = 0; x2 < 2; ++x2)
-#pragma unroll
-          for (int c = 0; c < 8; ++c)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(vrow + x2 * kRgHalf + c * 16), "r"(0u)
-                         : "memory");
-      }
-      fence_proxy_async_smem();
+      l += ((sa[0] + sa[1]) + (sa[2] + sa[3])) + ((sa[4] + sa[5]) + (sa[6] + sa[7]));
       tc_fence_before();
-      mbar_arrive(bar(kBarP + (i & 1)));
+      mbar_arrive(bar(kBarP + X));
       ++i;
     }
     // epilogue: O / l for this row (tiles i; zero when the row attended nothing)
     bool have = i > 0 && ok;
-    if (have && !warp_wait(bar(kBarDone + (i - 1) % kRgStages), (uint32_t)(((i - 1) / kRgStages) & 1))) {
+    if (have && !warp_wait(bar(kBarO + X), (uint32_t)((i - 1) & 1))) {
       ok = false;
       have = false;
     }
@@ -602,7 +707,7 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       float o[32];
-      if (__any_sync(0xffffffffu, have)) tmem_ld32(tm + lane_off + kColO + c * 32, o);
+      if (__any_sync(0xffffffffu, have)) tmem_ld32(oc + c * 32, o);
       if (!live) continue;
 #pragma unroll
       for (int j = 0; j < 32; ++j) o[j] = have ? o[j] * inv : 0.f;

@@ -251,3 +251,16 @@ def test_output_never_depends_on_page_placement():
     y.kv_lookup_table[:] = table
     bb = run(y, kernel=4)
     assert np.array_equal(a, bb)
+
+
+@pytest.mark.parametrize("factor", [-1.0, 0.0])
+def test_negative_and_zero_scale(factor):
+    """The kernel runs the softmax on raw scores times |scale log2(e)| and
+    applies a negative scale by negating Q (exact in BF16); a zero scale is a
+    uniform softmax over each row's own keys."""
+    x = CASES["g8_p64"].build()
+    x.scale = float(x.scale) * factor
+    ref = oracle.sparse_attention(x)
+    got = run(x, kernel=4)
+    assert_close(got, ref, f"scale x {factor}")
+    assert B.qsa_read_device_status(clear=True) == 0
