@@ -130,10 +130,14 @@ typedef enum qsa_status {
  * max_cache_length + max_prompt_length <= R * selection_width) run on the
  * row-group kernel: 2 R consecutive rows of a sequence share one CTA per kv
  * head, which loads the sequence's pages tile by tile once for all of them
- * and masks each row to its own positions.  It reads K and V at positions
- * some row of the group did not select (those scores are masked; those V
- * rows are zeroed before use), so a non-finite K or V there does not reach
- * the output.  Its workspace (one bitmap of max_cache_length +
+ * and masks each row to its own positions.  It reads K and V at every
+ * position of a tile some row of the group selects from.  Scores of keys a
+ * row did not select are masked, and V rows of keys no row of the group
+ * selects are zeroed before use, so a non-finite K anywhere, or a non-finite
+ * V at a position no row of the group selects, does not reach the output.  A
+ * non-finite V at a position another row of the same group selects does
+ * reach the rows that did not select it (as 0 x that value): for such caches
+ * force kernel 3 (qsa_options.kernel = 3).  Its workspace (one bitmap of max_cache_length +
  * max_prompt_length bits and one flag per row) comes from the same
  * per-stream workspace as split-K.  Rows that repeat a position, or whose
  * sequence is longer than the hints say, are served exactly by that

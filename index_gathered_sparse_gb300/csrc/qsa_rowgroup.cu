@@ -33,8 +33,9 @@
 //               and V (page 0 stands in for pages past the sequence or named
 //               by no page: none of their keys is selected), two stages with
 //               separate K and V arrivals; once a tile's V has landed it zeroes
-//               the V rows of keys no row of the group selects (so
-//               0 x non-finite never reaches O) before P.V may read them
+//               the V rows of keys no row of the group selects (so a
+//               non-finite value there cannot reach O as 0 x value) before
+//               P.V may read them
 //   warp 1      one thread issues the MMAs in the order
 //               QK_A(i) QK_B(i) PV_A(i) QK_A(i+1) PV_B(i) QK_B(i+1) ...,
 //               so each softmax warpgroup works while the tensor cores serve
@@ -343,7 +344,9 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
     int i = 0;
     bool ok = true;
     // Tile j's V has landed: zero the rows of keys no row of the group selects
-    // (lane l: keys l, l + 32, l + 64, l + 96), then let P.V read it.
+    // (lane l: keys l, l + 32, l + 64, l + 96), then let P.V read it.  (A
+    // non-finite V at a key another row of the group selects still reaches
+    // the rows that did not select it, as 0 x value.)
     auto finish_v = [&](int j) -> bool {
       const int sj = j % kRgStages;
       if (!warp_wait(bar(kBarV + sj), (uint32_t)((j / kRgStages) & 1))) return false;
