@@ -92,17 +92,42 @@ struct GroupInfo {
 };
 
 // Block-wide (every thread calls it): group gi of the call, where the rows of
-// sequence b form ceil(rows_b / R) groups of R consecutive rows, sequence by
-// sequence.  b < 0 when gi is past the last group.  `scratch` holds at least
-// blockDim.x / 32 + 2 words of shared memory.
-__device__ GroupInfo group_info(const Params& p, int gi, int R, int* scratch) {
+// sequence b form ceil(rows_b / R) groups of R consecutive rows.  Sequences
+// are numbered longest first (when batch <= blockDim.x; in sequence order
+// otherwise), so the CTAs with the most tiles start in the first waves and the
+// last wave holds short ones.  b < 0 when gi is past the last group.
+// `scratch` holds at least blockDim.x / 32 + 2 words of shared memory, `big`
+// 12 blockDim.x bytes (8-byte aligned).
+__device__ GroupInfo group_info(const Params& p, int gi, int R, int* scratch, unsigned char* big) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   int* found = scratch + nw;
   if (threadIdx.x == 0) found[0] = -1;
+  const bool longest_first = p.batch <= (int)blockDim.x;
+  int* ord = reinterpret_cast<int*>(big + 8 * blockDim.x);
+  if (longest_first) {
+    uint64_t* len = reinterpret_cast<uint64_t*>(big);
+    const int b = threadIdx.x;
+    uint64_t mine = 0;
+    if (b < p.batch) {
+      const uint32_t o0 = __ldg(p.row_offsets + b), o1 = __ldg(p.row_offsets + b + 1);
+      mine = (uint64_t)__ldg(p.cache_lengths + b) + (o1 > o0 ? (uint64_t)(o1 - o0) : 0u);
+      len[b] = mine;
+    }
+    __syncthreads();
+    if (b < p.batch) {
+      int rank = 0;  // sequences longer than b, or as long and earlier
+      for (int k = 0; k < p.batch; ++k) {
+        const uint64_t v = len[k];
+        rank += (v > mine || (v == mine && k < b)) ? 1 : 0;
+      }
+      ord[rank] = b;
+    }
+  }
   __syncthreads();
   int base = 0;
   for (int c0 = 0; c0 < p.batch; c0 += blockDim.x) {
-    const int b = c0 + (int)threadIdx.x;
+    const int t = c0 + (int)threadIdx.x;
+    const int b = t < p.batch ? (longest_first ? ord[t] : t) : p.batch;
     int ng = 0;
     if (b < p.batch) {
       const uint32_t o0 = __ldg(p.row_offsets + b), o1 = __ldg(p.row_offsets + b + 1);
@@ -285,7 +310,8 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
   const uint32_t sQ = smem_addr(smem), sStage = sQ + kRgStageOff;
   auto bar = [&](int k) { return smem_addr(&bars[k]); };
 
-  const GroupInfo gr = group_info(p, gi, R, reinterpret_cast<int*>(misc + 8));
+  // (the K/V stages are free scratch until the group is known)
+  const GroupInfo gr = group_info(p, gi, R, reinterpret_cast<int*>(misc + 8), smem + kRgStageOff);
   if (gr.b < 0) return;  // past the call's groups (the grid is sized for the most there can be)
   int flagged = 0;
   for (int i = tid; i < gr.nrows; i += blockDim.x) flagged |= __ldg(p.rg_flags + gr.row0 + i);
