@@ -195,12 +195,27 @@ __global__ void __launch_bounds__(256) rg_bitmap_kernel(const Params p) {
   uint32_t bad = 0;
   int dup = 0;
   const int32_t* idx = p.indices + (int64_t)r * p.W;
-  for (int j = threadIdx.x; j < ri.n; j += blockDim.x) {
+  // each thread a contiguous chunk of the list: bits of consecutive entries
+  // in one word are gathered in a register and set with one atomic (lists
+  // are usually sorted, with runs of adjacent positions); a bit already set,
+  // locally or in the bitmap, is a repeated position
+  const int chunk = (ri.n + (int)blockDim.x - 1) / (int)blockDim.x;
+  const int j0 = (int)threadIdx.x * chunk, j1 = min(ri.n, j0 + chunk);
+  int word = -1;
+  uint32_t acc = 0u;
+  for (int j = j0; j < j1; ++j) {
     const int32_t pos = __ldg(idx + j);
     if (logical_page(p, ri.kv_len, pos, bad) < 0) continue;
     const uint32_t bit = 1u << (pos & 31);
-    if (atomicOr(&bm[pos >> 5], bit) & bit) dup = 1;
+    if ((pos >> 5) != word) {
+      if (word >= 0 && (atomicOr(&bm[word], acc) & acc)) dup = 1;
+      word = pos >> 5;
+      acc = 0u;
+    }
+    if (acc & bit) dup = 1;
+    acc |= bit;
   }
+  if (word >= 0 && (atomicOr(&bm[word], acc) & acc)) dup = 1;
   dup = __syncthreads_or(dup);
   uint32_t* out = p.rg_bits + (int64_t)r * p.rg_capw;
   for (int w = threadIdx.x; w < words; w += blockDim.x) out[w] = bm[w];
