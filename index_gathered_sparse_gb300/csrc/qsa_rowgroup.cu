@@ -27,15 +27,17 @@
 //
 // CTA = (group of rows, kv head): R = 256 / group rows, whose 256 query
 // heads form two 128-row accumulator tiles A (the first R / 2 rows) and B
-// sharing every K/V tile.  10 warps:
+// sharing every K/V tile.  11 warps:
 //   warp 0      producer: the group's mask words of each tile from the bitmaps,
 //               empty tiles skipped, page-table lookups, TMA tile copies of K
 //               and V (page 0 stands in for pages past the sequence or named
 //               by no page: none of their keys is selected), two stages with
-//               separate K and V arrivals; once a tile's V has landed it zeroes
-//               the V rows of keys no row of the group selects (so a
-//               non-finite value there cannot reach O as 0 x value) before
-//               P.V may read them
+//               separate K and V arrivals
+//   warp 10     once a tile's V has landed, zeroes the V rows of keys no row
+//               of the group selects (so a non-finite value there cannot
+//               reach O as 0 x value) before P.V may read them; a non-finite
+//               V at a key another row of the group selects still reaches the
+//               rows that did not select it, as 0 x value
 //   warp 1      one thread issues the MMAs in the order
 //               QK_A(i) QK_B(i) PV_A(i) QK_A(i+1) PV_B(i) QK_B(i+1) ...,
 //               so each softmax warpgroup works while the tensor cores serve
@@ -55,7 +57,7 @@
 namespace qsa {
 namespace {
 
-constexpr int kRgThreads = 320;
+constexpr int kRgThreads = 352;
 constexpr int kRgStages = 2;
 constexpr uint32_t kRgHalf = 16384;           // 64 channels (128 B) x 128 rows, 128-byte swizzle
 constexpr uint32_t kRgTileBytes = 2 * kRgHalf;  // a Q tile, or one K or V tile
@@ -310,8 +312,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&x);
 }
 
-// 320 threads, one CTA per SM (its shared memory).  Ten warps put three on
-// two of the SM's four sub-partitions, whose register files hold 16 Ki
+// 352 threads, one CTA per SM (its shared memory).  Eleven warps put three on
+// three of the SM's four sub-partitions, whose register files hold 16 Ki
 // registers each: at most 168 registers a thread.
 __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -384,31 +386,6 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
     if (NT > 0) load_words(0, nxt);
     int i = 0;
     bool ok = true;
-    // Tile j's V has landed: zero the rows of keys no row of the group selects
-    // (lane l: keys l, l + 32, l + 64, l + 96), then let P.V read it.  (A
-    // non-finite V at a key another row of the group selects still reaches
-    // the rows that did not select it, as 0 x value.)
-    auto finish_v = [&](int j) -> bool {
-      const int sj = j % kRgStages;
-      if (!warp_wait(bar(kBarV + sj), (uint32_t)((j / kRgStages) & 1))) return false;
-      const uint32_t vt = sStage + (uint32_t)sj * kRgStageBytes + kRgTileBytes;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        const int k = lane + 32 * c;
-        if ((hdr[sj].any[c] >> lane) & 1u) continue;
-#pragma unroll
-        for (int x2 = 0; x2 < 2; ++x2)
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + x2 * kRgHalf + (uint32_t)k * 128 + q * 16),
-                         "r"(0u)
-                         : "memory");
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kBarVR + sj));
-      return true;
-    };
     for (int t = 0; t < NT && ok; ++t) {
       uint32_t cur[8], o = 0u;
 #pragma unroll
@@ -418,10 +395,6 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
       }
       if (t + 1 < NT) load_words(t + 1, nxt);
       if (!__any_sync(0xffffffffu, o != 0u)) continue;
-      if (i > 0 && !finish_v(i - 1)) {
-        ok = false;
-        break;
-      }
       const int s = i % kRgStages;
       if (i >= kRgStages && !warp_wait(bar(kBarFree + s), (uint32_t)((i / kRgStages - 1) & 1))) {
         ok = false;
@@ -500,7 +473,6 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
       }
       ++i;
     }
-    if (ok && i > 0 && !finish_v(i - 1)) ok = false;
     if (ok) {
       // end of the unit: a header with no copies, on the K barrier
       const int s = i % kRgStages;
@@ -517,6 +489,37 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         if (!warp_wait(bar(kBarK + j % kRgStages), (uint32_t)((j / kRgStages) & 1))) break;
         if (!warp_wait(bar(kBarV + j % kRgStages), (uint32_t)((j / kRgStages) & 1))) break;
       }
+    }
+  } else if (warp == 10) {
+    // V fix-up: once tile i's V has landed, zero the rows of keys no row of
+    // the group selects, then let P.V read it
+    for (int i = 0;; ++i) {
+      const int s = i % kRgStages;
+      if (!warp_wait(bar(kBarK + s), (uint32_t)((i / kRgStages) & 1))) {
+        if (lane == 0) give_up();
+        break;
+      }
+      if (*reinterpret_cast<volatile int32_t*>(&hdr[s].end)) break;
+      if (!warp_wait(bar(kBarV + s), (uint32_t)((i / kRgStages) & 1))) {
+        if (lane == 0) give_up();
+        break;
+      }
+      const uint32_t vt = sStage + (uint32_t)s * kRgStageBytes + kRgTileBytes;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        const int k = lane + 32 * c;
+        if ((hdr[s].any[c] >> lane) & 1u) continue;
+#pragma unroll
+        for (int x2 = 0; x2 < 2; ++x2)
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};\n" ::"r"(vt + x2 * kRgHalf + (uint32_t)k * 128 + q * 16),
+                         "r"(0u)
+                         : "memory");
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kBarVR + s));
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
