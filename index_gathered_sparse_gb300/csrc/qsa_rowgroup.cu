@@ -382,8 +382,25 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         if (w < nw && row < gr.nrows && wi < words_valid) wv[k] = __ldg(bits + (int64_t)row * p.rg_capw + wi);
       }
     };
+    // table entry of page `lane` of tile t (in_seq: the page holds positions of
+    // the sequence and the table has it), fetched a tile ahead like the mask
+    // words so no dependent load stands between a free stage and its copies
+    auto load_page = [&](int t, uint32_t& e, bool& in_seq) {
+      e = 0u;
+      in_seq = false;
+      if (lane < np) {
+        const int64_t lp = (int64_t)t * 128 / p.P + (BR < 128 ? lane : 0);
+        in_seq = lp < p.max_pages && lp * p.P < gr.kv_len;
+        if (in_seq) e = __ldg(p.table + (int64_t)gr.b * p.max_pages + lp);
+      }
+    };
     uint32_t nxt[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-    if (NT > 0) load_words(0, nxt);
+    uint32_t pe_nxt = 0u;
+    bool pin_nxt = false;
+    if (NT > 0) {
+      load_words(0, nxt);
+      load_page(0, pe_nxt, pin_nxt);
+    }
     int i = 0;
     bool ok = true;
     for (int t = 0; t < NT && ok; ++t) {
@@ -393,7 +410,12 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         cur[k] = nxt[k];
         o |= cur[k];
       }
-      if (t + 1 < NT) load_words(t + 1, nxt);
+      const uint32_t pe = pe_nxt;
+      const bool pin = pin_nxt;
+      if (t + 1 < NT) {
+        load_words(t + 1, nxt);
+        load_page(t + 1, pe_nxt, pin_nxt);
+      }
       if (!__any_sync(0xffffffffu, o != 0u)) continue;
       const int s = i % kRgStages;
       if (i >= kRgStages && !warp_wait(bar(kBarFree + s), (uint32_t)((i / kRgStages - 1) & 1))) {
@@ -408,15 +430,11 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
       const int64_t pos0 = (int64_t)t * 128;
       int phys = 0;
       bool badpage = false;
-      if (lane < np) {
-        const int64_t lp = pos0 / p.P + (BR < 128 ? lane : 0);
-        if (lp < p.max_pages && lp * p.P < gr.kv_len) {
-          const uint32_t e = __ldg(p.table + (int64_t)gr.b * p.max_pages + lp);
-          if (e < p.num_pages)
-            phys = (int)e;
-          else
-            badpage = true;
-        }
+      if (pin) {
+        if (pe < p.num_pages)
+          phys = (int)pe;
+        else
+          badpage = true;
       }
       const uint32_t badm = __ballot_sync(0xffffffffu, badpage);
       if (badm) {
