@@ -45,8 +45,9 @@
 //   warps 2..5  softmax of tile A (one thread per accumulator row), warps
 //   6..9        of tile B: a lazy running maximum (O is rescaled only when a
 //               row's maximum grows by more than 2^8), one read of S per
-//               tile, P written back over the scores it replaces (keys 2j,
-//               2j + 1 in column j), and the output.
+//               tile (the second 64 columns load while the first are
+//               processed), P written back over the scores it replaces
+//               (keys 2j, 2j + 1 in column j), and the output.
 // Tensor memory: S_A, S_B (128 columns each, P_A / P_B in their first 64
 // columns as packed bf16 pairs), O_A, O_B (128 each) = 512 columns.  P_X(i)
 // overwrites S_X(i) after it is read, and QK_X(i+1) overwrites P_X(i) only
@@ -307,6 +308,19 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity) {
   return __all_sync(0xffffffffu, mbar_wait(bar, parity));
 }
 
+// 32 lanes x 64 columns of 32 bits, issued without its wait: the words are
+// the tile's only after tmem_wait_ld64 on the same array, whose operands tie
+// every later use of them to the wait
+__device__ __forceinline__ void tmem_ld64_issue(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld64(uint32_t (&r)[64]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31]), "+r"(r[32]), "+r"(r[33]), "+r"(r[34]), "+r"(r[35]), "+r"(r[36]), "+r"(r[37]), "+r"(r[38]), "+r"(r[39]), "+r"(r[40]), "+r"(r[41]), "+r"(r[42]), "+r"(r[43]), "+r"(r[44]), "+r"(r[45]), "+r"(r[46]), "+r"(r[47]), "+r"(r[48]), "+r"(r[49]), "+r"(r[50]), "+r"(r[51]), "+r"(r[52]), "+r"(r[53]), "+r"(r[54]), "+r"(r[55]), "+r"(r[56]), "+r"(r[57]), "+r"(r[58]), "+r"(r[59]), "+r"(r[60]), "+r"(r[61]), "+r"(r[62]), "+r"(r[63]) : : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   const __nv_bfloat162 x = __floats2bfloat162_rn(a, b);  // low half: a
   return *reinterpret_cast<const uint32_t*>(&x);
@@ -543,15 +557,22 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
     // ---------------------------------------------------------------- MMA issue
     if (lane == 0) {
       uint32_t last_bar = 0, last_phase = 0;
+      // descriptors of the tile bases, computed once: a step's descriptor
+      // adds its byte offset / 16 to the start-address field (bits 0..13),
+      // which cannot carry (shared addresses stay below 256 KB).  This thread
+      // shares its sub-partition with two softmax warps: the fewer
+      // instructions between its MMAs, the sooner the tensor pipe is fed.
+      const uint64_t dq0 = smem_desc(sQ, 16, 1024, kSwizzle128);
+      const uint64_t dk0 = smem_desc(sStage, 16, 1024, kSwizzle128);
+      const uint64_t dv0 = smem_desc(sStage + kRgTileBytes, kRgHalf, 1024, kSwizzle128);
       auto qk = [&](int X, int i) {
-        const uint32_t kbase = sStage + (uint32_t)(i % kRgStages) * kRgStageBytes;
-        const uint32_t qbase = sQ + (uint32_t)X * kRgTileBytes;
+        const uint64_t dk = dk0 + (uint64_t)((i % kRgStages) * (kRgStageBytes >> 4));
+        const uint64_t dq = dq0 + (uint64_t)(X * (kRgTileBytes >> 4));
         const uint32_t sc = tm + kColS + (uint32_t)X * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
-          const uint32_t off = (uint32_t)(ks >> 2) * kRgHalf + (uint32_t)(ks & 3) * 32;
-          umma_f16(sc, smem_desc(qbase + off, 16, 1024, kSwizzle128), smem_desc(kbase + off, 16, 1024, kSwizzle128),
-                   kIdescQK, ks > 0);
+          const uint32_t off16 = ((uint32_t)(ks >> 2) * kRgHalf + (uint32_t)(ks & 3) * 32) >> 4;
+          umma_f16(sc, dq + off16, dk + off16, kIdescQK, ks > 0);
         }
         umma_commit(bar(kBarS + X));
         last_bar = bar(kBarS + X);
@@ -560,13 +581,12 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
       auto pv = [&](int X, int i) -> bool {
         if (!mbar_wait(bar(kBarP + X), (uint32_t)(i & 1))) return false;
         tc_fence_after();
-        const uint32_t vbase = sStage + (uint32_t)(i % kRgStages) * kRgStageBytes + kRgTileBytes;
+        const uint64_t dv = dv0 + (uint64_t)((i % kRgStages) * (kRgStageBytes >> 4));
         const uint32_t pcol = tm + kColS + (uint32_t)X * 128;  // P_X over the first 64 columns of S_X
         const uint32_t oc = tm + kColO + (uint32_t)X * 128;
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          umma_f16_ts(oc, pcol + ks * 8, smem_desc(vbase + ks * 2048, kRgHalf, 1024, kSwizzle128), kIdescPV,
-                      i > 0 || ks > 0);
+          umma_f16_ts(oc, pcol + ks * 8, dv + (uint64_t)(ks * (2048 >> 4)), kIdescPV, i > 0 || ks > 0);
         umma_commit(bar(kBarO + X));
         last_bar = bar(kBarO + X);
         last_phase = (uint32_t)(i & 1);
@@ -692,27 +712,28 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
           if (!warp_wait(bar(kBarO + X), (uint32_t)((i - 1) & 1))) return false;
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            uint32_t w[32];
-            tmem_ld32(oc + c * 32, o);
+          for (int c = 0; c < 8; ++c) {  // 16 columns at a time: the scores stay live across it
+            float o[16];
+            tmem_ld16(oc + c * 16, o);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = __float_as_uint(o[j] * f);
-            tmem_st32(oc + c * 32, w);
+            for (int j = 0; j < 16; ++j) o[j] *= f;
+            tmem_st16(oc + c * 16, o);
           }
         }
         if (hf == 1 && __any_sync(0xffffffffu, need && seen)) {
           // the first half's P was taken against the old reference
           tmem_wait_st();
-          float pw[32];
-          uint32_t w[32];
-          tmem_ld32(sc, pw);
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {
+            float pw[16];
+            tmem_ld16(sc + c * 16, pw);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const uint32_t b = __float_as_uint(pw[j]);
-            w[j] = pack_bf16(__uint_as_float(b << 16) * f, __uint_as_float(b & 0xFFFF0000u) * f);
+            for (int j = 0; j < 16; ++j) {
+              const uint32_t b = __float_as_uint(pw[j]);
+              pw[j] = __uint_as_float(pack_bf16(__uint_as_float(b << 16) * f, __uint_as_float(b & 0xFFFF0000u) * f));
+            }
+            tmem_st16(sc + c * 16, pw);
           }
-          tmem_st32(sc, w);
         }
         tmem_wait_st();
 #pragma unroll
@@ -721,10 +742,11 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         m_ref = mnew;
         return true;
       };
-      auto half_pass = [&](int hf) -> bool {
+      auto half_pass = [&](int hf, const uint32_t (&xr)[64]) -> bool {
         const uint32_t w0 = mw[2 * hf], w1 = mw[2 * hf + 1];
         float x[64];
-        tmem_ld64(sc + hf * 64, x);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) x[j] = __uint_as_float(xr[j]);
         float mxa[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mxa[k] = -CUDART_INF_F;
@@ -738,18 +760,32 @@ __global__ void __launch_bounds__(kRgThreads, 1) rg_kernel(const __grid_constant
         const float mxr = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
         if (!move_ref(mxr == -CUDART_INF_F ? -CUDART_INF_F : mxr * c_log2, hf)) return false;
         const float nm = m_ref == -CUDART_INF_F ? 0.f : -m_ref;
-        uint32_t pk[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float p0 = exp2_fast(fmaf(x[2 * j], c_log2, nm)), p1 = exp2_fast(fmaf(x[2 * j + 1], c_log2, nm));
-          sa[(2 * j) & 7] += p0;
-          sa[(2 * j + 1) & 7] += p1;
-          pk[j] = pack_bf16(p0, p1);
+        for (int q = 0; q < 2; ++q) {  // 32 keys at a time, so x is consumed as P is stored
+          float pk[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float p0 = exp2_fast(fmaf(x[32 * q + 2 * j], c_log2, nm));
+            const float p1 = exp2_fast(fmaf(x[32 * q + 2 * j + 1], c_log2, nm));
+            sa[(2 * j) & 7] += p0;
+            sa[(2 * j + 1) & 7] += p1;
+            pk[j] = __uint_as_float(pack_bf16(p0, p1));
+          }
+          tmem_st16(sc + hf * 32 + 16 * q, pk);
         }
-        tmem_st32(sc + hf * 32, pk);
         return true;
       };
-      if (!half_pass(0) || !half_pass(1)) {
+      // the second half's scores load while the first half is processed
+      uint32_t xr0[64], xr1[64];
+      tmem_ld64_issue(sc, xr0);
+      tmem_wait_ld64(xr0);
+      tmem_ld64_issue(sc + 64, xr1);
+      if (!half_pass(0, xr0)) {
+        ok = false;
+        break;
+      }
+      tmem_wait_ld64(xr1);
+      if (!half_pass(1, xr1)) {
         ok = false;
         break;
       }
