@@ -253,6 +253,29 @@ def test_output_never_depends_on_page_placement():
     assert np.array_equal(a, bb)
 
 
+def test_reference_moves_within_and_across_tiles():
+    """Scores that climb by more than 2^8 (in base 2) every 16 positions: the
+    lazy reference maximum moves inside tiles (the first half's P, already in
+    tensor memory, is rescaled) and across tiles (O is rescaled), on every row;
+    results still match the oracle."""
+    x = CASES["g8_p64"].build()
+    P = x.kv_shape[3]
+    kv6 = x.kv_view()
+    kv_len = x.cache_lengths.astype(np.int64) + np.diff(x.input_row_offsets.astype(np.int64))
+    x.q[:] = wl.encode(np.full(x.q.shape, 0.5, np.float32), "bf16")
+    D, nkv = x.head_dim, x.num_kv_heads
+    for b in range(x.batch):
+        for pos in range(int(kv_len[b])):
+            # q.k = 64 (pos // 16): 8.16 more (base 2, scale 1/sqrt(128)) per step of 16
+            page = int(x.kv_lookup_table[b, pos // P])
+            kv6[page, 0, x.layer_idx, pos % P] = wl.encode(np.full((nkv, D), float(pos // 16), np.float32), "bf16")
+    assert abs(x.scale * 64 * np.log2(np.e) - 8.16) < 0.01
+    ref = oracle.sparse_attention(x)
+    got = run(x, kernel=4)
+    assert_close(got, ref, "climbing scores")
+    assert B.qsa_read_device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("factor", [-1.0, 0.0])
 def test_negative_and_zero_scale(factor):
     """The kernel runs the softmax on raw scores times |scale log2(e)| and
