@@ -127,7 +127,8 @@ typedef enum qsa_status {
  *
  * Prefill-like BF16 calls (head_dim 128, group 4, 8 or 16, a power-of-two
  * page_size >= 8, on average at least R = 128 / group rows per sequence and
- * max_cache_length + max_prompt_length <= R * selection_width) run on the
+ * max_cache_length + max_prompt_length <= (128 / min(group, 8)) *
+ * selection_width) run on the
  * row-group kernel: 2 R consecutive rows of a sequence share one CTA per kv
  * head, which loads the sequence's pages tile by tile once for all of them
  * and masks each row to its own positions.  It reads K and V at every

@@ -140,11 +140,15 @@ const char* rowgroup_unfit(const Resolved& R, int32_t group) {
 // sequences short enough that walking every position in tiles costs no more
 // than the rows' own selections: on average at least 128 / group rows per
 // sequence (half the rows of one of its CTAs), and a hinted longest sequence
-// of at most (128 / group) x selection_width positions.  Hints of zero read as "not given" (every
-// sequence would then take the kernel's slow exact path).
+// of at most 128 / min(group, 8) x selection_width positions (the gathering
+// kernels do more math per gathered byte as the group grows, so the bound
+// tightens with it up to group 8; at group 16 on chunked prefill, a longest
+// sequence of 9 x selection_width, kernel 4 still took 0.83 ms against
+// kernel 3's 1.96).  Hints of zero read as "not given" (every sequence would
+// then take the kernel's slow exact path).
 bool rowgroup_pays(const Resolved& R, int32_t group) {
-  const int64_t rows = 128 / group;
-  return R.hint_ctx > 0 && R.total_q >= rows * R.batch && R.hint_ctx <= rows * R.W;
+  const int64_t rows = 128 / group, span = 128 / std::min<int32_t>(group, 8);
+  return R.hint_ctx > 0 && R.total_q >= rows * R.batch && R.hint_ctx <= span * R.W;
 }
 
 // Picks the kernel for a resolved call: for BF16 and FP8 with head_dim 128

@@ -389,7 +389,8 @@ def test_rows_outside_every_sequence_are_zero_and_reported():
 # on sampled rows the oracle computes one by one
 # ---------------------------------------------------------------------------
 
-FULL = ["bf16_decode", "bf16_chunked_prefill", "bf16_long_decode", "fp8_mixed", "tiny_ragged_fp32"]
+FULL = ["bf16_decode", "bf16_chunked_prefill", "bf16_chunked_prefill_g4", "bf16_chunked_prefill_g16",
+        "bf16_long_decode", "fp8_mixed", "tiny_ragged_fp32"]
 
 
 @pytest.mark.parametrize("name", FULL)
