@@ -482,7 +482,7 @@ WORKLOADS = {
     # smaller device footprint for profiler captures
     "bf16_decode_1layer": lambda: bf16_decode(num_layers=1, layer_idx=0, name="bf16_decode_1layer"),
     "bf16_chunked_prefill": bf16_chunked_prefill,
-    # the same rows and selections with 4 and 16 query heads per kv head (the
+    # the same rows, counts and selection recipe with 4 and 16 query heads per kv head (the
     # row-group kernel's other group sizes): 32 q / 8 kv and 64 q / 4 kv
     "bf16_chunked_prefill_g4": lambda: dataclasses.replace(bf16_chunked_prefill(), name="bf16_chunked_prefill_g4",
                                                            num_q_heads=32),

@@ -6,6 +6,8 @@ import json
 import os
 import shutil
 
+import numpy as np
+
 import bench
 
 
@@ -92,3 +94,16 @@ def test_cpu_baseline_reports_threads_and_one_thread():
     assert cpu["kind"] == "oracle" and cpu["cores"] == 2 and cpu["value"] > 0
     assert cpu["one_thread"]["cores"] == 1 and cpu["one_thread"]["value"] > 0
     assert bench.host_cores() >= 1
+
+
+def test_group_variants_of_chunked_prefill():
+    """The group-4 and group-16 workloads keep the headline's rows, counts and
+    page tables (their random picks follow the changed head counts)."""
+    from index_gathered_sparse_gb300 import workloads as wl
+
+    base = wl.WORKLOADS["bf16_chunked_prefill"]().build()
+    for name, nq, nkv in (("bf16_chunked_prefill_g4", 32, 8), ("bf16_chunked_prefill_g16", 64, 4)):
+        x = wl.WORKLOADS[name]().build()
+        assert (x.num_q_heads, x.num_kv_heads, x.group) == (nq, nkv, nq // nkv)
+        assert np.array_equal(x.input_row_offsets, base.input_row_offsets)
+        assert np.array_equal(x.counts, base.counts) and np.array_equal(x.kv_lookup_table, base.kv_lookup_table)
