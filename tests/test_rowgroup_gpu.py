@@ -276,6 +276,21 @@ def test_reference_moves_within_and_across_tiles():
     assert B.qsa_read_device_status(clear=True) == 0
 
 
+def test_more_sequences_than_threads():
+    """400 sequences, more than the kernel's 352 threads: groups are numbered
+    in sequence order instead of longest first, and every row still matches."""
+    rows = tuple([17] * 400)
+    cache = tuple(int(c) for c in np.arange(400) % 61)
+    x = spec("many_seqs", 37, rows, cache, 64).build()
+    assert plan(x)["kernel"] == 4
+    sample = np.unique(np.linspace(0, x.total_q - 1, 40).astype(np.int64))
+    ref = oracle.sparse_attention(x, sample)
+    got = run(x, kernel=4)
+    assert_close(got[sample], ref, "400 sequences")
+    assert np.isfinite(got).all()
+    assert B.qsa_read_device_status(clear=True) == 0
+
+
 @pytest.mark.parametrize("factor", [-1.0, 0.0])
 def test_negative_and_zero_scale(factor):
     """The kernel runs the softmax on raw scores times |scale log2(e)| and
